@@ -1,0 +1,14 @@
+"""GB300 (sm_103a) weight-only-quantized skinny matmul: Q8_1 activation quantizer,
+Q4_0 x Q8_1 MMVQ, NVFP4 W4A16 and FP8 W8A16 at M = 1..8.
+
+The compute lives in the C-ABI CUDA library ``_build/libqmv.so`` (declared in
+``include/qmv.h``); this package is its thin Python binding. Seeded synthetic
+inputs are in ``gemm_qmv_quantize_gb300.synth``.
+"""
+from ._binding import (QmvError, QmvLibraryMissing, error_flags, lib, library_path, qgemm_fp8_w8a16,
+                       qgemm_nvfp4_w4a16, qmv_debug_q4_0_block_dots, qmv_q4_0_q8_1, qmv_quantize_q8_1,
+                       route_counts, route_reset)
+
+__all__ = ["QmvError", "QmvLibraryMissing", "error_flags", "lib", "library_path", "qgemm_fp8_w8a16",
+           "qgemm_nvfp4_w4a16", "qmv_debug_q4_0_block_dots", "qmv_q4_0_q8_1", "qmv_quantize_q8_1",
+           "route_counts", "route_reset"]

@@ -1,0 +1,182 @@
+"""ctypes binding of libqmv.so (include/qmv.h): argument marshalling only.
+
+Every function takes torch tensors on the current CUDA device, checks dtype,
+shape and contiguity, passes raw pointers and sizes to the C entry point of the
+same name, and raises ``QmvError`` on a non-zero status. All arithmetic runs in
+the library's CUDA kernels; there is no CPU path. If the library is missing the
+first call raises ``QmvLibraryMissing`` (build it with ``__graft_entry__.build()``
+or ``python -m gemm_qmv_quantize_gb300.build``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_build", "libqmv.so")
+_lock = threading.Lock()
+_lib = None
+
+QMV_OK = 0
+STATUS_NAMES = {0: "QMV_OK", -1: "QMV_ERR_NULL", -2: "QMV_ERR_SHAPE", -3: "QMV_ERR_ALIGN",
+                -4: "QMV_ERR_CUDA", -5: "QMV_ERR_TIMEOUT"}
+
+# name -> (restype, argtypes), mirroring include/qmv.h
+_vp, _i32, _i64, _f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float
+SIGNATURES = {
+    "qmv_status_string": (ctypes.c_char_p, [_i32]),
+    "qmv_quantize_q8_1": (_i32, [_vp, _vp, _i32, _i64, _vp]),
+    "qmv_q4_0_q8_1": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _vp]),
+    "qgemm_nvfp4_w4a16": (_i32, [_vp, _vp, _f32, _vp, _vp, _i32, _i64, _i64, _vp]),
+    "qgemm_fp8_w8a16": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _vp]),
+    "qmv_debug_q4_0_block_dots": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _vp]),
+    "qmv_route_count": (_i32, []),
+    "qmv_route_name": (ctypes.c_char_p, [_i32]),
+    "qmv_route_launches": (_i64, [_i32]),
+    "qmv_route_reset": (None, []),
+    "qmv_error_flags": (_i32, [ctypes.POINTER(ctypes.c_uint32), _i32]),
+}
+
+
+class QmvLibraryMissing(RuntimeError):
+    pass
+
+
+class QmvError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)} ({lib().qmv_status_string(status).decode()})")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """The loaded libqmv.so (loaded once; raises if it was never built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise QmvLibraryMissing(
+                    f"{_LIB_PATH} not found: build the CUDA library first "
+                    "(python -c 'import __graft_entry__ as g; g.build()')")
+            handle = ctypes.CDLL(_LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != QMV_OK:
+        raise QmvError(fn, status)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: expected shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def qmv_quantize_q8_1(x: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """fp32 [M, K] -> Q8_1 uint8 [M, K/32*36]."""
+    _need(x, "x", torch.float32)
+    M, K = x.shape
+    if out is None:
+        out = torch.empty((M, K // 32 * 36), dtype=torch.uint8, device=x.device)
+    _need(out, "out", torch.uint8, (M, K // 32 * 36))
+    _check("qmv_quantize_q8_1", lib().qmv_quantize_q8_1(x.data_ptr(), out.data_ptr(), M, K, _stream(stream)))
+    return out
+
+
+def qmv_q4_0_q8_1(w: torch.Tensor, xq: torch.Tensor, K: int, out: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """Q4_0 uint8 [N, K/32*18] x Q8_1 uint8 [M, K/32*36] -> fp32 [M, N]."""
+    N, M = w.shape[0], xq.shape[0]
+    _need(w, "w", torch.uint8, (N, K // 32 * 18))
+    _need(xq, "xq", torch.uint8, (M, K // 32 * 36))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=w.device)
+    _need(out, "out", torch.float32, (M, N))
+    _check("qmv_q4_0_q8_1", lib().qmv_q4_0_q8_1(w.data_ptr(), xq.data_ptr(), out.data_ptr(), M, N, K,
+                                                _stream(stream)))
+    return out
+
+
+def qmv_debug_q4_0_block_dots(w: torch.Tensor, xq: torch.Tensor, K: int, out: torch.Tensor | None = None,
+                              stream=None) -> torch.Tensor:
+    """int32 [M, N, K/32]: S - 8T per block, from the product kernel's device code."""
+    N, M = w.shape[0], xq.shape[0]
+    _need(w, "w", torch.uint8, (N, K // 32 * 18))
+    _need(xq, "xq", torch.uint8, (M, K // 32 * 36))
+    if out is None:
+        out = torch.empty((M, N, K // 32), dtype=torch.int32, device=w.device)
+    _need(out, "out", torch.int32, (M, N, K // 32))
+    _check("qmv_debug_q4_0_block_dots",
+           lib().qmv_debug_q4_0_block_dots(w.data_ptr(), xq.data_ptr(), out.data_ptr(), M, N, K, _stream(stream)))
+    return out
+
+
+def qgemm_nvfp4_w4a16(codes: torch.Tensor, scales: torch.Tensor, global_scale: float, x: torch.Tensor,
+                      out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """NVFP4 codes uint8 [N, K/2], E4M3 scales uint8 [N, K/16], x fp16 [M, K] -> fp32 [M, N]."""
+    _need(x, "x", torch.float16)
+    M, K = x.shape
+    N = codes.shape[0]
+    _need(codes, "codes", torch.uint8, (N, K // 2))
+    _need(scales, "scales", torch.uint8, (N, K // 16))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _need(out, "out", torch.float32, (M, N))
+    _check("qgemm_nvfp4_w4a16", lib().qgemm_nvfp4_w4a16(codes.data_ptr(), scales.data_ptr(), float(global_scale),
+                                                        x.data_ptr(), out.data_ptr(), M, N, K, _stream(stream)))
+    return out
+
+
+def qgemm_fp8_w8a16(w: torch.Tensor, row_scale: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None,
+                    stream=None) -> torch.Tensor:
+    """FP8 E4M3 uint8 [N, K], fp32 row scale [N], x fp16 [M, K] -> fp32 [M, N]."""
+    _need(x, "x", torch.float16)
+    M, K = x.shape
+    N = w.shape[0]
+    _need(w, "w", torch.uint8, (N, K))
+    _need(row_scale, "row_scale", torch.float32, (N,))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _need(out, "out", torch.float32, (M, N))
+    _check("qgemm_fp8_w8a16", lib().qgemm_fp8_w8a16(w.data_ptr(), row_scale.data_ptr(), x.data_ptr(),
+                                                    out.data_ptr(), M, N, K, _stream(stream)))
+    return out
+
+
+def route_counts() -> dict:
+    L = lib()
+    return {L.qmv_route_name(i).decode(): int(L.qmv_route_launches(i)) for i in range(L.qmv_route_count())}
+
+
+def route_reset() -> None:
+    lib().qmv_route_reset()
+
+
+def error_flags(clear: bool = False) -> int:
+    v = ctypes.c_uint32(0)
+    _check("qmv_error_flags", lib().qmv_error_flags(ctypes.byref(v), int(clear)))
+    return int(v.value)

@@ -1,0 +1,191 @@
+// abi.cu -- the C ABI of include/qmv.h: argument validation (before any CUDA
+// call), the per-(M, N, K) kernel choice, the route census and the error word.
+#include <atomic>
+#include <mutex>
+
+#include "qmv.h"
+#include "qmv_internal.h"
+
+namespace qmv {
+
+namespace {
+
+std::atomic<int64_t> g_route_launches[kRouteCount];
+
+constexpr const char *kRouteNames[kRouteCount] = {
+    "quantize_q8_1", "q4_0_stream_dp4a", "q4_0_generic", "nvfp4_mma_m16n8k16", "nvfp4_generic",
+    "fp8_mma_m16n8k16", "fp8_generic", "zero_fill",
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_valid[kMaxDevices];
+
+constexpr int64_t kMaxDim = 0x7fffffffLL;
+
+bool misaligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
+
+qmv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMV_OK : QMV_ERR_CUDA; }
+
+// Shared shape checks: M in 0..8, 0 <= N, K <= 2^31-1, K a multiple of `kblock`.
+qmv_status check_shape(int M, int64_t N, int64_t K, int64_t kblock)
+{
+    if (M < 0 || M > 8 || N < 0 || K < 0 || N > kMaxDim || K > kMaxDim) return QMV_ERR_SHAPE;
+    if (kblock > 1 && K % kblock != 0) return QMV_ERR_SHAPE;
+    return QMV_OK;
+}
+
+qmv_status zero_fill(float *y, int M, int64_t N, cudaStream_t s)
+{
+    route_hit(kRouteZeroFill);
+    return from_cuda(cudaMemsetAsync(y, 0, static_cast<size_t>(M) * static_cast<size_t>(N) * sizeof(float), s));
+}
+
+}  // namespace
+
+const char *route_name(int r) { return (r >= 0 && r < kRouteCount) ? kRouteNames[r] : "unknown"; }
+
+void route_hit(Route r) { g_route_launches[r].fetch_add(1, std::memory_order_relaxed); }
+
+cudaError_t current_device_info(DeviceInfo *out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    if (!g_dev_valid[dev]) {
+        DeviceInfo d{};
+        d.device = dev;
+        if ((e = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+            return e;
+        if ((e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+            cudaSuccess)
+            return e;
+        g_dev[dev] = d;
+        g_dev_valid[dev] = true;
+    }
+    *out = g_dev[dev];
+    return cudaSuccess;
+}
+
+}  // namespace qmv
+
+using namespace qmv;
+
+extern "C" {
+
+const char *qmv_status_string(qmv_status status)
+{
+    switch (status) {
+    case QMV_OK: return "QMV_OK";
+    case QMV_ERR_NULL: return "QMV_ERR_NULL: a required pointer is NULL";
+    case QMV_ERR_SHAPE: return "QMV_ERR_SHAPE: M outside 0..8, a negative or oversized N/K, or K not a multiple of the block";
+    case QMV_ERR_ALIGN: return "QMV_ERR_ALIGN: a pointer is not aligned to its element type";
+    case QMV_ERR_CUDA: return "QMV_ERR_CUDA: a CUDA runtime call failed";
+    case QMV_ERR_TIMEOUT: return "QMV_ERR_TIMEOUT: a bounded device-side wait gave up";
+    default: return "unknown qmv status";
+    }
+}
+
+qmv_status qmv_quantize_q8_1(const float *x, void *xq, int M, int64_t K, qmv_stream_t stream)
+{
+    qmv_status st = check_shape(M, 1, K, 32);
+    if (st != QMV_OK) return st;
+    if (M == 0 || K == 0) return QMV_OK;
+    if (!x || !xq) return QMV_ERR_NULL;
+    if (misaligned(x, 4) || misaligned(xq, 4)) return QMV_ERR_ALIGN;
+    return from_cuda(launch_quantize_q8_1(x, xq, M, K, stream));
+}
+
+static qmv_status q4_0_common(const void *w, const void *xq, float *y, int32_t *dots, int M, int64_t N, int64_t K,
+                              qmv_stream_t stream)
+{
+    qmv_status st = check_shape(M, N, K, 32);
+    if (st != QMV_OK) return st;
+    if (M == 0 || N == 0) return QMV_OK;
+    if (!dots && !y) return QMV_ERR_NULL;
+    if (K == 0) return dots ? QMV_OK : zero_fill(y, M, N, stream);
+    if (!w || !xq) return QMV_ERR_NULL;
+    if (misaligned(w, 2) || misaligned(xq, 4) || misaligned(y, 4) || misaligned(dots, 4)) return QMV_ERR_ALIGN;
+    DeviceInfo dev;
+    cudaError_t e = current_device_info(&dev);
+    if (e != cudaSuccess) return QMV_ERR_CUDA;
+    Q4Plan plan;
+    if ((e = plan_q4_0(dev, w, xq, M, N, K, &plan)) != cudaSuccess) return QMV_ERR_CUDA;
+    return from_cuda(launch_q4_0(plan, w, xq, y, dots, M, N, K, stream));
+}
+
+qmv_status qmv_q4_0_q8_1(const void *w, const void *xq, float *y, int M, int64_t N, int64_t K, qmv_stream_t stream)
+{
+    return q4_0_common(w, xq, y, nullptr, M, N, K, stream);
+}
+
+qmv_status qmv_debug_q4_0_block_dots(const void *w, const void *xq, int32_t *dots, int M, int64_t N, int64_t K,
+                                     qmv_stream_t stream)
+{
+    if (!dots && M > 0 && N > 0 && K > 0) return QMV_ERR_NULL;
+    return q4_0_common(w, xq, nullptr, dots, M, N, K, stream);
+}
+
+qmv_status qgemm_nvfp4_w4a16(const uint8_t *codes, const uint8_t *scales_e4m3, float global_scale,
+                             const uint16_t *x, float *y, int M, int64_t N, int64_t K, qmv_stream_t stream)
+{
+    qmv_status st = check_shape(M, N, K, 16);
+    if (st != QMV_OK) return st;
+    if (M == 0 || N == 0) return QMV_OK;
+    if (!y) return QMV_ERR_NULL;
+    if (misaligned(y, 4)) return QMV_ERR_ALIGN;
+    if (K == 0) return zero_fill(y, M, N, stream);
+    if (!codes || !scales_e4m3 || !x) return QMV_ERR_NULL;
+    if (misaligned(x, 2)) return QMV_ERR_ALIGN;
+    DeviceInfo dev;
+    if (current_device_info(&dev) != cudaSuccess) return QMV_ERR_CUDA;
+    const Route r = plan_nvfp4(codes, scales_e4m3, x, K);
+    return from_cuda(launch_nvfp4(r, dev, codes, scales_e4m3, global_scale, x, y, M, N, K, stream));
+}
+
+qmv_status qgemm_fp8_w8a16(const uint8_t *w, const float *row_scale, const uint16_t *x, float *y, int M, int64_t N,
+                           int64_t K, qmv_stream_t stream)
+{
+    qmv_status st = check_shape(M, N, K, 1);
+    if (st != QMV_OK) return st;
+    if (M == 0 || N == 0) return QMV_OK;
+    if (!y) return QMV_ERR_NULL;
+    if (misaligned(y, 4)) return QMV_ERR_ALIGN;
+    if (K == 0) return zero_fill(y, M, N, stream);
+    if (!w || !row_scale || !x) return QMV_ERR_NULL;
+    if (misaligned(x, 2) || misaligned(row_scale, 4)) return QMV_ERR_ALIGN;
+    DeviceInfo dev;
+    if (current_device_info(&dev) != cudaSuccess) return QMV_ERR_CUDA;
+    const Route r = plan_fp8(w, x, K);
+    return from_cuda(launch_fp8(r, dev, w, row_scale, x, y, M, N, K, stream));
+}
+
+int qmv_route_count(void) { return kRouteCount; }
+
+const char *qmv_route_name(int route) { return route_name(route); }
+
+int64_t qmv_route_launches(int route)
+{
+    return (route >= 0 && route < kRouteCount) ? g_route_launches[route].load(std::memory_order_relaxed) : -1;
+}
+
+void qmv_route_reset(void)
+{
+    for (auto &c : g_route_launches) c.store(0, std::memory_order_relaxed);
+}
+
+qmv_status qmv_error_flags(uint32_t *flags, int clear)
+{
+    if (!flags) return QMV_ERR_NULL;
+    if (cudaDeviceSynchronize() != cudaSuccess) return QMV_ERR_CUDA;
+    uint32_t w = 0;
+    if (read_error_word_q4_0(&w, clear != 0) != cudaSuccess) return QMV_ERR_CUDA;
+    *flags = w;
+    return QMV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,157 @@
+/*
+ * qmv.h -- C ABI of the GB300 (sm_103a) weight-only-quantized skinny matmul library.
+ *
+ * The operations are the decode-time hot path of two systems described on the
+ * pages this library follows:
+ *  - "Machine Learning on NVIDIA CMP" (llama.cpp on throttled Ampere dies):
+ *    section "TL;DR" -- decode runs through MMVQ, the quantized mat x vec whose
+ *    inner loop is a 4-wide int8 dot with int32 accumulation (section "The DP2A
+ *    patch"), over Q4_0 weights (section "llama.cpp results", Llama-2-7B-Q4_0).
+ *  - "v100-skinny README": section "How QPN works" -- QPN2 (NVFP4 W4A16: e2m1
+ *    codes, an FP8 scale per 16 weights, a global scale) and QPN8 (FP8 e4m3
+ *    W8A16), weights decoded only in registers, fp16 activations; section
+ *    "Native mixed-precision checkpoint path" -- per-region dispatch at M = 1..8.
+ *
+ * Conventions shared by every entry point
+ *  - Pointers to weights, activations and outputs are DEVICE pointers on the
+ *    current CUDA device, owned by the caller. The library allocates no memory
+ *    and keeps no per-call state; it never frees or retains a pointer.
+ *  - All arrays are row-major and little-endian. M is the number of activation
+ *    rows (1..8), N the number of weight rows (outputs per activation row), K the
+ *    reduction length. Outputs y are fp32 [M][N] and fully overwritten.
+ *  - Every call is asynchronous on `stream` (NULL = the legacy default stream)
+ *    and may be captured in a CUDA graph. Arguments are validated on the host
+ *    before any CUDA call; an invalid call returns an error and launches nothing.
+ *    Faults during execution surface at the caller's next synchronization.
+ *  - M == 0 or N == 0 is a valid empty call (nothing launched). K == 0 writes
+ *    zeros to y (an empty sum).
+ *  - Calls are thread-safe. Calls that write overlapping outputs must not run
+ *    concurrently.
+ */
+#ifndef QMV_H_
+#define QMV_H_
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QMV_API __attribute__((visibility("default")))
+#else
+#define QMV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared opaquely so C callers need no CUDA header. */
+typedef struct CUstream_st *qmv_stream_t;
+
+typedef int qmv_status;
+#define QMV_OK                0
+#define QMV_ERR_NULL         -1  /* a required pointer is NULL */
+#define QMV_ERR_SHAPE        -2  /* M outside 0..8, N or K negative, K not a multiple of the format's block */
+#define QMV_ERR_ALIGN        -3  /* a pointer is not aligned to its element type (see each call) */
+#define QMV_ERR_CUDA         -4  /* a CUDA runtime call failed (launch, attribute, device query) */
+#define QMV_ERR_TIMEOUT      -5  /* qmv_error_flags: a bounded device-side wait gave up */
+
+/* Human-readable name of a status code (static string, never NULL). */
+QMV_API const char *qmv_status_string(qmv_status status);
+
+/*
+ * fp32 -> Q8_1 activation quantizer.
+ * The pages name MMVQ's int8 activation operand (section "The DP2A patch",
+ * "Machine Learning on NVIDIA CMP") but not its format; this is llama.cpp's Q8_1
+ * block as this library defines it:
+ *   x   fp32 [M][K], K a multiple of 32, 4-byte aligned.
+ *   xq  M * (K/32) blocks of 36 bytes, [M][K/32] order, 4-byte aligned:
+ *       bytes 0..1 d8 (fp16), 2..3 s8 (fp16), 4..35 q[32] (int8).
+ *   Per block, in IEEE fp32 with round to nearest even: d = max|x_i| / 127;
+ *   q_i = d == 0 ? 0 : clamp(round_half_away_from_zero(x_i / d), -127, 127);
+ *   d8 = fp16(d); s8 = fp16(d * sum_i q_i). NaN/Inf inputs are outside the
+ *   contract; |x| above 127 * 65504 makes d8 infinite.
+ */
+QMV_API qmv_status qmv_quantize_q8_1(const float *x, void *xq, int M, int64_t K, qmv_stream_t stream);
+
+/*
+ * Q4_0 x Q8_1 mat-vec (MMVQ), M = 1..8 activation rows.
+ *   w   Q4_0 [N][K/32] blocks of 18 bytes: fp16 scale d4, then 16 bytes qs;
+ *       element j of the block is qs[j] & 15, element j+16 is qs[j] >> 4;
+ *       weight value d4 * (q - 8). 2-byte aligned (16-byte aligned and K a
+ *       multiple of 256 select the streaming kernel).
+ *   xq  Q8_1 [M][K/32] (as written by qmv_quantize_q8_1), 4-byte aligned.
+ *   y   fp32 [M][N]: y[m][n] = sum_b d4[n][b] * d8[m][b] * (S - 8 T), with the
+ *       exact integer block sums S = sum_j q4_j * q8_j and T = sum_j q8_j
+ *       ("The DP2A patch": 4-wide int8 dot, int32 accumulation).
+ *   K must be a multiple of 32.
+ */
+QMV_API qmv_status qmv_q4_0_q8_1(const void *w, const void *xq, float *y, int M, int64_t N, int64_t K,
+                         qmv_stream_t stream);
+
+/*
+ * NVFP4 W4A16 skinny GEMM ("v100-skinny README", section "How QPN works": QPN2).
+ *   codes        [N][K/2] bytes, two E2M1 codes per byte: k even in the low
+ *                nibble, k odd in the high nibble (OCP MX E2M1 values).
+ *   scales_e4m3  [N][K/16] bytes, one OCP E4M3 (FN) scale per 16 consecutive k.
+ *   global_scale per-tensor fp32 scale g.
+ *   x            fp16 [M][K] (IEEE binary16 bit patterns), 2-byte aligned.
+ *   y            fp32 [M][N]: y[m][n] = g * sum_k e2m1(c[n][k]) * e4m3(s[n][k/16]) * x[m][k],
+ *                accumulated in fp32 (no fp16 partial sums: the page's own fix for
+ *                fp16 overflow on activation outliers).
+ *   K must be a multiple of 16. codes, x 16-byte aligned and K a multiple of 256
+ *   select the tensor-core streaming kernel.
+ */
+QMV_API qmv_status qgemm_nvfp4_w4a16(const uint8_t *codes, const uint8_t *scales_e4m3, float global_scale,
+                             const uint16_t *x, float *y, int M, int64_t N, int64_t K,
+                             qmv_stream_t stream);
+
+/*
+ * FP8 E4M3 W8A16 skinny GEMM ("v100-skinny README", section "How QPN works": QPN8,
+ * one contiguous e4m3 byte stream).
+ *   w          [N][K] OCP E4M3 (FN) bytes.
+ *   row_scale  fp32 [N] per-output-row scale, 4-byte aligned.
+ *   x          fp16 [M][K], 2-byte aligned.
+ *   y          fp32 [M][N]: y[m][n] = row_scale[n] * sum_k e4m3(w[n][k]) * x[m][k],
+ *              accumulated in fp32.
+ *   Any K >= 0. w, x 16-byte aligned and K a multiple of 128 select the
+ *   tensor-core streaming kernel.
+ */
+QMV_API qmv_status qgemm_fp8_w8a16(const uint8_t *w, const float *row_scale, const uint16_t *x, float *y,
+                           int M, int64_t N, int64_t K, qmv_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Introspection (tests and benchmarks)
+ * ------------------------------------------------------------------------- */
+
+/*
+ * Offset-corrected integer block dots of qmv_q4_0_q8_1, computed by the same
+ * device code and the same kernel choice as the product call:
+ *   dots int32 [M][N][K/32], dots[m][n][b] = S - 8 T (see qmv_q4_0_q8_1).
+ * Pointers and alignment as in qmv_q4_0_q8_1.
+ */
+QMV_API qmv_status qmv_debug_q4_0_block_dots(const void *w, const void *xq, int32_t *dots, int M, int64_t N,
+                                     int64_t K, qmv_stream_t stream);
+
+/*
+ * Kernel-choice census: a counter per kernel route, bumped on every launch, so a
+ * caller can check which kernel served each region and that no fallback ran
+ * (the census of "v100-skinny README", "Native mixed-precision checkpoint path").
+ * Routes are numbered 0 .. qmv_route_count()-1; counts are cumulative since the
+ * last reset.
+ */
+QMV_API int qmv_route_count(void);
+QMV_API const char *qmv_route_name(int route);
+QMV_API int64_t qmv_route_launches(int route);
+QMV_API void qmv_route_reset(void);
+
+/*
+ * Device-side error word of the current device: bit flags set by kernels whose
+ * bounded waits gave up (they skip their work instead of hanging). Synchronizes
+ * the device. Returns QMV_OK and writes the word to *flags; clear=1 resets it.
+ */
+QMV_API qmv_status qmv_error_flags(uint32_t *flags, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMV_H_ */

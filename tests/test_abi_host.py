@@ -1,0 +1,148 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+- libqmv.so builds for sm_103a, loads, and exports every entry point that
+  include/*.h declares (and the binding's signature table matches the header).
+- Argument validation runs before any CUDA call: invalid shapes, NULL and
+  misaligned pointers return their status codes and launch nothing. Only
+  pointer values are passed (never dereferenced on the host).
+"""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from gemm_qmv_quantize_gb300 import build
+    build.build()
+    import gemm_qmv_quantize_gb300 as q
+    return q.lib()
+
+
+def _declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        with open(h) as f:
+            text = f.read()
+        names |= set(re.findall(r"QMV_API\s+[\w\s\*]+?\b(\w+)\s*\(", text))
+    return names
+
+
+def test_header_declares_the_four_entry_points():
+    names = _declared_symbols()
+    for n in ("qmv_quantize_q8_1", "qmv_q4_0_q8_1", "qgemm_nvfp4_w4a16", "qgemm_fp8_w8a16"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_binding_table_matches_header():
+    from gemm_qmv_quantize_gb300 import _binding
+    assert set(_binding.SIGNATURES) == _declared_symbols()
+
+
+def test_library_is_sm_103a(lib):
+    from gemm_qmv_quantize_gb300 import build
+    assert "arch=compute_103a,code=sm_103a" in build.ARCH
+
+
+OK, NULL, SHAPE, ALIGN = 0, -1, -2, -3
+P = 0x10000          # a 16-byte aligned fake pointer value (never dereferenced)
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, P, 1, 4096, None), NULL),
+    ((P, 0, 1, 4096, None), NULL),
+    ((P, P, 9, 4096, None), SHAPE),
+    ((P, P, -1, 4096, None), SHAPE),
+    ((P, P, 1, 4097, None), SHAPE),
+    ((P + 2, P, 1, 4096, None), ALIGN),
+    ((P, P + 1, 1, 4096, None), ALIGN),
+    ((0, 0, 0, 4096, None), OK),     # M == 0: empty call
+    ((0, 0, 1, 0, None), OK),        # K == 0: nothing to quantize
+])
+def test_quantize_validation(lib, args, status):
+    assert lib.qmv_quantize_q8_1(*args) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, P, P, 1, 64, 4096, None), NULL),
+    ((P, 0, P, 1, 64, 4096, None), NULL),
+    ((P, P, 0, 1, 64, 4096, None), NULL),
+    ((P, P, P, 9, 64, 4096, None), SHAPE),
+    ((P, P, P, 1, -5, 4096, None), SHAPE),
+    ((P, P, P, 1, 64, 4100, None), SHAPE),
+    ((P, P, P, 1, 1 << 32, 4096, None), SHAPE),
+    ((P + 1, P, P, 1, 64, 4096, None), ALIGN),
+    ((P, P + 2, P, 1, 64, 4096, None), ALIGN),
+    ((P, P, P + 2, 1, 64, 4096, None), ALIGN),
+    ((0, 0, 0, 1, 0, 4096, None), OK),    # N == 0
+    ((0, 0, 0, 0, 64, 4096, None), OK),   # M == 0
+])
+def test_q4_0_validation(lib, args, status):
+    assert lib.qmv_q4_0_q8_1(*args) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, P, 0.01, P, P, 1, 64, 512, None), NULL),
+    ((P, 0, 0.01, P, P, 1, 64, 512, None), NULL),
+    ((P, P, 0.01, 0, P, 1, 64, 512, None), NULL),
+    ((P, P, 0.01, P, 0, 1, 64, 512, None), NULL),
+    ((P, P, 0.01, P, P, 1, 64, 520, None), SHAPE),
+    ((P, P, 0.01, P, P, 10, 64, 512, None), SHAPE),
+    ((P, P, 0.01, P + 1, P, 1, 64, 512, None), ALIGN),
+    ((P, P, 0.01, P, P + 2, 1, 64, 512, None), ALIGN),
+    ((0, 0, 0.01, 0, 0, 1, 0, 512, None), OK),
+])
+def test_nvfp4_validation(lib, args, status):
+    assert lib.qgemm_nvfp4_w4a16(*args) == status
+
+
+@pytest.mark.parametrize("args,status", [
+    ((0, P, P, P, 1, 64, 512, None), NULL),
+    ((P, 0, P, P, 1, 64, 512, None), NULL),
+    ((P, P, 0, P, 1, 64, 512, None), NULL),
+    ((P, P, P, 0, 1, 64, 512, None), NULL),
+    ((P, P, P, P, 1, 64, -1, None), SHAPE),
+    ((P, P + 2, P, P, 1, 64, 512, None), ALIGN),
+    ((P, P, P + 1, P, 1, 64, 512, None), ALIGN),
+    ((P, P, P, P + 1, 1, 64, 512, None), ALIGN),
+])
+def test_fp8_validation(lib, args, status):
+    assert lib.qgemm_fp8_w8a16(*args) == status
+
+
+def test_debug_dots_validation(lib):
+    assert lib.qmv_debug_q4_0_block_dots(P, P, 0, 1, 64, 4096, None) == NULL
+    assert lib.qmv_debug_q4_0_block_dots(P, P, P, 9, 64, 4096, None) == SHAPE
+
+
+def test_status_strings_and_routes(lib):
+    for s in (OK, NULL, SHAPE, ALIGN, -4, -5, 123):
+        assert lib.qmv_status_string(s)
+    n = lib.qmv_route_count()
+    names = [lib.qmv_route_name(i).decode() for i in range(n)]
+    assert len(set(names)) == n and "q4_0_stream_dp4a" in names
+    lib.qmv_route_reset()
+    assert all(lib.qmv_route_launches(i) == 0 for i in range(n))
+    assert lib.qmv_route_launches(n) == -1
+
+
+def test_error_flags_null(lib):
+    assert lib.qmv_error_flags(None, 0) == NULL
+
+
+def test_binding_raises_loudly_when_library_missing(monkeypatch, tmp_path):
+    from gemm_qmv_quantize_gb300 import _binding
+    monkeypatch.setattr(_binding, "_LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_binding, "_lib", None)
+    with pytest.raises(_binding.QmvLibraryMissing):
+        _binding.lib()

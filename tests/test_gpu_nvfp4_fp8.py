@@ -1,0 +1,157 @@
+"""GPU parity: NVFP4 W4A16 and FP8 W8A16 skinny GEMM through the C ABI vs the CPU oracle.
+
+fp32 outputs within |y - y_ref| <= 1e-3 * sum|w*x| + 1e-6 on: several tiles with
+a ragged tail at M = 1..8; the full-size matrices of the 27B-class dense stack
+and its 151936-row lm_head (sampled rows); fp16 activation outliers up to
+6e4 (the overflow case of "v100-skinny README", section "How QPN works");
+zero scales; K that is not a multiple of the streaming step (generic kernel).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import assert_close
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def q():
+    from gemm_qmv_quantize_gb300 import build
+    build.build()
+    import gemm_qmv_quantize_gb300 as q
+    return q
+
+
+def _synth():
+    from gemm_qmv_quantize_gb300 import synth
+    return synth
+
+
+def _nvfp4(q, M, N, K, seed, outliers=0, rows=None, g=None):
+    synth = _synth()
+    codes, scales, g0 = synth.nvfp4_weights(N, K, seed=seed, device=DEV)
+    g = g0 if g is None else g
+    x = synth.activations_f16(M, K, seed=seed + 1, device=DEV, outliers=outliers)
+    y = q.qgemm_nvfp4_w4a16(codes, scales, g, x).cpu().numpy()
+    rows = np.arange(N) if rows is None else rows
+    y_ref, bound = oracle.nvfp4_w4a16(codes.cpu().numpy()[rows], scales.cpu().numpy()[rows], g, x.cpu().numpy())
+    assert_close(f"nvfp4 M={M} N={N} K={K}", y[:, rows], y_ref, bound)
+    return y
+
+
+def _fp8(q, M, N, K, seed, outliers=0, rows=None):
+    synth = _synth()
+    w, rs = synth.fp8_weights(N, K, seed=seed, device=DEV)
+    x = synth.activations_f16(M, K, seed=seed + 1, device=DEV, outliers=outliers)
+    y = q.qgemm_fp8_w8a16(w, rs, x).cpu().numpy()
+    rows = np.arange(N) if rows is None else rows
+    y_ref, bound = oracle.fp8_w8a16(w.cpu().numpy()[rows], rs.cpu().numpy()[rows], x.cpu().numpy())
+    assert_close(f"fp8 M={M} N={N} K={K}", y[:, rows], y_ref, bound)
+    return y
+
+
+@pytest.mark.parametrize("M", range(1, 9))
+def test_nvfp4_multi_tile_ragged(q, M):
+    q.route_reset()
+    _nvfp4(q, M, 16 * 37 + 5, 5120, seed=300 + M)
+    assert q.route_counts()["nvfp4_mma_m16n8k16"] == 1
+
+
+@pytest.mark.parametrize("M", range(1, 9))
+def test_fp8_multi_tile_ragged(q, M):
+    q.route_reset()
+    _fp8(q, M, 16 * 21 + 11, 5120, seed=400 + M)
+    assert q.route_counts()["fp8_mma_m16n8k16"] == 1
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 256), (3, 17, 512), (8, 16, 17408), (2, 100, 768)])
+def test_nvfp4_shapes(q, M, N, K):
+    _nvfp4(q, M, N, K, seed=N + K)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 128), (5, 40, 384), (8, 16, 17408), (2, 31, 1152)])
+def test_fp8_shapes(q, M, N, K):
+    _fp8(q, M, N, K, seed=N + K)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 33, 16), (4, 19, 80), (8, 40, 5136)])
+def test_nvfp4_generic_k(q, M, N, K):
+    q.route_reset()
+    _nvfp4(q, M, N, K, seed=K)
+    assert q.route_counts()["nvfp4_generic"] == 1
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 9, 1), (3, 21, 100), (8, 33, 5130)])
+def test_fp8_generic_k(q, M, N, K):
+    q.route_reset()
+    _fp8(q, M, N, K, seed=K)
+    assert q.route_counts()["fp8_generic"] == 1
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_outliers(q, M):
+    _nvfp4(q, M, 64, 5120, seed=9, outliers=8)
+    _fp8(q, M, 64, 5120, seed=10, outliers=8)
+
+
+@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("N,K", [(7168, 5120), (5120, 5120), (17408, 5120), (5120, 17408)])
+def test_nvfp4_27b_shapes_sampled(q, M, N, K):
+    rows = _synth().sample_rows(N, 64, seed=N + K).numpy()
+    _nvfp4(q, M, N, K, seed=N * 5 + K + M, rows=rows)
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_nvfp4_lm_head_sampled(q, M):
+    N, K = 151936, 5120
+    rows = _synth().sample_rows(N, 48, seed=M).numpy()
+    _nvfp4(q, M, N, K, seed=151936 + M, rows=rows)
+
+
+@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("N,K", [(7168, 5120), (5120, 5120)])
+def test_fp8_27b_attention_shapes_sampled(q, M, N, K):
+    rows = _synth().sample_rows(N, 64, seed=N + K + 1).numpy()
+    _fp8(q, M, N, K, seed=N * 3 + K + M, rows=rows)
+
+
+def test_zero_scales(q):
+    synth = _synth()
+    M, N, K = 3, 48, 2048
+    codes, scales, g = synth.nvfp4_weights(N, K, seed=1, device=DEV)
+    x = synth.activations_f16(M, K, seed=2, device=DEV)
+    scales[7] = 0
+    y = q.qgemm_nvfp4_w4a16(codes, scales, g, x)
+    assert torch.all(y[:, 7] == 0) and torch.any(y[:, 6] != 0)
+    assert torch.all(q.qgemm_nvfp4_w4a16(codes, scales, 0.0, x) == 0)
+    w, rs = synth.fp8_weights(N, K, seed=3, device=DEV)
+    rs[11] = 0.0
+    y = q.qgemm_fp8_w8a16(w, rs, x)
+    assert torch.all(y[:, 11] == 0)
+
+
+def test_unit_codes_closed_form(q):
+    """Every code 1.0, every scale 1.0, g = 1: y = sum_k x exactly up to fp32 rounding."""
+    M, N, K = 4, 32, 4096
+    codes = torch.full((N, K // 2), 0x22, dtype=torch.uint8, device=DEV)
+    scales = torch.full((N, K // 16), 0x38, dtype=torch.uint8, device=DEV)
+    x = _synth().activations_f16(M, K, seed=5, device=DEV)
+    y = q.qgemm_nvfp4_w4a16(codes, scales, 1.0, x).cpu().numpy()
+    ref = x.double().sum(dim=1, keepdim=True).expand(M, N).cpu().numpy()
+    bound = x.double().abs().sum(dim=1, keepdim=True).expand(M, N).cpu().numpy()
+    assert_close("nvfp4 unit codes", y, ref, bound)
+    w = torch.full((N, K), 0x38, dtype=torch.uint8, device=DEV)
+    y = q.qgemm_fp8_w8a16(w, torch.ones(N, device=DEV), x).cpu().numpy()
+    assert_close("fp8 unit codes", y, ref, bound)
+
+
+def test_k0_and_empty(q):
+    x = torch.zeros((2, 0), dtype=torch.float16, device=DEV)
+    y = q.qgemm_nvfp4_w4a16(torch.zeros((5, 0), dtype=torch.uint8, device=DEV),
+                            torch.zeros((5, 0), dtype=torch.uint8, device=DEV), 1.0, x)
+    assert y.shape == (2, 5) and torch.all(y == 0)
+    y = q.qgemm_fp8_w8a16(torch.zeros((5, 0), dtype=torch.uint8, device=DEV), torch.ones(5, device=DEV), x)
+    assert torch.all(y == 0)

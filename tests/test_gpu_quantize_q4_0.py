@@ -1,0 +1,194 @@
+"""GPU parity: Q8_1 quantizer and Q4_0 x Q8_1 MMVQ through the C ABI vs the CPU oracle.
+
+- Q8_1 bytes (d8, s8, q) identical to the oracle's.
+- Integer block sums S - 8T identical (qmv_debug_q4_0_block_dots runs the
+  product kernel's device code with the product kernel choice).
+- fp32 outputs within |y - y_ref| <= 1e-3 * sum|w*x| + 1e-6.
+Shapes span several tiles with a ragged tail, M = 1..8, the streaming and the
+generic kernels, and the full-size matrices of the Llama-2-7B and Llama-3-8B
+shaped workloads (sampled rows).
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from conftest import GOLDEN
+from gpu_util import assert_close
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def q():
+    from gemm_qmv_quantize_gb300 import build
+    build.build()
+    import gemm_qmv_quantize_gb300 as q
+    return q
+
+
+def _synth():
+    from gemm_qmv_quantize_gb300 import synth
+    return synth
+
+
+# ---------------------------------------------------------------- quantizer
+
+@pytest.mark.parametrize("M,K", [(1, 32), (1, 4096), (3, 11008), (8, 14336), (2, 4128)])
+def test_quantize_bytes_exact(q, M, K):
+    x = _synth().activations_f32(M, K, seed=M * 7 + K, device=DEV)
+    x[0, :32] *= 1e-30        # subnormal-range scale
+    if K >= 64:
+        x[0, 32:64] = 0.0     # all-zero block
+    xq = q.qmv_quantize_q8_1(x)
+    ref = oracle.quantize_q8_1(x.cpu().numpy())
+    assert np.array_equal(xq.cpu().numpy(), ref)
+
+
+def test_quantize_golden_blocks(q):
+    with open(os.path.join(GOLDEN, "q8_1_blocks.json")) as f:
+        cases = json.load(f)["cases"]
+    by = {c["name"]: c for c in cases}
+    rows = []
+    for c in cases:
+        x = np.array(c["x"] if "x" in c else by[c["x_from"]]["x"], dtype=np.float32)
+        if "x_scale" in c:
+            x = x * np.float32(c["x_scale"])
+        rows.append(x)
+    x = torch.from_numpy(np.concatenate(rows)[None, :]).to(DEV)
+    xq = q.qmv_quantize_q8_1(x).cpu().numpy().reshape(-1, 36)
+    for i, c in enumerate(cases):
+        d8 = int(xq[i, 0]) | int(xq[i, 1]) << 8
+        s8 = int(xq[i, 2]) | int(xq[i, 3]) << 8
+        assert list(xq[i, 4:].view(np.int8)) == c["q"], c["name"]
+        assert d8 == int(c["d8"], 16) and s8 == int(c["s8"], 16), c["name"]
+
+
+def test_quantize_ties_and_extremes(q):
+    """Elements landing exactly on k + 1/2 after the division, and large magnitudes."""
+    K = 32 * 64
+    rng = np.random.default_rng(3)
+    x = np.empty((2, K), np.float32)
+    for b in range(64):
+        blk = (rng.integers(-254, 255, 32) / 2.0).astype(np.float32)   # multiples of 1/2
+        blk[0] = 127.0                                                  # d = 1 -> ties at .5
+        x[0, 32 * b:32 * (b + 1)] = blk * np.float32(2.0 ** (b % 9 - 4))
+    x[1] = (rng.standard_normal(K) * 1e5).astype(np.float32)
+    xt = torch.from_numpy(x).to(DEV)
+    assert np.array_equal(q.qmv_quantize_q8_1(xt).cpu().numpy(), oracle.quantize_q8_1(x))
+
+
+# ---------------------------------------------------------------- Q4_0 MMVQ
+
+def _q4_case(q, M, N, K, seed, offset=0):
+    synth = _synth()
+    w = synth.q4_0_weights(N, K, seed=seed, device=DEV)
+    if offset:
+        # same bytes at a 2-byte (not 16-byte) aligned address: the generic kernel
+        buf = torch.empty(w.numel() + 16, dtype=torch.uint8, device=DEV)
+        buf[offset:offset + w.numel()] = w.view(-1)
+        w = buf[offset:offset + w.numel()].view(N, -1)
+    x = synth.activations_f32(M, K, seed=seed + 1, device=DEV)
+    xq = q.qmv_quantize_q8_1(x)
+    return w, xq
+
+
+def _check_q4(q, M, N, K, seed, offset=0, full=True, rows=None):
+    w, xq = _q4_case(q, M, N, K, seed, offset)
+    if offset:
+        from gemm_qmv_quantize_gb300 import _binding
+        y = torch.empty((M, N), dtype=torch.float32, device=DEV)
+        dots = torch.empty((M, N, K // 32), dtype=torch.int32, device=DEV)
+        L = _binding.lib()
+        s = torch.cuda.current_stream().cuda_stream
+        assert L.qmv_q4_0_q8_1(w.data_ptr(), xq.data_ptr(), y.data_ptr(), M, N, K, s) == 0
+        assert L.qmv_debug_q4_0_block_dots(w.data_ptr(), xq.data_ptr(), dots.data_ptr(), M, N, K, s) == 0
+    else:
+        y = q.qmv_q4_0_q8_1(w, xq, K)
+        dots = q.qmv_debug_q4_0_block_dots(w, xq, K)
+    torch.cuda.synchronize()
+    wn = w.cpu().numpy()
+    xqn = xq.cpu().numpy()
+    if rows is None:
+        rows = np.arange(N)
+    S, T = oracle.q4_0_block_dots(np.ascontiguousarray(wn[rows]), xqn, K)
+    assert np.array_equal(dots.cpu().numpy()[:, rows, :], S - 8 * T[:, None, :]), "integer block sums"
+    y_ref, bound = oracle.q4_0_q8_1(np.ascontiguousarray(wn[rows]), xqn, K)
+    assert_close(f"q4_0 M={M} N={N} K={K}", y.cpu().numpy()[:, rows], y_ref, bound)
+
+
+@pytest.mark.parametrize("M", range(1, 9))
+def test_q4_0_multi_tile_ragged(q, M):
+    _check_q4(q, M, 1000 + M, 4096, seed=100 + M)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 1, 256), (2, 37, 256), (1, 5, 512), (3, 300, 11008), (8, 130, 14336),
+                                   (1, 2049, 768)])
+def test_q4_0_shapes(q, M, N, K):
+    _check_q4(q, M, N, K, seed=N + K)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 33, 96), (4, 70, 4128), (8, 9, 32)])
+def test_q4_0_generic_k(q, M, N, K):
+    q.route_reset()
+    _check_q4(q, M, N, K, seed=K)
+    assert q.route_counts()["q4_0_generic"] > 0
+
+
+def test_q4_0_unaligned_rows_use_generic_kernel(q):
+    q.route_reset()
+    _check_q4(q, 2, 200, 4096, seed=5, offset=2)
+    rc = q.route_counts()
+    assert rc["q4_0_generic"] == 2 and rc["q4_0_stream_dp4a"] == 0
+
+
+def test_q4_0_full_4096_square(q):
+    """The small single-matrix workload: M = 1, N = K = 4096, every output checked."""
+    q.route_reset()
+    _check_q4(q, 1, 4096, 4096, seed=2024)
+    assert q.route_counts()["q4_0_stream_dp4a"] == 2
+
+
+@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("N,K", [(11008, 4096), (4096, 11008), (32000, 4096)])
+def test_q4_0_llama2_7b_shapes_sampled(q, M, N, K):
+    from gemm_qmv_quantize_gb300 import synth
+    rows = synth.sample_rows(N, 96, seed=N).numpy()
+    _check_q4(q, M, N, K, seed=N * 3 + K, rows=rows)
+
+
+@pytest.mark.parametrize("M", range(1, 9))
+@pytest.mark.parametrize("N,K", [(14336, 4096), (4096, 14336)])
+def test_q4_0_llama3_8b_mlp_sampled(q, M, N, K):
+    from gemm_qmv_quantize_gb300 import synth
+    rows = synth.sample_rows(N, 48, seed=N + M).numpy()
+    _check_q4(q, M, N, K, seed=N + 7 * K + M, rows=rows)
+
+
+def test_q4_0_special_weights(q):
+    """Zero scales give zero rows; all-8 nibbles give exact zeros."""
+    M, N, K = 2, 64, 4096
+    w, xq = _q4_case(q, M, N, K, seed=77)
+    blk = w.view(N, K // 32, 18)
+    blk[3, :, 0:2] = 0
+    blk[5, :, 2:] = 0x88
+    y = q.qmv_q4_0_q8_1(w, xq, K).cpu().numpy()
+    assert np.all(y[:, 3] == 0.0) and np.all(y[:, 5] == 0.0)
+
+
+def test_q4_0_empty_and_k0(q):
+    x = torch.zeros((1, 0), dtype=torch.float32, device=DEV)
+    w = torch.zeros((4, 0), dtype=torch.uint8, device=DEV)
+    xq = torch.zeros((1, 0), dtype=torch.uint8, device=DEV)
+    assert q.qmv_quantize_q8_1(x).numel() == 0
+    y = torch.full((1, 4), 7.0, device=DEV)
+    q.qmv_q4_0_q8_1(w, xq, 0, out=y)
+    assert torch.all(y == 0)
+    w0 = torch.zeros((0, 4096 // 32 * 18), dtype=torch.uint8, device=DEV)
+    xq0 = torch.zeros((1, 4096 // 32 * 36), dtype=torch.uint8, device=DEV)
+    assert q.qmv_q4_0_q8_1(w0, xq0, 4096).shape == (1, 0)
