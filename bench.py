@@ -1,0 +1,654 @@
+#!/usr/bin/env python3
+"""Benchmark of the weight-only-quantized skinny matmul hot path on GB300.
+
+Default workload: the Llama-2-7B-shaped Q4_0 decode stack at M = 1 -- 32 layers of
+{q, k, v, o 4096x4096; gate, up 11008x4096; down 4096x11008} plus the 32000x4096
+lm_head, 225 matrices, 3,716,481,024 bytes of Q4_0 weights, each call quantizing a
+fresh fp32 activation row to Q8_1 and running the Q4_0 x Q8_1 MMVQ ("Machine
+Learning on NVIDIA CMP", section "llama.cpp results": Llama-2-7B-Q4_0 decode). One
+step = one pass over the stack = one decoded token. Calls run in stream order
+(each waits for the previous one, as in decode), captured once in a CUDA graph.
+
+metric: achieved weight-stream GB/s (bytes = packed weights + scales + Q8_1
+activations + fp32 outputs, per step) and its fraction of the measured HBM copy
+bandwidth; tok/s equivalent = M / step time.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME] [--eager]
+Under torchrun every rank runs an independent replica (the path has no exchange
+step); the value is the units all ranks processed / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "achieved weight-stream GB/s and % of HBM roofline; equiv. decode tok/s (M=1..8)"
+FALLBACK_HBM_GBS = 6800.0
+Q4_0_BLOCK, Q8_1_BLOCK = 18, 36
+
+# ----------------------------------------------------------------------------- workloads
+
+
+def llama2_7b_stack():
+    layer = [(4096, 4096)] * 4 + [(11008, 4096)] * 2 + [(4096, 11008)]
+    return [("q4_0", n, k) for _ in range(32) for (n, k) in layer] + [("q4_0", 32000, 4096)]
+
+
+def llama2_7b_stages():
+    """Decode dependency structure: per layer {q, k, v} read the layer input, o reads
+    attention's output, {gate, up} read the MLP input, down reads their product;
+    then the lm_head. 129 dependent stages for 225 matrices."""
+    st = []
+    for layer in range(32):
+        b = 7 * layer
+        st += [[b, b + 1, b + 2], [b + 3], [b + 4, b + 5], [b + 6]]
+    return st + [[224]]
+
+
+def dense_27b_stack(mixed: bool):
+    """64 layers of {qkv 7168x5120, o 5120x5120, gate/up 17408x5120, down 5120x17408};
+    mixed: attention projections of layers 3, 7, ..., 63 in FP8, plus an NVFP4 lm_head."""
+    mats = []
+    for layer in range(64):
+        attn = "fp8" if (mixed and layer % 4 == 3) else "nvfp4"
+        mats += [(attn, 7168, 5120), (attn, 5120, 5120), ("nvfp4", 17408, 5120), ("nvfp4", 17408, 5120),
+                 ("nvfp4", 5120, 17408)]
+    if mixed:
+        mats.append(("nvfp4", 151936, 5120))
+    return mats
+
+
+def llama3_8b_mlp():
+    return [("q4_0", 14336, 4096), ("q4_0", 14336, 4096), ("q4_0", 4096, 14336)]
+
+
+WORKLOADS = {
+    "llama2_7b_q4_0_m1": dict(M=1, mats=llama2_7b_stack, stages=llama2_7b_stages,
+                             desc="Llama-2-7B-shaped Q4_0 decode stack, M=1 (225 matrices + per-call Q8_1 quantize)"),
+    "nvfp4_27b_m1": dict(M=1, mats=lambda: dense_27b_stack(False), desc="27B-class dense NVFP4 W4A16 stack, M=1"),
+    "nvfp4_27b_m8": dict(M=8, mats=lambda: dense_27b_stack(False), desc="27B-class dense NVFP4 W4A16 stack, M=8"),
+    "mixed_27b_m1": dict(M=1, mats=lambda: dense_27b_stack(True),
+                         desc="27B-class stack, FP8 attention every 4th layer + NVFP4 lm_head, M=1"),
+    "mixed_27b_m8": dict(M=8, mats=lambda: dense_27b_stack(True),
+                         desc="27B-class stack, FP8 attention every 4th layer + NVFP4 lm_head, M=8"),
+}
+for _m in range(1, 9):
+    WORKLOADS[f"llama3_8b_mlp_q4_0_m{_m}"] = dict(
+        M=_m, mats=llama3_8b_mlp, stages=lambda: [[0, 1], [2]],
+        desc=f"Llama-3-8B MLP Q4_0 (gate/up 14336x4096, down 4096x14336), M={_m}")
+# Single shapes, rotated through enough distinct copies (> 3x the 129 MB L2) that
+# every call streams from HBM: the small single-matrix case and per-kernel profiling.
+WORKLOADS["q4_0_4096sq_m1"] = dict(M=1, mats=lambda: [("q4_0", 4096, 4096)] * 48,
+                                   desc="Q4_0 GEMV M=1, N=K=4096, 48 rotated copies")
+WORKLOADS["q4_0_11008x4096_m1"] = dict(M=1, mats=lambda: [("q4_0", 11008, 4096)] * 16,
+                                       desc="Q4_0 GEMV M=1, 11008x4096, 16 rotated copies")
+for _m in (1, 8):
+    WORKLOADS[f"nvfp4_17408x5120_m{_m}"] = dict(M=_m, mats=lambda: [("nvfp4", 17408, 5120)] * 8,
+                                               desc=f"NVFP4 W4A16 17408x5120, M={_m}, 8 rotated copies")
+    WORKLOADS[f"fp8_7168x5120_m{_m}"] = dict(M=_m, mats=lambda: [("fp8", 7168, 5120)] * 12,
+                                            desc=f"FP8 W8A16 7168x5120, M={_m}, 12 rotated copies")
+DEFAULT_WORKLOAD = "llama2_7b_q4_0_m1"
+
+
+def weight_bytes(fmt, n, k):
+    if fmt == "q4_0":
+        return n * (k // 32) * Q4_0_BLOCK
+    if fmt == "nvfp4":
+        return n * k // 2 + n * k // 16
+    return n * k + 4 * n   # fp8 + fp32 row scale
+
+
+def call_bytes(fmt, M, n, k, fused=False):
+    """Algorithmic bytes of one call: weights + scales + activations + outputs.
+    Q4_0 reads Q8_1 activations, or fp32 ones when the quantize is fused in."""
+    if fmt == "q4_0":
+        act = M * k * 4 if fused else M * (k // 32) * Q8_1_BLOCK
+    else:
+        act = M * k * 2
+    return weight_bytes(fmt, n, k) + act + M * n * 4
+
+
+# ----------------------------------------------------------------------------- host-side plumbing
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"qmv_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu_index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.fh.close()
+
+    def summary(self):
+        try:
+            with open(self.path) as f:
+                rows = [[c.strip() for c in ln.split(",")] for ln in f if ln.strip()]
+            os.unlink(self.path)
+        except OSError:
+            rows = []
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def source_digest(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel's source
+    has not changed since the capture (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[kernel]
+        if e.get("workload") != workload or e.get("source_sha") != source_digest(e["sources"]):
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError, TypeError):
+        return None
+
+
+# ----------------------------------------------------------------------------- the GPU arm
+
+
+class Stack:
+    """Resident weights and per-call activation/output buffers of one workload."""
+
+    def __init__(self, name: str, device, seed: int = 1234, fused: bool = True, grouped: bool = True):
+        import torch
+        from gemm_qmv_quantize_gb300 import synth
+        w = WORKLOADS[name]
+        self.name, self.M, self.mats, self.device = name, w["M"], w["mats"](), device
+        self.fused = fused
+        # Dependent stages: matrices of a stage read the same input and are
+        # independent of each other; a grouped launch runs them together.
+        if grouped and fused and "stages" in w:
+            self.stages = w["stages"]()
+        else:
+            self.stages = [[i] for i in range(len(self.mats))]
+        assert sorted(i for st in self.stages for i in st) == list(range(len(self.mats)))
+        M = self.M
+        self.weights = []
+        for i, (fmt, n, k) in enumerate(self.mats):
+            s = seed * 100003 + i
+            if fmt == "q4_0":
+                self.weights.append((synth.q4_0_weights(n, k, s, device),))
+            elif fmt == "nvfp4":
+                self.weights.append(synth.nvfp4_weights(n, k, s, device))
+            else:
+                self.weights.append(synth.fp8_weights(n, k, s, device))
+        # activations and outputs: views into two contiguous buffers (one copy each way for e2e)
+        self.x_is_f32 = [fmt == "q4_0" for fmt, _, _ in self.mats]
+        x_elems = [M * k for _, _, k in self.mats]
+        self.x_bytes = sum(e * (4 if f else 2) for e, f in zip(x_elems, self.x_is_f32))
+        self.x_buf = torch.empty(self.x_bytes, dtype=torch.uint8, device=device)
+        self.xs, off = [], 0
+        for i, (fmt, n, k) in enumerate(self.mats):
+            nbytes = M * k * (4 if self.x_is_f32[i] else 2)
+            dt = torch.float32 if self.x_is_f32[i] else torch.float16
+            self.xs.append(self.x_buf[off:off + nbytes].view(dt).view(M, k))
+            off += nbytes
+        g = torch.Generator(device=device)
+        g.manual_seed(seed)
+        for x in self.xs:
+            x.copy_(torch.randn(x.shape, generator=g, device=device, dtype=torch.float32))
+        self.y_elems = sum(M * n for _, n, _ in self.mats)
+        self.y_buf = torch.empty(self.y_elems, dtype=torch.float32, device=device)
+        self.ys, off = [], 0
+        for _, n, _ in self.mats:
+            self.ys.append(self.y_buf[off:off + M * n].view(M, n))
+            off += M * n
+        self.xqs = [torch.empty((M, k // 32 * Q8_1_BLOCK), dtype=torch.uint8, device=device)
+                    if fmt == "q4_0" else None for fmt, _, k in self.mats]
+        self.bytes_per_step = sum(call_bytes(fmt, M, n, k, fused) for fmt, n, k in self.mats)
+        self.weight_bytes = sum(weight_bytes(fmt, n, k) for fmt, n, k in self.mats)
+
+    def run(self, events=None):
+        """One step: every stage in stream order. events[j] = (start, end) around
+        stage j's GEMV launch."""
+        import gemm_qmv_quantize_gb300 as q
+        for j, st in enumerate(self.stages):
+            if len(st) > 1:
+                if events is not None:
+                    events[j][0].record()
+                q.qmv_q4_0_q8_1_fused_group([self.weights[i][0] for i in st], [self.xs[i] for i in st],
+                                            [self.ys[i] for i in st])
+                if events is not None:
+                    events[j][1].record()
+                continue
+            self._run_one(st[0], None if events is None else events[j])
+
+    def _run_one(self, i, ev):
+        import gemm_qmv_quantize_gb300 as q
+        fmt, n, k = self.mats[i]
+        x, y, wt = self.xs[i], self.ys[i], self.weights[i]
+        if fmt == "q4_0" and not self.fused:
+            q.qmv_quantize_q8_1(x, out=self.xqs[i])
+        if ev is not None:
+            ev[0].record()
+        if fmt == "q4_0" and self.fused:
+            q.qmv_q4_0_q8_1_fused(wt[0], x, out=y)
+        elif fmt == "q4_0":
+            q.qmv_q4_0_q8_1(wt[0], self.xqs[i], k, out=y)
+        elif fmt == "nvfp4":
+            q.qgemm_nvfp4_w4a16(wt[0], wt[1], wt[2], x, out=y)
+        else:
+            q.qgemm_fp8_w8a16(wt[0], wt[1], x, out=y)
+        if ev is not None:
+            ev[1].record()
+
+    def kernels_per_step(self):
+        return sum(1 if len(st) > 1 else (2 if (self.mats[st[0]][0] == "q4_0" and not self.fused) else 1)
+                   for st in self.stages)
+
+
+def capture(fn, stream):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        fn()   # warm: attributes, lazy module loads
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def timed(replay, steps, barrier, sync):
+    import torch
+    barrier()
+    sync()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        replay()
+    end.record()
+    sync()
+    barrier()
+    return start.elapsed_time(end) * 1e-3
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import gemm_qmv_quantize_gb300 as q
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if dist is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    stack = Stack(args.workload, dev, seed=1234 + rank, fused=not args.unfused, grouped=not args.serial)
+    stream = torch.cuda.Stream(device=dev)
+    q.route_reset()
+    q.set_launch_overlap(not args.no_overlap)
+    with torch.cuda.stream(stream):
+        line = _run_ours_on_stream(args, rank, world, local_rank, stack, stream, barrier, max_over_ranks)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line if rank == 0 else None
+
+
+def _run_ours_on_stream(args, rank, world, local_rank, stack, stream, barrier, max_over_ranks):
+    import torch
+    import gemm_qmv_quantize_gb300 as q
+    if args.eager:
+        replay = stack.run
+    else:
+        graph = capture(stack.run, stream)
+        replay = graph.replay
+    for _ in range(args.warmup):
+        replay()
+    torch.cuda.synchronize()
+    launches0 = sum(q.route_counts().values())
+
+    with ClockSampler(local_rank) as clocks:
+        t_step_total = timed(replay, args.steps, barrier, torch.cuda.synchronize)
+    t = max_over_ranks(t_step_total)
+    ms_per_step = t / args.steps * 1e3
+    step_s = t / args.steps
+    gbs = stack.bytes_per_step * world / step_s / 1e9
+    kernels = stack.kernels_per_step() * args.steps if not args.eager else \
+        sum(q.route_counts().values()) - launches0
+
+    # dominant kernel: the GEMV of every call, timed per launch with event nodes in the graph
+    roof = kernel_roofline(args, stack, stream, barrier)
+
+    # end to end through the public API with host buffers: pinned x in, y out, every step
+    e2e = end_to_end(args, stack, replay, stream, barrier, max_over_ranks, world)
+
+    err = q.error_flags(clear=True)
+    peak, peak_kind = measured_peak()
+    line = {
+        "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(stack), "data": "synthetic",
+        "hbm_frac": round(gbs / world / peak, 4), "hbm_peak_gbs": peak, "hbm_peak_kind": peak_kind,
+        "tok_per_s": round(stack.M * world / step_s, 1),
+        "config": {"workload": stack.name, "desc": WORKLOADS[stack.name]["desc"], "M": stack.M,
+                   "matrices": len(stack.mats), "weight_bytes": stack.weight_bytes,
+                   "bytes_per_step": stack.bytes_per_step,
+                   "l2": "inputs larger than L2: every step streams all weights (> 129 MB)",
+                   "launch": "eager" if args.eager else "cuda_graph", "launch_overlap": not args.no_overlap,
+                   "q8_1_quantize": "two calls" if args.unfused else "fused into the MMVQ prologue",
+                   "dependent_stages": len(stack.stages),
+                   "schedule": ("one launch per matrix, each after the previous" if len(stack.stages) == len(stack.mats)
+                                else "decode dependency structure: matrices reading the same input share a launch"),
+                   "parallelism": f"replicas{world}"},
+        "roofline": roof, "e2e": e2e, "gpu_launches": int(kernels), "clocks": clocks.summary(),
+        "device_error_flags": err,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
+    return line
+
+
+def dtype_of(stack):
+    fmts = {f for f, _, _ in stack.mats}
+    if fmts == {"q4_0"}:
+        return "int8 dp4a (int32 block sums) + fp32 scale/accumulate"
+    return "fp16 x fp16 tensor-core MMA, fp32 accumulate (exact fp16 decode of e2m1/e4m3)"
+
+
+def kernel_roofline(args, stack, stream, barrier):
+    import torch
+    peak, peak_kind = measured_peak()
+    n = len(stack.stages)
+    try:
+        events = [(torch.cuda.Event(enable_timing=True, external=True),
+                   torch.cuda.Event(enable_timing=True, external=True)) for _ in range(n)]
+        graph = capture(lambda: stack.run(events), stream)
+        replay, how = graph.replay, "cuda_graph with event-record nodes"
+    except TypeError:   # no external events: time eager launches instead
+        events = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+
+        def replay():
+            stack.run(events)
+        how = "eager launches"
+    for _ in range(max(1, args.warmup)):
+        replay()
+    torch.cuda.synchronize()
+    steps = max(3, min(args.steps, 200))
+    total = [0.0] * n
+    barrier()
+    for _ in range(steps):
+        replay()
+        torch.cuda.synchronize()
+        for j, (a, b) in enumerate(events):
+            total[j] += a.elapsed_time(b) * 1e-3
+    barrier()
+    fmt_main = stack.mats[0][0]
+    kname = {"q4_0": "q4_0_stream_fused_quantize" if stack.fused else "q4_0_stream_dp4a",
+             "nvfp4": "nvfp4_mma_m16n8k16", "fp8": "fp8_mma_m16n8k16"}[fmt_main]
+    sel = [j for j, st in enumerate(stack.stages) if stack.mats[st[0]][0] == fmt_main]
+    stage_bytes = [sum(call_bytes(stack.mats[i][0], stack.M, stack.mats[i][1], stack.mats[i][2], stack.fused)
+                       for i in stack.stages[j]) for j in sel]
+    bytes_per_launch = sum(stage_bytes) / len(sel)
+    dur = sum(total[j] for j in sel) / (len(sel) * steps)
+    achieved = bytes_per_launch / dur / 1e9
+    return {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
+            "peak_kind": f"{peak_kind} (HBM copy bandwidth)", "unit": "GB/s", "frac": round(achieved / peak, 4),
+            "traffic": profiled_traffic(kname, stack.name), "bytes_per_launch": round(bytes_per_launch),
+            "avg_launch_us": round(dur * 1e6, 3), "launches_timed": len(sel) * steps, "timing": how}
+
+
+def end_to_end(args, stack, replay, stream, barrier, max_over_ranks, world):
+    import torch
+    x_host = torch.empty(stack.x_bytes, dtype=torch.uint8, pin_memory=True)
+    x_host.copy_(stack.x_buf.cpu())
+    y_host = torch.empty(stack.y_elems, dtype=torch.float32, pin_memory=True)
+    steps = args.steps
+
+    def one():   # all on the current stream (the bench stream)
+        stack.x_buf.copy_(x_host, non_blocking=True)
+        replay()
+        y_host.copy_(stack.y_buf, non_blocking=True)
+
+    for _ in range(args.warmup):
+        one()
+    torch.cuda.synchronize()
+    barrier()
+    t0 = time.perf_counter()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        one()
+    end.record()
+    torch.cuda.synchronize()
+    barrier()
+    t = max_over_ranks(max(start.elapsed_time(end) * 1e-3, 0.0))
+    return {"value": round(stack.bytes_per_step * world / (t / steps) / 1e9, 1), "unit": "GB/s",
+            "tok_per_s": round(stack.M * world / (t / steps), 1),
+            "h2d_bytes_per_step": stack.x_bytes, "d2h_bytes_per_step": stack.y_elems * 4,
+            "wall_s": round(time.perf_counter() - t0, 4)}
+
+
+# ----------------------------------------------------------------------------- the oracle (CPU) arm
+
+
+class OracleSampler:
+    """Times the CPU oracle on a bounded sample of a workload: for each distinct
+    matrix shape, the first rows of one seeded matrix with the same per-call work
+    (Q8_1 quantize of the activation + the dot products), the time budget split
+    across shapes in proportion to the stack's bytes. Inputs are generated once
+    (untimed) and reused by every sample."""
+
+    def __init__(self, workload: str, seed: int = 99):
+        w = WORKLOADS[workload]
+        self.M, mats = w["M"], w["mats"]()
+        self.shapes = sorted(set(mats), key=mats.index)
+        per_shape = {sh: sum(call_bytes(m[0], self.M, m[1], m[2]) for m in mats if m == sh) for sh in self.shapes}
+        total = sum(per_shape.values())
+        self.share = {sh: per_shape[sh] / total for sh in self.shapes}
+        self.seed = seed
+        self.cache = {}
+
+    def _inputs(self, shape, rows):
+        from gemm_qmv_quantize_gb300 import synth
+        fmt, n, k = shape
+        have = self.cache.get(shape)
+        if have is None or have[0] < rows:
+            r = min(n, max(rows, 2 * (have[0] if have else 0), 64))
+            if fmt == "q4_0":
+                w = (synth.q4_0_weights(r, k, self.seed, "cpu").numpy(),)
+                x = synth.activations_f32(self.M, k, self.seed + 1, "cpu").numpy()
+            elif fmt == "nvfp4":
+                c, sc, g = synth.nvfp4_weights(r, k, self.seed, "cpu")
+                w = (c.numpy(), sc.numpy(), g)
+                x = synth.activations_f16(self.M, k, self.seed + 1, "cpu").numpy()
+            else:
+                wt, rs = synth.fp8_weights(r, k, self.seed, "cpu")
+                w = (wt.numpy(), rs.numpy())
+                x = synth.activations_f16(self.M, k, self.seed + 1, "cpu").numpy()
+            self.cache[shape] = have = (r, w, x)
+        return have
+
+    def sample(self, budget_s: float):
+        import numpy as np
+
+        import oracle
+        done_bytes, done_time, rows_done = 0, 0.0, {}
+        for shape in self.shapes:
+            fmt, n, k = shape
+            rows, t_shape, key = 16, 0.0, f"{fmt} {n}x{k}"
+            rows_done[key] = 0
+            while t_shape < budget_s * self.share[shape] and rows_done[key] < n:
+                r = min(rows, n - rows_done[key])
+                _, w, x = self._inputs(shape, r)
+                if fmt == "q4_0":
+                    t0 = time.perf_counter()
+                    oracle.q4_0_q8_1(np.ascontiguousarray(w[0][:r]), oracle.quantize_q8_1(x), k)
+                elif fmt == "nvfp4":
+                    t0 = time.perf_counter()
+                    oracle.nvfp4_w4a16(np.ascontiguousarray(w[0][:r]), np.ascontiguousarray(w[1][:r]), w[2], x)
+                else:
+                    t0 = time.perf_counter()
+                    oracle.fp8_w8a16(np.ascontiguousarray(w[0][:r]), np.ascontiguousarray(w[1][:r]), x)
+                dt = time.perf_counter() - t0
+                # the sampled rows' weights and outputs, plus the activation once per call
+                act = self.M * (k // 32) * Q8_1_BLOCK if fmt == "q4_0" else self.M * k * 2
+                done_bytes += weight_bytes(fmt, r, k) + self.M * r * 4 + act
+                done_time += dt
+                t_shape += dt
+                rows_done[key] += r
+                rows = min(rows * 2, 2048)
+        sample = ("oracle (plain C, fp64, one thread) on the first rows of one seeded matrix per distinct shape, "
+                  f"time split by the stack's bytes per shape; rows per shape: {rows_done}")
+        return done_bytes / done_time / 1e9, {"bytes": done_bytes, "seconds": round(done_time, 3), "sample": sample}
+
+
+def cpu_sample(workload: str, budget_s: float):
+    return OracleSampler(workload).sample(budget_s)
+
+
+def cpu_baseline(workload: str, budget_s: float):
+    gbs, info = cpu_sample(workload, budget_s)
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": info["sample"],
+            "seconds": info["seconds"]}
+
+
+def run_reference(args, rank, world):
+    """The oracle as it stands, timed on this host's cores: each step is a bounded
+    sample of the workload; --ref-seconds is the budget of the whole run."""
+    if rank != 0:
+        return None
+    sampler = OracleSampler(args.workload)
+    budget = args.ref_seconds / max(1, args.steps + args.warmup)
+    for _ in range(args.warmup):
+        sampler.sample(budget)
+    vals, info = [], None
+    for _ in range(args.steps):
+        gbs, info = sampler.sample(budget)
+        vals.append(gbs)
+    value = statistics.mean(vals)
+    w = WORKLOADS[args.workload]
+    stack_bytes = sum(call_bytes(*m[:1], w["M"], *m[1:]) for m in w["mats"]())
+    step_s = stack_bytes / (value * 1e9)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic", "tok_per_s": round(w["M"] / step_s, 4),
+        "config": {"workload": args.workload, "desc": w["desc"], "M": w["M"]},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": info["sample"] if info else ""},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
+    p.add_argument("--eager", action="store_true", help="launch every call from Python (no CUDA graph)")
+    p.add_argument("--unfused", action="store_true",
+                   help="Q4_0: qmv_quantize_q8_1 + qmv_q4_0_q8_1 per call instead of the fused entry point")
+    p.add_argument("--serial", action="store_true",
+                   help="one launch per matrix in stream order (no grouped launches of independent matrices)")
+    p.add_argument("--no-overlap", action="store_true",
+                   help="no programmatic dependent launch between consecutive calls")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="time budget of the cpu_baseline sample")
+    p.add_argument("--ref-seconds", type=float, default=60.0,
+                   help="oracle time budget of the whole --impl reference run")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        if args.warmup < 3:
+            print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+        line = run_ours(args, rank, world, local_rank)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

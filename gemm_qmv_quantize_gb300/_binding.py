@@ -29,9 +29,14 @@ SIGNATURES = {
     "qmv_status_string": (ctypes.c_char_p, [_i32]),
     "qmv_quantize_q8_1": (_i32, [_vp, _vp, _i32, _i64, _vp]),
     "qmv_q4_0_q8_1": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _vp]),
+    "qmv_q4_0_q8_1_fused": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _vp]),
+    "qmv_q4_0_q8_1_fused_group": (_i32, [_i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                         ctypes.POINTER(_i64), _i32, _i64, _vp]),
     "qgemm_nvfp4_w4a16": (_i32, [_vp, _vp, _f32, _vp, _vp, _i32, _i64, _i64, _vp]),
     "qgemm_fp8_w8a16": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _vp]),
     "qmv_debug_q4_0_block_dots": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _vp]),
+    "qmv_set_launch_overlap": (None, [_i32]),
+    "qmv_get_launch_overlap": (_i32, []),
     "qmv_route_count": (_i32, []),
     "qmv_route_name": (ctypes.c_char_p, [_i32]),
     "qmv_route_launches": (_i64, [_i32]),
@@ -121,6 +126,43 @@ def qmv_q4_0_q8_1(w: torch.Tensor, xq: torch.Tensor, K: int, out: torch.Tensor |
     return out
 
 
+def qmv_q4_0_q8_1_fused(w: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """Q4_0 uint8 [N, K/32*18] x fp32 [M, K] (quantized to Q8_1 in-kernel) -> fp32 [M, N]."""
+    _need(x, "x", torch.float32)
+    M, K = x.shape
+    N = w.shape[0]
+    _need(w, "w", torch.uint8, (N, K // 32 * 18))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _need(out, "out", torch.float32, (M, N))
+    _check("qmv_q4_0_q8_1_fused", lib().qmv_q4_0_q8_1_fused(w.data_ptr(), x.data_ptr(), out.data_ptr(), M, N, K,
+                                                            _stream(stream)))
+    return out
+
+
+def qmv_q4_0_q8_1_fused_group(ws, xs, outs=None, stream=None):
+    """Several independent fused calls (same M, K) in one launch; returns the outputs."""
+    count = len(ws)
+    if count != len(xs) or not 1 <= count <= 8:
+        raise ValueError("need 1..8 matrices and as many activations")
+    M, K = xs[0].shape
+    Ns = [w.shape[0] for w in ws]
+    for i, (w, x) in enumerate(zip(ws, xs)):
+        _need(x, f"x[{i}]", torch.float32, (M, K))
+        _need(w, f"w[{i}]", torch.uint8, (Ns[i], K // 32 * 18))
+    if outs is None:
+        outs = [torch.empty((M, n), dtype=torch.float32, device=xs[0].device) for n in Ns]
+    for i, o in enumerate(outs):
+        _need(o, f"out[{i}]", torch.float32, (M, Ns[i]))
+    arr = ctypes.c_void_p * count
+    wp, xp, yp = arr(*[w.data_ptr() for w in ws]), arr(*[x.data_ptr() for x in xs]), arr(*[o.data_ptr() for o in outs])
+    npa = (ctypes.c_int64 * count)(*Ns)
+    _check("qmv_q4_0_q8_1_fused_group",
+           lib().qmv_q4_0_q8_1_fused_group(count, wp, xp, yp, npa, M, K, _stream(stream)))
+    return outs
+
+
 def qmv_debug_q4_0_block_dots(w: torch.Tensor, xq: torch.Tensor, K: int, out: torch.Tensor | None = None,
                               stream=None) -> torch.Tensor:
     """int32 [M, N, K/32]: S - 8T per block, from the product kernel's device code."""
@@ -165,6 +207,15 @@ def qgemm_fp8_w8a16(w: torch.Tensor, row_scale: torch.Tensor, x: torch.Tensor, o
     _check("qgemm_fp8_w8a16", lib().qgemm_fp8_w8a16(w.data_ptr(), row_scale.data_ptr(), x.data_ptr(),
                                                     out.data_ptr(), M, N, K, _stream(stream)))
     return out
+
+
+def set_launch_overlap(enable: bool) -> None:
+    """Programmatic dependent launch between consecutive calls (see qmv.h)."""
+    lib().qmv_set_launch_overlap(int(bool(enable)))
+
+
+def get_launch_overlap() -> bool:
+    return bool(lib().qmv_get_launch_overlap())
 
 
 def route_counts() -> dict:

@@ -1,6 +1,7 @@
 // abi.cu -- the C ABI of include/qmv.h: argument validation (before any CUDA
 // call), the per-(M, N, K) kernel choice, the route census and the error word.
 #include <atomic>
+#include <cstdlib>
 #include <mutex>
 
 #include "qmv.h"
@@ -13,7 +14,8 @@ namespace {
 std::atomic<int64_t> g_route_launches[kRouteCount];
 
 constexpr const char *kRouteNames[kRouteCount] = {
-    "quantize_q8_1", "q4_0_stream_dp4a", "q4_0_generic", "nvfp4_mma_m16n8k16", "nvfp4_generic",
+    "quantize_q8_1", "q4_0_stream_dp4a", "q4_0_generic", "q4_0_stream_fused_quantize", "nvfp4_mma_m16n8k16",
+    "nvfp4_generic",
     "fp8_mma_m16n8k16", "fp8_generic", "zero_fill",
 };
 
@@ -43,6 +45,60 @@ qmv_status zero_fill(float *y, int M, int64_t N, cudaStream_t s)
 }
 
 }  // namespace
+
+namespace {
+std::atomic<int> g_launch_overlap{0};
+
+struct SmemAttrEntry {
+    const void *kernel;
+    int device;
+    int bytes;
+};
+std::mutex g_attr_mutex;
+SmemAttrEntry g_attr_cache[256];
+int g_attr_count = 0;
+}  // namespace
+
+int env_int(const char *name, int fallback)
+{
+    const char *v = std::getenv(name);
+    if (!v || !*v) return fallback;
+    char *end = nullptr;
+    const long x = std::strtol(v, &end, 10);
+    return (end && *end == 0) ? static_cast<int>(x) : fallback;
+}
+
+int set_launch_overlap_attr(cudaLaunchAttribute *attr)
+{
+    if (!g_launch_overlap.load(std::memory_order_relaxed)) return 0;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    return 1;
+}
+
+cudaError_t ensure_smem_attr(const void *kernel, int bytes, int carveout)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_attr_mutex);
+    for (int i = 0; i < g_attr_count; ++i) {
+        SmemAttrEntry &c = g_attr_cache[i];
+        if (c.kernel == kernel && c.device == dev) {
+            if (c.bytes >= bytes) return cudaSuccess;
+            if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) == cudaSuccess)
+                c.bytes = bytes;
+            return e;
+        }
+    }
+    if ((e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes)) != cudaSuccess)
+        return e;
+    if (carveout >= 0 &&
+        (e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, carveout)) != cudaSuccess)
+        return e;
+    if (g_attr_count < 256) g_attr_cache[g_attr_count++] = SmemAttrEntry{kernel, dev, bytes};
+    return cudaSuccess;
+}
 
 const char *route_name(int r) { return (r >= 0 && r < kRouteCount) ? kRouteNames[r] : "unknown"; }
 
@@ -100,6 +156,18 @@ qmv_status qmv_quantize_q8_1(const float *x, void *xq, int M, int64_t K, qmv_str
     return from_cuda(launch_quantize_q8_1(x, xq, M, K, stream));
 }
 
+static Q4Group single_group(const void *w, const void *x, float *y, int64_t N)
+{
+    Q4Group g{};
+    g.count = 1;
+    g.w[0] = static_cast<const uint8_t *>(w);
+    g.x[0] = x;
+    g.y[0] = y;
+    g.row_start[0] = 0;
+    g.row_start[1] = N;
+    return g;
+}
+
 static qmv_status q4_0_common(const void *w, const void *xq, float *y, int32_t *dots, int M, int64_t N, int64_t K,
                               qmv_stream_t stream)
 {
@@ -113,9 +181,10 @@ static qmv_status q4_0_common(const void *w, const void *xq, float *y, int32_t *
     DeviceInfo dev;
     cudaError_t e = current_device_info(&dev);
     if (e != cudaSuccess) return QMV_ERR_CUDA;
+    const Q4Group grp = single_group(w, xq, y, N);
     Q4Plan plan;
-    if ((e = plan_q4_0(dev, w, xq, M, N, K, &plan)) != cudaSuccess) return QMV_ERR_CUDA;
-    return from_cuda(launch_q4_0(plan, w, xq, y, dots, M, N, K, stream));
+    if ((e = plan_q4_0(dev, grp, M, K, &plan)) != cudaSuccess) return QMV_ERR_CUDA;
+    return from_cuda(launch_q4_0(plan, grp, dots, M, K, false, stream));
 }
 
 qmv_status qmv_q4_0_q8_1(const void *w, const void *xq, float *y, int M, int64_t N, int64_t K, qmv_stream_t stream)
@@ -128,6 +197,55 @@ qmv_status qmv_debug_q4_0_block_dots(const void *w, const void *xq, int32_t *dot
 {
     if (!dots && M > 0 && N > 0 && K > 0) return QMV_ERR_NULL;
     return q4_0_common(w, xq, nullptr, dots, M, N, K, stream);
+}
+
+qmv_status qmv_q4_0_q8_1_fused_group(int count, const void *const *w, const float *const *x, float *const *y,
+                                     const int64_t *N, int M, int64_t K, qmv_stream_t stream)
+{
+    if (count < 1 || count > kMaxGroup) return QMV_ERR_SHAPE;
+    if (!w || !x || !y || !N) return QMV_ERR_NULL;
+    Q4Group grp{};
+    grp.count = count;
+    grp.row_start[0] = 0;
+    for (int i = 0; i < count; ++i) {
+        qmv_status st = check_shape(M, N[i], K, 256);
+        if (st != QMV_OK) return st;
+        grp.row_start[i + 1] = grp.row_start[i] + N[i];
+    }
+    if (grp.row_start[count] > kMaxDim) return QMV_ERR_SHAPE;
+    if (M == 0 || grp.row_start[count] == 0) return QMV_OK;
+    for (int i = 0; i < count; ++i) {
+        if (N[i] > 0 && !y[i]) return QMV_ERR_NULL;
+        if (misaligned(y[i], 4)) return QMV_ERR_ALIGN;
+    }
+    if (K == 0) {
+        for (int i = 0; i < count; ++i) {
+            if (N[i] == 0) continue;
+            qmv_status st = zero_fill(y[i], M, N[i], stream);
+            if (st != QMV_OK) return st;
+        }
+        return QMV_OK;
+    }
+    for (int i = 0; i < count; ++i) {
+        if (!w[i] || !x[i]) return QMV_ERR_NULL;
+        if (misaligned(w[i], 16) || misaligned(x[i], 16)) return QMV_ERR_ALIGN;
+        grp.w[i] = static_cast<const uint8_t *>(w[i]);
+        grp.x[i] = x[i];
+        grp.y[i] = y[i];
+    }
+    DeviceInfo dev;
+    cudaError_t e = current_device_info(&dev);
+    if (e != cudaSuccess) return QMV_ERR_CUDA;
+    Q4Plan plan;
+    if ((e = plan_q4_0(dev, grp, M, K, &plan)) != cudaSuccess) return QMV_ERR_CUDA;
+    if (plan.route != kRouteQ4_0Stream) return QMV_ERR_SHAPE;   // does not fit the streaming kernel
+    return from_cuda(launch_q4_0(plan, grp, nullptr, M, K, true, stream));
+}
+
+qmv_status qmv_q4_0_q8_1_fused(const void *w, const float *x, float *y, int M, int64_t N, int64_t K,
+                               qmv_stream_t stream)
+{
+    return qmv_q4_0_q8_1_fused_group(1, &w, &x, &y, &N, M, K, stream);
 }
 
 qmv_status qgemm_nvfp4_w4a16(const uint8_t *codes, const uint8_t *scales_e4m3, float global_scale,
@@ -163,6 +281,10 @@ qmv_status qgemm_fp8_w8a16(const uint8_t *w, const float *row_scale, const uint1
     const Route r = plan_fp8(w, x, K);
     return from_cuda(launch_fp8(r, dev, w, row_scale, x, y, M, N, K, stream));
 }
+
+void qmv_set_launch_overlap(int enable) { g_launch_overlap.store(enable ? 1 : 0, std::memory_order_relaxed); }
+
+int qmv_get_launch_overlap(void) { return g_launch_overlap.load(std::memory_order_relaxed); }
 
 int qmv_route_count(void) { return kRouteCount; }
 

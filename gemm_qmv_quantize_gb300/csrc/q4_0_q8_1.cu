@@ -10,15 +10,22 @@
 // dp4a is a full-rate instruction here, so the dot stays one dp4a per word.
 //
 // Streaming kernel (K % 256 == 0, 16-byte aligned rows): a row is K/32 blocks of
-// 18 bytes, a multiple of 144 = 9 x 16 bytes, so tiles of whole rows are one
-// contiguous, 16-byte aligned span. Each CTA streams its tiles with 1-D bulk
-// copies into a ring of shared-memory stages (mbarrier completion, evict-first
-// L2 hint), after staging the Q8_1 activations once in shared memory. A thread
-// consumes block pairs (36 bytes, always 4-byte aligned); lanes stride by one
-// pair, so its nine 32-bit reads are bank-conflict free, and the activation
-// pairs are padded to 80 bytes so the 16-byte activation reads are too.
+// 18 bytes, a whole number of 144-byte units (8 blocks, 9 x 16 bytes). The grid is
+// persistent and every warp owns a contiguous span of rows of one matrix, i.e. one
+// contiguous, 16-byte aligned byte range, which it streams through its own ring
+// of shared-memory slots with one 1-D bulk copy of up to 32 units (4608 bytes) per
+// iteration (mbarrier completion, evict-first L2 hint): after the activation
+// prologue no warp waits for another, and the cost of issuing a copy is spread
+// over all warps of the SM. Per iteration a lane takes one unit -- nine
+// conflict-free 16-byte shared-memory reads, 8 blocks of independent work -- and
+// rows that end inside the chunk are closed with a warp segmented scan (a row may
+// span chunks: its partial sum is carried). The high nibbles are summed under a
+// 0xF0 mask (one shift per block, not per word). Weight copies are issued before
+// the programmatic-dependency wait: with programmatic dependent launch the next
+// call's weights stream in while the previous call finishes.
 #include <algorithm>
 
+#include "q8_1_block.cuh"
 #include "qmv_device.cuh"
 #include "qmv_internal.h"
 
@@ -27,91 +34,114 @@ namespace {
 
 __device__ uint32_t g_q4_error;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;        // generic kernel
 constexpr int kWarps = kThreads / 32;
-constexpr int kPairBytes = 36;        // two Q4_0 blocks
-constexpr int kActPairStride = 80;    // 64 int8 activations + 16 bytes of padding
-
-struct ActBlock {
-    float d8;   // Q8_1 scale as fp32
-    int t8;     // 8 * sum(q8)
-};
+constexpr int kStreamThreads = 512;      // streaming kernel, M == 1: up to 16 warps
+constexpr int kStreamThreadsWide = 256;  // streaming kernel, M > 1: up to 8 warps
+// Staged activations, per activation row, one record per unit (8 blocks):
+// q8[256] (bytes 0..255), d8[8] as fp32 (256..287), 8*sum(q8)[8] (288..319),
+// padded to 336 bytes (21 x 16, odd) so 16-byte reads of consecutive records by
+// eight lanes fall in distinct bank groups.
+constexpr int kActUnitStride = 336;
+constexpr int kActD8Off = 256, kActT8Off = 288;
+constexpr int kUnitBytes = 144;      // 8 blocks: the 16-byte aligned unit of a row
+constexpr int kChunkUnits = 32;      // units per ring slot: one per lane
 
 struct Q4Layout {
-    uint32_t rowbytes, tilebytes;
-    uint32_t off_act, act_m_stride, off_dt, off_red, off_bar, total;
+    uint32_t rowbytes, units, slotbytes;
+    uint32_t off_act, act_m_stride, off_ring, ring_warp_stride, off_bar, total;
 };
 
-__host__ __device__ inline Q4Layout q4_layout(int M, int64_t K, int R, int S)
+// Shared memory: staged activations (act_rows = matrices x M rows), then one ring of
+// S slots of 32 units per warp, then the warps' mbarriers.
+__host__ __device__ inline Q4Layout q4_layout(int act_rows, int64_t K, int warps, int S)
 {
     Q4Layout L;
-    const uint32_t nb = static_cast<uint32_t>(K / 32), np = static_cast<uint32_t>(K / 64);
+    const uint32_t nb = static_cast<uint32_t>(K / 32);
+    L.units = static_cast<uint32_t>(K / 256);
     L.rowbytes = nb * 18u;
-    L.tilebytes = static_cast<uint32_t>(R) * L.rowbytes;
-    L.off_act = static_cast<uint32_t>(S) * L.tilebytes;
-    L.act_m_stride = np * kActPairStride;
-    L.off_dt = L.off_act + static_cast<uint32_t>(M) * L.act_m_stride;
-    L.off_red = L.off_dt + static_cast<uint32_t>(M) * nb * static_cast<uint32_t>(sizeof(ActBlock));
-    const uint32_t red_rows = static_cast<uint32_t>(R > kWarps ? R : kWarps);
-    L.off_bar = (L.off_red + red_rows * static_cast<uint32_t>(M) * 4u + 7u) & ~7u;
-    L.total = L.off_bar + static_cast<uint32_t>(S) * 8u;
+    L.slotbytes = kChunkUnits * kUnitBytes;
+    L.off_act = 0;
+    L.act_m_stride = L.units * kActUnitStride;
+    L.off_ring = (static_cast<uint32_t>(act_rows) * L.act_m_stride + 127u) & ~127u;
+    L.ring_warp_stride = static_cast<uint32_t>(S) * L.slotbytes;
+    L.off_bar = L.off_ring + static_cast<uint32_t>(warps) * L.ring_warp_stride;
+    L.total = L.off_bar + static_cast<uint32_t>(warps * S) * 8u;
     return L;
 }
 
-// Dot of one block pair of a weight row against M staged activation rows.
-// wp: the pair's 36 bytes in shared memory (4-byte aligned).
-// act: the pair's activations of row 0 (stride act_stride per row).
-// dt:  ActBlock of block 2p of row 0 (stride nb per row).
-template <int M, bool kDots>
-__device__ __forceinline__ void q4_pair(const uint8_t *wp8, const uint8_t *act, uint32_t act_stride,
-                                        const ActBlock *dt, int nb, float (&acc)[M], int32_t *dots,
-                                        int64_t dots_m_stride)
+// S - 8T of one block: qs (4 words of nibbles), its 8 activation words, and 8T.
+// The high nibbles stay in place under a 0xF0 mask (bytes 0..240, exact), so their
+// sum is 16x and is shifted once.
+__device__ __forceinline__ int q4_block_dot(const uint32_t (&qs)[4], const uint4 &a0, const uint4 &a1, int t8)
 {
-    const uint32_t *wp = reinterpret_cast<const uint32_t *>(wp8);
-    uint32_t w[9];
+    int lo = 0, hi = 0;
+    lo = dp4a_us(qs[0] & 0x0f0f0f0fu, a0.x, lo);
+    hi = dp4a_us(qs[0] & 0xf0f0f0f0u, a1.x, hi);
+    lo = dp4a_us(qs[1] & 0x0f0f0f0fu, a0.y, lo);
+    hi = dp4a_us(qs[1] & 0xf0f0f0f0u, a1.y, hi);
+    lo = dp4a_us(qs[2] & 0x0f0f0f0fu, a0.z, lo);
+    hi = dp4a_us(qs[2] & 0xf0f0f0f0u, a1.z, hi);
+    lo = dp4a_us(qs[3] & 0x0f0f0f0fu, a0.w, lo);
+    hi = dp4a_us(qs[3] & 0xf0f0f0f0u, a1.w, hi);
+    return lo + (hi >> 4) - t8;
+}
+
+// Dot of one 8-block unit of a weight row against M staged activation rows.
+// wu: the unit's 144 bytes in shared memory (16-byte aligned).
+// act: the unit's activation record of row 0 (stride act_stride per row).
+// dots: block dots of row 0 (stride dots_m_stride per row), kDots only.
+template <int M, bool kDots>
+__device__ __forceinline__ void q4_unit(const uint8_t *wu, const uint8_t *act, uint32_t act_stride, float (&acc)[M],
+                                        int32_t *dots, int64_t dots_m_stride)
+{
+    const uint4 *wp = reinterpret_cast<const uint4 *>(wu);
+    uint32_t w[36];
 #pragma unroll
-    for (int i = 0; i < 9; ++i) w[i] = wp[i];
-    // block A = bytes 0..17: d4 in bytes 0..1, qs in bytes 2..17 (2 mod 4: realign)
-    // block B = bytes 18..35: d4 in bytes 18..19, qs in bytes 20..35 (aligned)
-    const float d4a = f16_bits_to_float(w[0] & 0xffffu);
-    const float d4b = f16_bits_to_float(w[4] >> 16);
-    uint32_t la[4], ha[4], lb[4], hb[4];
+    for (int i = 0; i < 9; ++i) {
+        const uint4 v = wp[i];
+        w[4 * i] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+    }
+    // block j starts at byte 18j: d4 in its first two bytes, qs in the next 16;
+    // even blocks have their qs at 2 mod 4 and are realigned with byte permutes.
+    float d4[8];
+    uint32_t qs[8][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t qa = __byte_perm(w[i], w[i + 1], 0x5432);
-        la[i] = qa & 0x0f0f0f0fu;          // elements 4i..4i+3
-        ha[i] = (qa >> 4) & 0x0f0f0f0fu;   // elements 16+4i..16+4i+3
-        lb[i] = w[5 + i] & 0x0f0f0f0fu;
-        hb[i] = (w[5 + i] >> 4) & 0x0f0f0f0fu;
+    for (int j = 0; j < 8; j += 2) {
+        const int wa = (18 * j) / 4;           // word holding block j's first byte (aligned)
+        d4[j] = f16_bits_to_float(w[wa] & 0xffffu);
+        d4[j + 1] = f16_bits_to_float(w[wa + 4] >> 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            qs[j][i] = __byte_perm(w[wa + i], w[wa + i + 1], 0x5432);
+            qs[j + 1][i] = w[wa + 5 + i];
+        }
     }
 #pragma unroll
     for (int m = 0; m < M; ++m) {
-        const uint4 *a = reinterpret_cast<const uint4 *>(act + m * act_stride);
-        const uint4 a0 = a[0], a1 = a[1], a2 = a[2], a3 = a[3];
-        int sa = 0, sb = 0;
-        sa = dp4a_us(la[0], a0.x, sa);
-        sa = dp4a_us(la[1], a0.y, sa);
-        sa = dp4a_us(la[2], a0.z, sa);
-        sa = dp4a_us(la[3], a0.w, sa);
-        sa = dp4a_us(ha[0], a1.x, sa);
-        sa = dp4a_us(ha[1], a1.y, sa);
-        sa = dp4a_us(ha[2], a1.z, sa);
-        sa = dp4a_us(ha[3], a1.w, sa);
-        sb = dp4a_us(lb[0], a2.x, sb);
-        sb = dp4a_us(lb[1], a2.y, sb);
-        sb = dp4a_us(lb[2], a2.z, sb);
-        sb = dp4a_us(lb[3], a2.w, sb);
-        sb = dp4a_us(hb[0], a3.x, sb);
-        sb = dp4a_us(hb[1], a3.y, sb);
-        sb = dp4a_us(hb[2], a3.z, sb);
-        sb = dp4a_us(hb[3], a3.w, sb);
-        const ActBlock ba = dt[m * nb], bb = dt[m * nb + 1];
-        const int da = sa - ba.t8, db = sb - bb.t8;
+        const uint8_t *am = act + m * act_stride;
+        const uint4 *a = reinterpret_cast<const uint4 *>(am);
+        const float4 d8a = *reinterpret_cast<const float4 *>(am + kActD8Off);
+        const float4 d8b = *reinterpret_cast<const float4 *>(am + kActD8Off + 16);
+        const int4 t8a = *reinterpret_cast<const int4 *>(am + kActT8Off);
+        const int4 t8b = *reinterpret_cast<const int4 *>(am + kActT8Off + 16);
+        const float d8[8] = {d8a.x, d8a.y, d8a.z, d8a.w, d8b.x, d8b.y, d8b.z, d8b.w};
+        const int t8[8] = {t8a.x, t8a.y, t8a.z, t8a.w, t8b.x, t8b.y, t8b.z, t8b.w};
+        int sd[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) sd[j] = q4_block_dot(qs[j], a[2 * j], a[2 * j + 1], t8[j]);
         if (kDots) {
-            dots[m * dots_m_stride] = da;
-            dots[m * dots_m_stride + 1] = db;
+            int32_t *dm = dots + m * dots_m_stride;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dm[j] = sd[j];
         } else {
-            acc[m] += (d4a * ba.d8) * static_cast<float>(da) + (d4b * bb.d8) * static_cast<float>(db);
+            float part = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) part = fmaf(d4[j] * d8[j], static_cast<float>(sd[j]), part);
+            acc[m] += part;
         }
     }
 }
@@ -123,121 +153,198 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
-template <int M, bool kDots>
-__global__ void __launch_bounds__(kThreads) q4_0_stream_kernel(const uint8_t *__restrict__ w,
-                                                              const uint8_t *__restrict__ xq,
-                                                              float *__restrict__ y, int32_t *__restrict__ dots,
-                                                              int64_t N, int64_t K, int R, int S)
+// Shared-memory record of the unit holding block b of activation row gm (= matrix * M + m).
+__device__ __forceinline__ uint8_t *act_block(uint8_t *smem, const Q4Layout &L, int gm, int b)
 {
-    extern __shared__ __align__(128) uint8_t smem[];
-    const Q4Layout L = q4_layout(M, K, R, S);
-    const int nb = static_cast<int>(K >> 5), np = static_cast<int>(K >> 6);
-    const int64_t ntiles = (N + R - 1) / R;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.off_bar);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    return smem + L.off_act + gm * L.act_m_stride + (b >> 3) * kActUnitStride;
+}
 
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    const uint64_t pol = policy_evict_first();
-    auto issue = [&](int64_t tile, int slot) {
-        const int64_t row0 = tile * R;
-        const uint32_t rows = static_cast<uint32_t>(min(static_cast<int64_t>(R), N - row0));
-        const uint32_t bytes = rows * L.rowbytes;
-        mbar_arrive_expect_tx(&bars[slot], bytes);
-        bulk_copy_g2s(smem + static_cast<uint32_t>(slot) * L.tilebytes, w + row0 * L.rowbytes, bytes, &bars[slot],
-                      pol);
-    };
-    // Weights do not depend on the preceding kernel: start streaming before waiting on it.
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            const int64_t tile = blockIdx.x + static_cast<int64_t>(s) * gridDim.x;
-            if (tile < ntiles) issue(tile, s);
+// Quantize the group's fp32 activations to Q8_1 straight into the shared-memory
+// staging layout, a quad of lanes per 32-value block (the quantizer's own code).
+template <int M>
+__device__ __forceinline__ void stage_fused(const Q4Group &grp, int nb, uint8_t *smem, const Q4Layout &L,
+                                            int nthreads)
+{
+    constexpr int kPasses = 4;   // loads of up to 4 passes are issued before any is used
+    const int part = threadIdx.x & 3;
+    const int total = grp.count * M * nb;   // blocks over (matrix, row m, block b)
+    const int quads = nthreads >> 2;
+    for (int base = 0; base < total; base += kPasses * quads) {   // uniform trip count: whole warps shuffle
+        float v[kPasses][8];
+#pragma unroll
+        for (int ps = 0; ps < kPasses; ++ps) {
+            const int u = base + ps * quads + static_cast<int>(threadIdx.x >> 2);
+            const int uc = u < total ? u : 0;
+            const int gm = uc / nb, b = uc - gm * nb;
+            const int gi = gm / M, m = gm - gi * M;
+            const float *src = static_cast<const float *>(grp.x[gi]) + static_cast<int64_t>(m) * (nb * 32) + b * 32 +
+                               8 * part;
+            if (base + ps * quads < total) {
+                const float4 a = __ldg(reinterpret_cast<const float4 *>(src));
+                const float4 c = __ldg(reinterpret_cast<const float4 *>(src) + 1);
+                v[ps][0] = a.x; v[ps][1] = a.y; v[ps][2] = a.z; v[ps][3] = a.w;
+                v[ps][4] = c.x; v[ps][5] = c.y; v[ps][6] = c.z; v[ps][7] = c.w;
+            }
+        }
+#pragma unroll
+        for (int ps = 0; ps < kPasses; ++ps) {
+            if (base + ps * quads >= total) break;   // uniform over the CTA
+            const int u = base + ps * quads + static_cast<int>(threadIdx.x >> 2);
+            const Q8Quad r = q8_1_quantize_quad(v[ps]);
+            if (u < total) {
+                const int gm = u / nb, b = u - gm * nb;
+                uint8_t *rec = act_block(smem, L, gm, b);
+                const int j = b & 7;
+                *reinterpret_cast<uint2 *>(rec + 32 * j + 8 * part) = make_uint2(r.qlo, r.qhi);
+                if (part == 0) {
+                    reinterpret_cast<float *>(rec + kActD8Off)[j] = f16_bits_to_float(q8_1_d8_bits(r));
+                    reinterpret_cast<int *>(rec + kActT8Off)[j] = 8 * r.sum;
+                }
+            }
         }
     }
-    grid_launch_dependents();
-    grid_dependency_wait();
+}
 
-    // Stage the Q8_1 activations: padded int8 pairs + (d8, 8T) per block.
-    ActBlock *dts = reinterpret_cast<ActBlock *>(smem + L.off_dt);
-    for (int i = tid; i < M * nb; i += kThreads) {
-        const int m = i / nb, b = i - m * nb;
-        const uint32_t *src = reinterpret_cast<const uint32_t *>(xq + static_cast<int64_t>(i) * 36);
+// Copy the group's Q8_1 activations into the staging layout, adding 8 * sum(q) per block.
+template <int M>
+__device__ __forceinline__ void stage_q8_1(const Q4Group &grp, int nb, uint8_t *smem, const Q4Layout &L,
+                                           int nthreads)
+{
+    const int total = grp.count * M * nb;
+    for (int u = threadIdx.x; u < total; u += nthreads) {
+        const int gm = u / nb, b = u - gm * nb;
+        const int gi = gm / M, m = gm - gi * M;
+        const uint32_t *src = reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(grp.x[gi]) +
+                                                                 (static_cast<int64_t>(m) * nb + b) * 36);
         uint32_t q[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) q[j] = __ldg(src + 1 + j);
         int t = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) t = __dp4a(static_cast<int>(q[j]), 0x01010101, t);
-        dts[i].d8 = f16_bits_to_float(__ldg(src) & 0xffffu);
-        dts[i].t8 = 8 * t;
-        uint4 *dst = reinterpret_cast<uint4 *>(smem + L.off_act + m * L.act_m_stride + (b >> 1) * kActPairStride +
-                                               (b & 1) * 32);
+        uint8_t *rec = act_block(smem, L, gm, b);
+        const int j = b & 7;
+        reinterpret_cast<float *>(rec + kActD8Off)[j] = f16_bits_to_float(__ldg(src) & 0xffffu);
+        reinterpret_cast<int *>(rec + kActT8Off)[j] = 8 * t;
+        uint4 *dst = reinterpret_cast<uint4 *>(rec + 32 * j);
         dst[0] = make_uint4(q[0], q[1], q[2], q[3]);
         dst[1] = make_uint4(q[4], q[5], q[6], q[7]);
     }
-    __syncthreads();
+}
 
-    const int wpr = (R >= kWarps) ? 1 : kWarps / R;   // warps sharing one row
-    const int rows_par = kWarps / wpr;                  // rows in flight per pass
-    const int sub = warp % wpr;
-    float *red = reinterpret_cast<float *>(smem + L.off_red);
+// kFused: the group's activations are fp32 [M][K], quantized to Q8_1 in the
+// prologue; else they are Q8_1 [M][K/32]. kDots: write the integer block dots of
+// matrix 0 instead of y (a single-matrix group).
+template <int M, bool kDots, bool kFused>
+__global__ void __launch_bounds__(M == 1 ? kStreamThreads : kStreamThreadsWide) q4_0_stream_kernel(
+    const __grid_constant__ Q4Group grp, int32_t *__restrict__ dots, int64_t K, int S)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warps = blockDim.x >> 5;
+    const Q4Layout L = q4_layout(M * grp.count, K, warps, S);
+    const int nb = static_cast<int>(K >> 5);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int U = static_cast<int>(L.units);
+    uint8_t *ring = smem + L.off_ring + warp * L.ring_warp_stride;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.off_bar) + warp * S;
 
-    int64_t local = 0;
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++local) {
-        const int slot = static_cast<int>(local % S);
-        const uint32_t parity = static_cast<uint32_t>((local / S) & 1);
-        const bool ok = mbar_wait(&bars[slot], parity);
-        if (!__syncthreads_and(ok)) {
-            if (tid == 0) {
+    // This warp's span: rows [r0, r1) of matrix mi (warps are split over the
+    // matrices in proportion to their rows, then rows evenly over the warps).
+    const int gw = blockIdx.x * warps + warp;
+    int mi = 0;
+#pragma unroll
+    for (int i = 1; i < kMaxGroup; ++i)
+        if (i < grp.count && gw >= grp.cta_start[i]) mi = i;
+    const int64_t Nm = grp.row_start[mi + 1] - grp.row_start[mi];
+    const int64_t wm = grp.cta_start[mi + 1] - grp.cta_start[mi];
+    const int64_t j = gw - grp.cta_start[mi];
+    const int64_t r0 = j < wm ? j * Nm / wm : Nm, r1 = j < wm ? (j + 1) * Nm / wm : Nm;
+    const int TU = static_cast<int>((r1 - r0) * U);   // units in the span (< 2^31: checked by the host)
+    const int nchunks = (TU + kChunkUnits - 1) / kChunkUnits;
+    const uint8_t *span = grp.w[mi] + r0 * L.rowbytes;
+    const uint64_t pol = policy_evict_first();
+
+    auto issue = [&](int c) {   // chunk c into slot c % S
+        const int slot = c % S;
+        const uint32_t bytes = static_cast<uint32_t>(min(kChunkUnits, TU - c * kChunkUnits)) * kUnitBytes;
+        mbar_arrive_expect_tx(&bars[slot], bytes);
+        bulk_copy_g2s(ring + slot * L.slotbytes, span + static_cast<int64_t>(c) * (kChunkUnits * kUnitBytes), bytes,
+                      &bars[slot], pol);
+    };
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+        fence_barrier_init();
+        // weights do not depend on the preceding kernel: start streaming them now
+        for (int c = 0; c < S && c < nchunks; ++c) issue(c);
+    }
+    __syncwarp();
+    grid_launch_dependents();
+    grid_dependency_wait();
+
+    if (kFused)
+        stage_fused<M>(grp, nb, smem, L, blockDim.x);
+    else
+        stage_q8_1<M>(grp, nb, smem, L, blockDim.x);
+    __syncthreads();   // the only CTA-wide barrier
+
+    const uint8_t *act0 = smem + L.off_act + (mi * M) * L.act_m_stride;
+    float *ym = grp.y[mi];
+    float carry[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) carry[m] = 0.0f;
+    int carry_row = -1;
+    for (int c = 0; c < nchunks; ++c) {
+        const int slot = c % S;
+        if (!mbar_wait_sleep(&bars[slot], (c / S) & 1)) {
+            if (lane == 0) {
                 atomicOr(&g_q4_error, kErrWaitTimeout);
-                // let copies still in flight land before the CTA's shared memory is released
-                for (int s = 1; s < S; ++s) {
-                    const int64_t lt = local + s;
-                    if (blockIdx.x + lt * gridDim.x < ntiles)
-                        (void)mbar_wait(&bars[lt % S], static_cast<uint32_t>((lt / S) & 1));
-                }
+                // let this warp's other copies land before the CTA can release its memory
+                for (int s = 1; s < S && c + s < nchunks; ++s)
+                    (void)mbar_wait_sleep(&bars[(c + s) % S], ((c + s) / S) & 1);
             }
             return;
         }
-        const uint8_t *tb = smem + static_cast<uint32_t>(slot) * L.tilebytes;
-        const int64_t row0 = tile * R;
-        const int rows_here = static_cast<int>(min(static_cast<int64_t>(R), N - row0));
-
-        for (int rr = warp / wpr; rr < rows_here; rr += rows_par) {
-            float acc[M];
+        const int gu = c * kChunkUnits + lane;   // unit index in the span
+        const bool live = gu < TU;
+        const int rr = live ? gu / U : -1;       // row within the span
+        const int uin = live ? gu - rr * U : 0;  // unit within its row
+        float v[M];
 #pragma unroll
-            for (int m = 0; m < M; ++m) acc[m] = 0.0f;
-            const uint8_t *wrow = tb + rr * L.rowbytes;
-            int32_t *drow = kDots ? dots + (row0 + rr) * nb : nullptr;
-            for (int p = sub * 32 + lane; p < np; p += 32 * wpr) {
-                q4_pair<M, kDots>(wrow + kPairBytes * p, smem + L.off_act + kActPairStride * p, L.act_m_stride,
-                                  dts + 2 * p, nb, acc, kDots ? drow + 2 * p : nullptr, N * nb);
-            }
-            if (!kDots) {
+        for (int m = 0; m < M; ++m) v[m] = 0.0f;
+        if (live) {
+            q4_unit<M, kDots>(ring + slot * L.slotbytes + lane * kUnitBytes, act0 + uin * kActUnitStride,
+                              L.act_m_stride, v, kDots ? dots + (r0 + rr) * nb + 8 * uin : nullptr, Nm * nb);
+        }
+        __syncwarp();   // every lane is done with the slot
+        if (lane == 0 && c + S < nchunks) issue(c + S);
+        if (!kDots) {
+            // segmented inclusive scan over lanes of the same row (rows increase with lane)
 #pragma unroll
-                for (int m = 0; m < M; ++m) acc[m] = warp_sum(acc[m]);
-                if (lane == 0) {
+            for (int d = 1; d < 32; d <<= 1) {
+                const int ro = __shfl_up_sync(0xffffffffu, rr, d);
 #pragma unroll
-                    for (int m = 0; m < M; ++m) red[(rr * wpr + sub) * M + m] = acc[m];
+                for (int m = 0; m < M; ++m) {
+                    const float o = __shfl_up_sync(0xffffffffu, v[m], d);
+                    if (lane >= d && ro == rr) v[m] += o;
                 }
             }
-        }
-        __syncthreads();   // every thread is done with this stage
-        if (tid == 0) {
-            const int64_t next = tile + static_cast<int64_t>(S) * gridDim.x;
-            if (next < ntiles) issue(next, slot);
-        }
-        if (!kDots) {
-            for (int i = tid; i < rows_here * M; i += kThreads) {
-                const int r = i / M, m = i - r * M;
-                float s = 0.0f;
-                for (int j = 0; j < wpr; ++j) s += red[(r * wpr + j) * M + m];
-                y[m * N + row0 + r] = s;
+            const int rnext = __shfl_down_sync(0xffffffffu, rr, 1);
+            const bool tail = live && (lane == 31 || rnext != rr);   // last lane of its row here
+            if (tail && rr == carry_row) {
+#pragma unroll
+                for (int m = 0; m < M; ++m) v[m] += carry[m];
             }
+            const bool row_end = tail && uin == U - 1;
+            if (row_end) {
+#pragma unroll
+                for (int m = 0; m < M; ++m) ym[m * Nm + r0 + rr] = v[m];
+            }
+            // the chunk's last live lane passes an unfinished row on to the next chunk
+            const int last = min(31, TU - 1 - c * kChunkUnits);
+            const bool open = __shfl_sync(0xffffffffu, static_cast<int>(tail && !row_end), last) != 0;
+            carry_row = open ? __shfl_sync(0xffffffffu, rr, last) : -1;
+#pragma unroll
+            for (int m = 0; m < M; ++m) carry[m] = __shfl_sync(0xffffffffu, v[m], last);
         }
     }
 }
@@ -302,85 +409,113 @@ __global__ void __launch_bounds__(kThreads) q4_0_generic_kernel(const uint8_t *_
 
 // ---------------------------------------------------------------- host side
 
-template <int M, bool kDots>
-cudaError_t launch_m(const Q4Plan &p, const uint8_t *w, const uint8_t *xq, float *y, int32_t *dots, int64_t N,
-                     int64_t K, cudaStream_t s)
+template <int M, bool kDots, bool kFused>
+cudaError_t launch_m(const Q4Plan &p, const Q4Group &grp, int32_t *dots, int64_t K, cudaStream_t s)
 {
+    cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(kThreads);
     cfg.stream = s;
     cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+    cfg.attrs = attr;
+    cfg.numAttrs = set_launch_overlap_attr(attr);
     if (p.route == kRouteQ4_0Stream) {
-        auto kern = q4_0_stream_kernel<M, kDots>;
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, p.smem_bytes);
+        auto kern = q4_0_stream_kernel<M, kDots, kFused>;
+        cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), p.smem_bytes);
         if (e != cudaSuccess) return e;
+        cfg.blockDim = dim3(static_cast<unsigned>(p.warps * 32));   // consumers + the producer
         cfg.dynamicSmemBytes = static_cast<size_t>(p.smem_bytes);
-        return cudaLaunchKernelEx(&cfg, kern, w, xq, y, dots, N, K, p.rows_per_tile, p.stages);
+        return cudaLaunchKernelEx(&cfg, kern, grp, dots, K, p.stages);
     }
-    return cudaLaunchKernelEx(&cfg, q4_0_generic_kernel<M, kDots>, w, xq, y, dots, N, K);
+    if (kFused || grp.count != 1) return cudaErrorInvalidValue;   // these need the streaming kernel
+    cfg.blockDim = dim3(kThreads);
+    auto gk = q4_0_generic_kernel<M, kDots>;
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gk), 0);
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, gk, grp.w[0], static_cast<const uint8_t *>(grp.x[0]), grp.y[0], dots,
+                              grp.row_start[1], K);
 }
 
-template <bool kDots>
-cudaError_t launch_dispatch(const Q4Plan &p, const uint8_t *w, const uint8_t *xq, float *y, int32_t *dots, int M,
-                            int64_t N, int64_t K, cudaStream_t s)
+template <bool kDots, bool kFused>
+cudaError_t launch_dispatch(const Q4Plan &p, const Q4Group &grp, int32_t *dots, int M, int64_t K, cudaStream_t s)
 {
     switch (M) {
-    case 1: return launch_m<1, kDots>(p, w, xq, y, dots, N, K, s);
-    case 2: return launch_m<2, kDots>(p, w, xq, y, dots, N, K, s);
-    case 3: return launch_m<3, kDots>(p, w, xq, y, dots, N, K, s);
-    case 4: return launch_m<4, kDots>(p, w, xq, y, dots, N, K, s);
-    case 5: return launch_m<5, kDots>(p, w, xq, y, dots, N, K, s);
-    case 6: return launch_m<6, kDots>(p, w, xq, y, dots, N, K, s);
-    case 7: return launch_m<7, kDots>(p, w, xq, y, dots, N, K, s);
-    case 8: return launch_m<8, kDots>(p, w, xq, y, dots, N, K, s);
+    case 1: return launch_m<1, kDots, kFused>(p, grp, dots, K, s);
+    case 2: return launch_m<2, kDots, kFused>(p, grp, dots, K, s);
+    case 3: return launch_m<3, kDots, kFused>(p, grp, dots, K, s);
+    case 4: return launch_m<4, kDots, kFused>(p, grp, dots, K, s);
+    case 5: return launch_m<5, kDots, kFused>(p, grp, dots, K, s);
+    case 6: return launch_m<6, kDots, kFused>(p, grp, dots, K, s);
+    case 7: return launch_m<7, kDots, kFused>(p, grp, dots, K, s);
+    case 8: return launch_m<8, kDots, kFused>(p, grp, dots, K, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-cudaError_t plan_q4_0(const DeviceInfo &dev, const void *w, const void *xq, int M, int64_t N, int64_t K,
-                      Q4Plan *plan)
+cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t K, Q4Plan *plan)
 {
-    (void)xq;
-    const bool aligned = (reinterpret_cast<uintptr_t>(w) & 15u) == 0;
+    bool aligned = true;
+    for (int i = 0; i < grp.count; ++i) aligned = aligned && (reinterpret_cast<uintptr_t>(grp.w[i]) & 15u) == 0;
+    const int64_t N = grp.row_start[grp.count];
     plan->route = kRouteQ4_0Generic;
-    plan->rows_per_tile = 0;
+    plan->warps = kWarps;
     plan->stages = 0;
     plan->smem_bytes = 0;
     plan->grid = static_cast<int>((N + kWarps - 1) / kWarps);
     if (!aligned || K % 256 != 0) return cudaSuccess;
 
-    const int64_t rowbytes = K / 32 * 18;
-    // Tile: whole rows, at most ~20 KB per stage; fewer rows when the matrix is
-    // short so every CTA gets several tiles.
-    int R = 1;
-    while (R < 64 && (2 * R) * rowbytes <= 20 * 1024) R *= 2;
-    while (R > 1 && (N + R - 1) / R < 4LL * dev.sm_count) R /= 2;
-    int S = 4;
-    Q4Layout L = q4_layout(M, K, R, S);
-    while (L.total > static_cast<uint32_t>(dev.smem_optin) && S > 2) L = q4_layout(M, K, R, --S);
-    while (L.total > static_cast<uint32_t>(dev.smem_optin) && R > 1) L = q4_layout(M, K, R /= 2, S);
-    if (L.total > static_cast<uint32_t>(dev.smem_optin)) return cudaSuccess;   // generic kernel
-
-    const int per_sm = std::max(1, std::min(kWarps, dev.smem_per_sm / static_cast<int>(L.total + 1024)));
-    const int64_t ntiles = (N + R - 1) / R;
+    // Warps hide latency (each also issues its own copies); slots are the bytes in flight.
+    const int act_rows = M * grp.count;
+    const int cap = (M == 1 ? kStreamThreads : kStreamThreadsWide) / 32;
+    int warps = std::max(1, std::min(cap, env_int("QMV_Q4_WARPS", cap)));
+    const int S = std::max(1, std::min(8, env_int("QMV_Q4_SLOTS", 2)));
+    const int budget = env_int("QMV_Q4_PAIR_SMEM", 0) ? dev.smem_per_sm / 2 - 2048 : dev.smem_optin;
+    while (warps > 1 && q4_layout(act_rows, K, warps, S).total > static_cast<uint32_t>(budget)) --warps;
+    if (q4_layout(act_rows, K, warps, S).total > static_cast<uint32_t>(dev.smem_optin)) return cudaSuccess;
+    const int per_sm = std::max(1, std::min(4, env_int("QMV_Q4_CTAS_PER_SM", 1)));
+    const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>((N + warps - 1) / warps,
+                                                                 static_cast<int64_t>(dev.sm_count) * per_sm));
+    if ((N / (ctas * warps) + 1) * (K / 256) >= (int64_t(1) << 31)) return cudaSuccess;   // 32-bit unit counters
     plan->route = kRouteQ4_0Stream;
-    plan->rows_per_tile = R;
+    plan->warps = warps;
     plan->stages = S;
-    plan->smem_bytes = static_cast<int>(L.total);
-    plan->grid = static_cast<int>(std::min<int64_t>(ntiles, static_cast<int64_t>(dev.sm_count) * per_sm));
+    plan->chunk_units = kChunkUnits;
+    plan->smem_bytes = static_cast<int>(q4_layout(act_rows, K, warps, S).total);
+    plan->grid = static_cast<int>(ctas);
     return cudaSuccess;
 }
 
-cudaError_t launch_q4_0(const Q4Plan &plan, const void *w, const void *xq, float *y, int32_t *dots, int M,
-                        int64_t N, int64_t K, cudaStream_t s)
+// Split the grid's warps over the group's matrices in proportion to their rows
+// (at least one warp per non-empty matrix when there are enough warps).
+void assign_ctas(Q4Group &grp, int total)
 {
-    const uint8_t *wb = static_cast<const uint8_t *>(w);
-    const uint8_t *xb = static_cast<const uint8_t *>(xq);
-    route_hit(plan.route);
-    if (dots) return launch_dispatch<true>(plan, wb, xb, y, dots, M, N, K, s);
-    return launch_dispatch<false>(plan, wb, xb, y, dots, M, N, K, s);
+    const int64_t N = grp.row_start[grp.count];
+    int64_t acc = 0;
+    grp.cta_start[0] = 0;
+    for (int i = 0; i < grp.count; ++i) {
+        const int64_t n = grp.row_start[i + 1] - grp.row_start[i];
+        acc += n;
+        int64_t end = (acc * total + N - 1) / N;   // ceil share of the CTAs so far
+        const int64_t lo = grp.cta_start[i] + (n > 0 ? 1 : 0);
+        const int64_t hi = total - (grp.count - 1 - i);
+        end = std::max(lo, std::min(end, hi));
+        if (i == grp.count - 1) end = total;
+        grp.cta_start[i + 1] = static_cast<int>(end);
+    }
+    for (int i = grp.count + 1; i <= kMaxGroup; ++i) grp.cta_start[i] = total;
+}
+
+cudaError_t launch_q4_0(const Q4Plan &plan, const Q4Group &grp_in, int32_t *dots, int M, int64_t K, bool fused,
+                        cudaStream_t s)
+{
+    if (fused && plan.route != kRouteQ4_0Stream) return cudaErrorInvalidValue;
+    Q4Group grp = grp_in;
+    if (plan.route == kRouteQ4_0Stream) assign_ctas(grp, plan.grid * plan.warps);   // per warp
+    route_hit(fused ? kRouteQ4_0StreamFused : plan.route);
+    if (dots) return launch_dispatch<true, false>(plan, grp, dots, M, K, s);
+    if (fused) return launch_dispatch<false, true>(plan, grp, dots, M, K, s);
+    return launch_dispatch<false, false>(plan, grp, dots, M, K, s);
 }
 
 cudaError_t read_error_word_q4_0(uint32_t *out, bool clear)

@@ -34,6 +34,11 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
                  : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 {
     uint32_t ok;
@@ -47,11 +52,36 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return ok != 0;
 }
 
+// Like mbar_try_wait, but the thread may sleep up to `suspend_ns` inside the
+// instruction until the phase completes (no busy polling).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t suspend_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait: false if the phase did not complete within kMaxWaitIters polls.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
 {
     for (uint32_t i = 0; i < kMaxWaitIters; ++i)
         if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// Bounded sleeping wait: at most kMaxSleepWaits suspensions of up to 1 ms each
+// (about 2 s in all) before giving up.
+constexpr uint32_t kMaxSleepWaits = 2000u;
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < kMaxSleepWaits; ++i)
+        if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
     return false;
 }
 

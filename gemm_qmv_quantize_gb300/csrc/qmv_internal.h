@@ -12,6 +12,7 @@ enum Route : int {
     kRouteQuantizeQ8_1 = 0,
     kRouteQ4_0Stream,     // Q4_0: bulk-copy staged rows, dp4a
     kRouteQ4_0Generic,    // Q4_0: any K % 32 == 0, 2-byte aligned rows
+    kRouteQ4_0StreamFused,  // Q4_0 with the Q8_1 quantize in the prologue
     kRouteNvfp4Mma,       // NVFP4: register-fed m16n8k16, K % 256 == 0
     kRouteNvfp4Generic,   // NVFP4: any K % 16 == 0
     kRouteFp8Mma,         // FP8: register-fed m16n8k16, K % 128 == 0
@@ -35,18 +36,40 @@ cudaError_t current_device_info(DeviceInfo *out);
 // ---- launchers (arguments already validated by the ABI layer)
 cudaError_t launch_quantize_q8_1(const float *x, void *xq, int M, int64_t K, cudaStream_t s);
 
-// Q4_0 plan: which kernel, tile rows, pipeline stages, grid.
+// Q4_0 plan: which kernel, warps per CTA, ring slots per warp, grid.
 struct Q4Plan {
     Route route;
-    int rows_per_tile;
-    int stages;
+    int warps;         // streaming kernel: warps per CTA
+    int stages;        // streaming kernel: ring slots per warp
+    int chunk_units;   // 144-byte units per ring slot
     int grid;
     int smem_bytes;
 };
-cudaError_t plan_q4_0(const DeviceInfo &dev, const void *w, const void *xq, int M, int64_t N, int64_t K,
-                      Q4Plan *plan);
-cudaError_t launch_q4_0(const Q4Plan &plan, const void *w, const void *xq, float *y, int32_t *dots, int M,
-                        int64_t N, int64_t K, cudaStream_t s);
+
+// Programmatic dependent launch (opt-in, qmv_set_launch_overlap): fills attr[0]
+// and returns 1 when enabled, else returns 0.
+int set_launch_overlap_attr(cudaLaunchAttribute *attr);
+// Integer from the environment (plan overrides for sweeps), else `fallback`.
+int env_int(const char *name, int fallback);
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize = bytes, and the preferred
+// shared-memory carveout in percent unless negative) once per kernel and device.
+cudaError_t ensure_smem_attr(const void *kernel, int bytes, int carveout = cudaSharedmemCarveoutMaxShared);
+// A group of Q4_0 matrices with the same K launched together (count 1 for a
+// single call): rows are concatenated in order, each matrix with its own
+// activations and outputs. Passed to the kernel by value.
+constexpr int kMaxGroup = 8;
+struct Q4Group {
+    int count;
+    const uint8_t *w[kMaxGroup];
+    const void *x[kMaxGroup];      // fp32 [M][K] (fused) or Q8_1 [M][K/32]
+    float *y[kMaxGroup];           // fp32 [M][N_i]
+    int64_t row_start[kMaxGroup + 1];
+    int cta_start[kMaxGroup + 1];   // streaming kernel: warps of matrix i are [cta_start[i], cta_start[i+1])
+};
+
+cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t K, Q4Plan *plan);
+cudaError_t launch_q4_0(const Q4Plan &plan, const Q4Group &grp, int32_t *dots, int M, int64_t K, bool fused,
+                        cudaStream_t s);
 
 Route plan_nvfp4(const uint8_t *codes, const uint8_t *scales, const uint16_t *x, int64_t K);
 cudaError_t launch_nvfp4(Route r, const DeviceInfo &dev, const uint8_t *codes, const uint8_t *scales, float g,

@@ -178,16 +178,22 @@ template <bool kFp4>
 cudaError_t launch_wq(Route r, const uint8_t *codes, const uint8_t *scales, const float *rs, float g,
                       const uint16_t *x, float *y, int M, int64_t N, int64_t K, cudaStream_t s)
 {
+    cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads);
     cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = set_launch_overlap_attr(attr);
     route_hit(r);
     const bool mma = (r == kRouteNvfp4Mma || r == kRouteFp8Mma);
     const int64_t grid = mma ? (N + kRowsPerCta - 1) / kRowsPerCta : (N + kWarps - 1) / kWarps;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    if (mma) return cudaLaunchKernelEx(&cfg, wq_mma_kernel<kFp4>, codes, scales, rs, g, x, y, M, N, K);
-    return cudaLaunchKernelEx(&cfg, wq_generic_kernel<kFp4>, codes, scales, rs, g, x, y, M, N, K);
+    auto kern = mma ? wq_mma_kernel<kFp4> : wq_generic_kernel<kFp4>;
+    // activations are re-read through L1: keep the default L1/shared split
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), 0, -1);
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, kern, codes, scales, rs, g, x, y, M, N, K);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

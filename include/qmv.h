@@ -88,6 +88,35 @@ QMV_API qmv_status qmv_q4_0_q8_1(const void *w, const void *xq, float *y, int M,
                          qmv_stream_t stream);
 
 /*
+ * Quantize + MMVQ in one kernel: the same result as qmv_quantize_q8_1(x) followed
+ * by qmv_q4_0_q8_1 (bit-identical outputs; the Q8_1 blocks are built in shared
+ * memory by the quantizer's own device code and never written to global memory).
+ * Saves one launch and the Q8_1 round trip per call.
+ *   w  Q4_0 as in qmv_q4_0_q8_1, 16-byte aligned; K a multiple of 256.
+ *   x  fp32 [M][K], 16-byte aligned.   y  fp32 [M][N].
+ * Returns QMV_ERR_SHAPE for shapes the streaming kernel cannot take (use the
+ * two-call path there) and QMV_ERR_ALIGN for a misaligned w or x.
+ */
+QMV_API qmv_status qmv_q4_0_q8_1_fused(const void *w, const float *x, float *y, int M, int64_t N, int64_t K,
+                                       qmv_stream_t stream);
+
+/*
+ * Several independent fused calls with the same M and K in ONE launch: call i
+ * computes y[i] = W[i] x[i] exactly as qmv_q4_0_q8_1_fused(w[i], x[i], y[i], M,
+ * N[i], K) would (bit-identical). Decode runs matrices that read the same input
+ * -- the q, k, v projections of a layer, or its gate and up projections -- one
+ * after another only because each is a separate call; grouping them removes the
+ * dependent launches between them.
+ *   count       1..8 matrices.
+ *   w, x, y, N  HOST arrays of `count` entries (device pointers and row counts),
+ *               read during the call only. Each x[i] may equal another x[j].
+ * Errors as in qmv_q4_0_q8_1_fused, checked per matrix.
+ */
+QMV_API qmv_status qmv_q4_0_q8_1_fused_group(int count, const void *const *w, const float *const *x,
+                                             float *const *y, const int64_t *N, int M, int64_t K,
+                                             qmv_stream_t stream);
+
+/*
  * NVFP4 W4A16 skinny GEMM ("v100-skinny README", section "How QPN works": QPN2).
  *   codes        [N][K/2] bytes, two E2M1 codes per byte: k even in the low
  *                nibble, k odd in the high nibble (OCP MX E2M1 values).
@@ -117,6 +146,20 @@ QMV_API qmv_status qgemm_nvfp4_w4a16(const uint8_t *codes, const uint8_t *scales
  */
 QMV_API qmv_status qgemm_fp8_w8a16(const uint8_t *w, const float *row_scale, const uint16_t *x, float *y,
                            int M, int64_t N, int64_t K, qmv_stream_t stream);
+
+/*
+ * Launch overlap between consecutive calls (programmatic dependent launch),
+ * process-wide, off by default. When enabled, every kernel of this library is
+ * launched so that it may start while the preceding kernel on the stream is
+ * still running: it reads its WEIGHTS (and scales) at once, and waits for the
+ * preceding kernel to finish and flush before it reads activations or writes
+ * outputs. Contract: weights must not be written by the kernel that immediately
+ * precedes a call on its stream (static model weights never are; copies and
+ * memsets are not kernels and keep full ordering). This hides the launch gap and
+ * the pipeline ramp of a chain of small calls, such as the layers of a decode step.
+ */
+QMV_API void qmv_set_launch_overlap(int enable);
+QMV_API int qmv_get_launch_overlap(void);
 
 /* ---------------------------------------------------------------------------
  * Introspection (tests and benchmarks)

@@ -83,6 +83,38 @@ def test_quantize_ties_and_extremes(q):
     assert np.array_equal(q.qmv_quantize_q8_1(xt).cpu().numpy(), oracle.quantize_q8_1(x))
 
 
+def test_quantize_near_ties(q):
+    """Values within a few ulps of k + 1/2 after the division, at scales whose
+    reciprocal is inexact: the kernels must take every rounding decision as the
+    correctly rounded fp32 quotient does."""
+    rng = np.random.default_rng(17)
+    nblk = 2048
+    x = np.zeros((1, 32 * nblk), np.float32)
+    for bi in range(nblk):
+        amax = np.float32(rng.uniform(0.01, 100.0))
+        d = np.float32(amax / np.float32(127.0))
+        blk = np.empty(32, np.float32)
+        blk[0] = amax if bi % 2 else -amax
+        k = rng.integers(-126, 126, 31).astype(np.float32)
+        t = (k + np.float32(0.5)) * d                      # near a tie after x / d
+        steps = rng.integers(-3, 4, 31)
+        blk[1:] = np.array([np.nextafter(tv, np.float32(np.inf) if st > 0 else np.float32(-np.inf))
+                            if st else tv for tv, st in zip(t, steps)], np.float32)
+        for _ in range(2):   # up to a few more ulps
+            blk[1:] = np.where(steps > 1, np.nextafter(blk[1:], np.float32(np.inf)), blk[1:])
+            blk[1:] = np.where(steps < -1, np.nextafter(blk[1:], np.float32(-np.inf)), blk[1:])
+        np.clip(blk, -amax, amax, out=blk)
+        x[0, 32 * bi:32 * (bi + 1)] = blk
+    xt = torch.from_numpy(x).to(DEV)
+    ref = oracle.quantize_q8_1(x)
+    assert np.array_equal(q.qmv_quantize_q8_1(xt).cpu().numpy(), ref)
+    # the fused prologue takes the same decisions: compare against the two-call path
+    from gemm_qmv_quantize_gb300 import synth
+    K = x.shape[1]
+    w = synth.q4_0_weights(64, K, seed=3, device=DEV)
+    assert torch.equal(q.qmv_q4_0_q8_1_fused(w, xt), q.qmv_q4_0_q8_1(w, torch.from_numpy(ref).to(DEV), K))
+
+
 # ---------------------------------------------------------------- Q4_0 MMVQ
 
 def _q4_case(q, M, N, K, seed, offset=0):
@@ -192,3 +224,112 @@ def test_q4_0_empty_and_k0(q):
     w0 = torch.zeros((0, 4096 // 32 * 18), dtype=torch.uint8, device=DEV)
     xq0 = torch.zeros((1, 4096 // 32 * 36), dtype=torch.uint8, device=DEV)
     assert q.qmv_q4_0_q8_1(w0, xq0, 4096).shape == (1, 0)
+
+
+def test_launch_overlap_chain_matches_plain(q):
+    """A dependent chain of calls (each activation produced by the previous call's
+    output, as in decode) gives bit-identical results with launch overlap on."""
+    from gemm_qmv_quantize_gb300 import synth
+    shapes = [(4096, 4096), (11008, 4096), (4096, 11008), (4096, 4096)]
+    ws = [synth.q4_0_weights(n, k, seed=50 + i, device=DEV) for i, (n, k) in enumerate(shapes)]
+    x0 = synth.activations_f32(1, 4096, seed=49, device=DEV)
+
+    def chain():
+        x = x0
+        outs = []
+        for (n, k), w in zip(shapes, ws):
+            xin = x[:, :k] if x.shape[1] >= k else x.repeat(1, (k + x.shape[1] - 1) // x.shape[1])[:, :k]
+            xin = xin.contiguous()
+            y = q.qmv_q4_0_q8_1(w, q.qmv_quantize_q8_1(xin), k)
+            outs.append(y)
+            x = y
+        return [o.clone() for o in outs]
+
+    prev = q.get_launch_overlap()
+    try:
+        q.set_launch_overlap(False)
+        plain = chain()
+        q.set_launch_overlap(True)
+        over = chain()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            graphed = chain()
+        g.replay()
+        torch.cuda.synchronize()
+    finally:
+        q.set_launch_overlap(prev)
+    for a, b, c in zip(plain, over, graphed):
+        assert torch.equal(a, b) and torch.equal(a, c)
+    # and the chain itself is right: check the first call against the oracle
+    xq_ref = oracle.quantize_q8_1(x0.cpu().numpy())
+    y_ref, bound = oracle.q4_0_q8_1(ws[0].cpu().numpy(), xq_ref, 4096)
+    assert_close("chain[0]", plain[0].cpu().numpy(), y_ref, bound)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 4096, 4096), (3, 1000, 11008), (8, 300, 14336), (2, 37, 256),
+                                   (1, 32000, 4096), (5, 777, 4096)])
+def test_q4_0_fused_matches_two_calls(q, M, N, K):
+    """Quantize-in-prologue gives bit-identical outputs to quantize + MMVQ, and meets the oracle."""
+    from gemm_qmv_quantize_gb300 import synth
+    w = synth.q4_0_weights(N, K, seed=N + K + M, device=DEV)
+    x = synth.activations_f32(M, K, seed=N + K + M + 1, device=DEV)
+    x[0, :32] *= 1e-30
+    q.route_reset()
+    y2 = q.qmv_q4_0_q8_1(w, q.qmv_quantize_q8_1(x), K)
+    y1 = q.qmv_q4_0_q8_1_fused(w, x)
+    assert torch.equal(y1, y2)
+    assert q.route_counts()["q4_0_stream_fused_quantize"] == 1
+    rows = synth.sample_rows(N, 64, seed=M).numpy()
+    xq_ref = oracle.quantize_q8_1(x.cpu().numpy())
+    y_ref, bound = oracle.q4_0_q8_1(np.ascontiguousarray(w.cpu().numpy()[rows]), xq_ref, K)
+    assert_close("fused", y1.cpu().numpy()[:, rows], y_ref, bound)
+
+
+def test_q4_0_fused_rejects_unsupported_shapes(q):
+    from gemm_qmv_quantize_gb300 import QmvError, synth
+    w = synth.q4_0_weights(8, 96, seed=1, device=DEV)
+    x = synth.activations_f32(1, 96, seed=2, device=DEV)
+    with pytest.raises(QmvError, match="SHAPE"):
+        q.qmv_q4_0_q8_1_fused(w, x)
+    w = synth.q4_0_weights(8, 512, seed=1, device=DEV)
+    buf = torch.empty(w.numel() + 16, dtype=torch.uint8, device=DEV)
+    wm = buf[2:2 + w.numel()].view(8, -1)
+    with pytest.raises(QmvError, match="ALIGN"):
+        q.qmv_q4_0_q8_1_fused(wm, synth.activations_f32(1, 512, seed=2, device=DEV))
+
+
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_q4_0_fused_group_matches_single_calls(q, M):
+    """A grouped launch of independent matrices (q/k/v-like, with one input shared
+    by two of them) is bit-identical to one fused call per matrix."""
+    from gemm_qmv_quantize_gb300 import synth
+    K = 4096
+    Ns = [4096, 1024, 1024, 11008]
+    ws = [synth.q4_0_weights(n, K, seed=900 + i, device=DEV) for i, n in enumerate(Ns)]
+    xa = synth.activations_f32(M, K, seed=990, device=DEV)
+    xb = synth.activations_f32(M, K, seed=991, device=DEV)
+    xs = [xa, xa, xb, xb]
+    q.route_reset()
+    outs = q.qmv_q4_0_q8_1_fused_group(ws, xs)
+    singles = [q.qmv_q4_0_q8_1_fused(w, x) for w, x in zip(ws, xs)]
+    for a, b in zip(outs, singles):
+        assert torch.equal(a, b)
+    assert q.route_counts()["q4_0_stream_fused_quantize"] == 5
+    rows = synth.sample_rows(Ns[3], 32, seed=M).numpy()
+    y_ref, bound = oracle.q4_0_q8_1(np.ascontiguousarray(ws[3].cpu().numpy()[rows]),
+                                    oracle.quantize_q8_1(xb.cpu().numpy()), K)
+    assert_close("group[3]", outs[3].cpu().numpy()[:, rows], y_ref, bound)
+
+
+def test_q4_0_fused_group_validation(q):
+    from gemm_qmv_quantize_gb300 import _binding
+    L = _binding.lib()
+    import ctypes
+    P = ctypes.c_void_p * 9
+    n = (ctypes.c_int64 * 9)(*([64] * 9))
+    z = P(*([0x10000] * 9))
+    assert L.qmv_q4_0_q8_1_fused_group(9, z, z, z, n, 1, 4096, None) == -2     # count > 8
+    assert L.qmv_q4_0_q8_1_fused_group(0, z, z, z, n, 1, 4096, None) == -2
+    assert L.qmv_q4_0_q8_1_fused_group(2, z, z, z, n, 1, 4000, None) == -2     # K % 256
+    bad = P(0x10000, 0x10008)
+    assert L.qmv_q4_0_q8_1_fused_group(2, bad, z, z, n, 1, 4096, None) == -3   # w not 16-aligned
