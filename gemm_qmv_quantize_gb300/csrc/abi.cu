@@ -304,9 +304,10 @@ qmv_status qmv_error_flags(uint32_t *flags, int clear)
 {
     if (!flags) return QMV_ERR_NULL;
     if (cudaDeviceSynchronize() != cudaSuccess) return QMV_ERR_CUDA;
-    uint32_t w = 0;
+    uint32_t w = 0, w2 = 0;
     if (read_error_word_q4_0(&w, clear != 0) != cudaSuccess) return QMV_ERR_CUDA;
-    *flags = w;
+    if (read_error_word_wq(&w2, clear != 0) != cudaSuccess) return QMV_ERR_CUDA;
+    *flags = w | w2;
     return QMV_OK;
 }
 

@@ -104,6 +104,18 @@ __device__ __forceinline__ void bulk_copy_g2s(void *dst, const void *src, uint32
         : "memory");
 }
 
+// 2-D tensor copy global -> shared of one box at coordinates (x bytes, y rows),
+// completion counted on `bar`. The tensor map lives in kernel parameter space.
+__device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, int y, uint64_t *bar,
+                                            uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 
 // Wait until the grid this launch depends on has completed and its writes are

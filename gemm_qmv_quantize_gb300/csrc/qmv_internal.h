@@ -81,5 +81,6 @@ cudaError_t launch_fp8(Route r, const DeviceInfo &dev, const uint8_t *w, const f
 
 // Device error words of each translation unit (read synchronously; optionally cleared).
 cudaError_t read_error_word_q4_0(uint32_t *out, bool clear);
+cudaError_t read_error_word_wq(uint32_t *out, bool clear);
 
 }  // namespace qmv

@@ -20,116 +20,219 @@
 //    the order of k, so each lane takes a contiguous 32-byte run of its row
 //    (one 128-byte line per four lanes: full-line, coalesced loads) and the
 //    activation fragment is gathered in the same k order.
-//  * Split K: a CTA owns 16 rows; its 8 warps take interleaved 128-byte steps
-//    of the rows (adjacent lines in flight together), then reduce in shared memory.
+//  * Split K: a persistent CTA walks 16-row tiles; its 8 warps take interleaved
+//    128-byte steps of the tile's rows (adjacent lines in flight together), then
+//    reduce in shared memory.
+//  * Weight streaming: each step's 16 x 128-byte box of codes (and 16 x 16-byte box
+//    of E4M3 scales) is one 2-D tensor copy (TMA) into the warp's ring of shared-
+//    memory slots, with the hardware 128-byte swizzle so the fragment reads are
+//    bank-conflict free and zero fill past the last row. Every warp keeps S steps in
+//    flight across tile boundaries, and the first copies are issued before the
+//    programmatic-dependency wait.
+//  * Activations: staged once per CTA in shared memory when they fit, in an
+//    XOR-swizzled layout (16-byte chunk c of a row stored at c ^ 2((c >> 3) & 3),
+//    row stride 16 mod 32 bytes) that makes the fragment reads bank-conflict free;
+//    else read through L1.
+#include <algorithm>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "qmv_device.cuh"
 #include "qmv_internal.h"
 
 namespace qmv {
 namespace {
 
+__device__ uint32_t g_wq_error;
+
 constexpr int kThreads = 256;
 constexpr int kWarps = 8;
 constexpr int kRowsPerCta = 16;
 constexpr int kStepBytes = 128;   // bytes of one weight row per warp step
 
+// Row stride of the staged activations (16 mod 32 bytes) and the chunk swizzle.
+__host__ __device__ inline uint32_t xs_row_stride(int64_t K) { return static_cast<uint32_t>(K * 2 + 16); }
+__device__ __forceinline__ uint32_t xs_chunk(uint32_t c) { return c ^ (2u * ((c >> 3) & 3u)); }
+
+constexpr int kCodesBox = kRowsPerCta * kStepBytes;   // 2048 bytes: 16 rows x 128 bytes
+constexpr int kScalesBox = kRowsPerCta * 16;          // 256 bytes: 16 rows x 16 scales
+
+struct WqLayout {
+    uint32_t off_codes, off_scales, off_bar, off_x, total;
+};
+
+// Shared memory: per-warp rings of codes boxes (1024-byte aligned for the swizzle),
+// of scale boxes, their mbarriers, then the staged activations.
+__host__ __device__ inline WqLayout wq_layout(int S, uint32_t xbytes)
+{
+    WqLayout L;
+    L.off_codes = 0;
+    L.off_scales = static_cast<uint32_t>(kWarps * S * kCodesBox);
+    L.off_bar = L.off_scales + static_cast<uint32_t>(kWarps * S * kScalesBox);
+    L.off_x = (L.off_bar + static_cast<uint32_t>(kWarps * S) * 8u + 127u) & ~127u;
+    L.total = L.off_x + xbytes;
+    return L;
+}
+
 // kFp4: NVFP4 (256 k per step, E4M3 group scales); else FP8 (128 k per step, row scale).
-template <bool kFp4>
-__global__ void __launch_bounds__(kThreads) wq_mma_kernel(const uint8_t *__restrict__ codes,
-                                                         const uint8_t *__restrict__ scales,
+// kXSmem: activations staged in shared memory.
+template <bool kFp4, bool kXSmem>
+__global__ void __launch_bounds__(kThreads) wq_mma_kernel(const __grid_constant__ CUtensorMap tm_codes,
+                                                         const __grid_constant__ CUtensorMap tm_scales,
                                                          const float *__restrict__ row_scale, float g,
                                                          const uint16_t *__restrict__ x, float *__restrict__ y,
-                                                         int M, int64_t N, int64_t K)
+                                                         int M, int64_t N, int64_t K, int S)
 {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ float red[kWarps][kRowsPerCta][9];
+    // the 128-byte swizzle needs 1024-byte aligned boxes (1 KB extra is allocated)
+    uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     constexpr int kStepK = kFp4 ? 2 * kStepBytes : kStepBytes;
     constexpr int kXWords = kStepK / 8;    // this lane's activation words per step (4 k per 2 words)
+    constexpr int kXChunks = kXWords / 4;  // ... in 16-byte chunks
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, t = lane & 3;
-    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * kRowsPerCta;
-    // Rows past N read row 0 (valid memory); their results are discarded.
-    const int64_t ra = row0 + gid < N ? row0 + gid : 0;
-    const int64_t rb = row0 + gid + 8 < N ? row0 + gid + 8 : 0;
-    const int64_t row_bytes = kFp4 ? K / 2 : K;
-    const uint8_t *pa = codes + ra * row_bytes + 32 * t;
-    const uint8_t *pb = codes + rb * row_bytes + 32 * t;
-    const uint8_t *sa_ptr = kFp4 ? scales + ra * (K / 16) + 4 * t : nullptr;
-    const uint8_t *sb_ptr = kFp4 ? scales + rb * (K / 16) + 4 * t : nullptr;
+    const int64_t ntiles = (N + kRowsPerCta - 1) / kRowsPerCta;
+    const int nsteps = static_cast<int>(K / kStepK);
     const bool has_x = gid < M;
-    const uint16_t *xp = x + (has_x ? gid : 0) * K + (kStepK / 4) * t;
-    const int64_t nsteps = K / kStepK;
+    const uint32_t RS = xs_row_stride(K);
+    const WqLayout L = wq_layout(S, kXSmem ? static_cast<uint32_t>(M) * RS : 0u);
+    uint8_t *codes_ring = smem + L.off_codes + warp * S * kCodesBox;
+    uint8_t *scales_ring = smem + L.off_scales + warp * S * kScalesBox;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.off_bar) + warp * S;
+    uint8_t *xs = smem + L.off_x;
     const uint64_t pol = policy_evict_first();
 
+    // This warp's items: (tile, step) for tiles blockIdx.x, +gridDim.x, ... and
+    // steps warp, warp + 8, ...; lane 0 keeps S of them in flight.
+    int64_t p_tile = blockIdx.x;
+    int p_step = warp;
+    auto issue = [&](int slot) {
+        const int y0 = static_cast<int>(p_tile * kRowsPerCta);
+        mbar_arrive_expect_tx(&bars[slot], kFp4 ? kCodesBox + kScalesBox : kCodesBox);
+        tma_load_2d(codes_ring + slot * kCodesBox, &tm_codes, p_step * kStepBytes, y0, &bars[slot], pol);
+        if (kFp4) tma_load_2d(scales_ring + slot * kScalesBox, &tm_scales, p_step * 16, y0, &bars[slot], pol);
+        p_step += kWarps;
+        if (p_step >= nsteps) {
+            p_step = warp;
+            p_tile += gridDim.x;
+        }
+    };
+    const bool any = warp < nsteps;
+    if (lane == 0) {
+        for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+        fence_barrier_init();
+        // weights do not depend on the preceding kernel: start streaming them now
+        for (int i = 0; i < S && any && p_tile < ntiles; ++i) issue(i);
+    }
+    __syncwarp();
     grid_launch_dependents();
     grid_dependency_wait();
 
-    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int64_t s = warp; s < nsteps; s += kWarps) {
-        const int64_t off = s * kStepBytes;
-        const uint4 a0 = ld_stream_v4(pa + off, pol), a1 = ld_stream_v4(pa + off + 16, pol);
-        const uint4 b0 = ld_stream_v4(pb + off, pol), b1 = ld_stream_v4(pb + off + 16, pol);
-        const uint32_t cwa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-        const uint32_t cwb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-        uint32_t xw[kXWords];
-        if (has_x) {
-#pragma unroll
-            for (int i = 0; i < kXWords / 4; ++i) {
-                const uint4 v = ld_shared_v4(xp + s * kStepK + 8 * i);
-                xw[4 * i] = v.x;
-                xw[4 * i + 1] = v.y;
-                xw[4 * i + 2] = v.z;
-                xw[4 * i + 3] = v.w;
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < kXWords; ++i) xw[i] = 0u;
-        }
-        if (kFp4) {
-            // 4 scale bytes: group q covers this lane's codes bytes 8q..8q+7 (k 64t+16q ..).
-            const uint32_t sa = ld_stream_u32(sa_ptr + s * 16, pol);
-            const uint32_t sb = ld_stream_u32(sb_ptr + s * 16, pol);
-            const uint32_t sa01 = e4m3x2_to_f16x2(sa & 0xffffu), sa23 = e4m3x2_to_f16x2(sa >> 16);
-            const uint32_t sb01 = e4m3x2_to_f16x2(sb & 0xffffu), sb23 = e4m3x2_to_f16x2(sb >> 16);
-            const uint32_t sca[4] = {dup_lo16(sa01), dup_hi16(sa01), dup_lo16(sa23), dup_hi16(sa23)};
-            const uint32_t scb[4] = {dup_lo16(sb01), dup_hi16(sb01), dup_lo16(sb23), dup_hi16(sb23)};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                // word i = codes bytes 4i..4i+3 = k 8i..8i+7 of this lane's run; group i/2
-                uint32_t ha[4], hb[4];
-                e2m1x8_to_f16x2(cwa[i], ha);
-                e2m1x8_to_f16x2(cwb[i], hb);
-                const uint32_t ga = sca[i >> 1], gb = scb[i >> 1];
-                mma_16816(d, hmul2_u32(ha[0], ga), hmul2_u32(hb[0], gb), hmul2_u32(ha[1], ga),
-                          hmul2_u32(hb[1], gb), xw[4 * i], xw[4 * i + 1]);
-                mma_16816(d, hmul2_u32(ha[2], ga), hmul2_u32(hb[2], gb), hmul2_u32(ha[3], ga),
-                          hmul2_u32(hb[3], gb), xw[4 * i + 2], xw[4 * i + 3]);
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                // word j = codes bytes 4j..4j+3 = k 4j..4j+3 of this lane's run
-                mma_16816(d, e4m3x2_to_f16x2(cwa[j] & 0xffffu), e4m3x2_to_f16x2(cwb[j] & 0xffffu),
-                          e4m3x2_to_f16x2(cwa[j] >> 16), e4m3x2_to_f16x2(cwb[j] >> 16), xw[2 * j],
-                          xw[2 * j + 1]);
-            }
+    if (kXSmem) {
+        // stage x [M][K] fp16, 16-byte chunks, swizzled
+        const int chunks = static_cast<int>(K / 8);
+        for (int i = tid; i < M * chunks; i += kThreads) {
+            const int m = i / chunks, c = i - m * chunks;
+            const uint4 v = ld_shared_v4(x + static_cast<int64_t>(m) * K + 8 * c);
+            *reinterpret_cast<uint4 *>(xs + m * RS + 16 * xs_chunk(static_cast<uint32_t>(c))) = v;
         }
     }
-
-    red[warp][gid][2 * t] = d[0];
-    red[warp][gid][2 * t + 1] = d[1];
-    red[warp][gid + 8][2 * t] = d[2];
-    red[warp][gid + 8][2 * t + 1] = d[3];
     __syncthreads();
-    if (tid < kRowsPerCta * 8) {
-        const int r = tid >> 3, m = tid & 7;
-        const int64_t n = row0 + r;
-        if (m < M && n < N) {
-            float s = 0.0f;
+
+    uint32_t it = 0;   // position in this warp's item sequence
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+        for (int s = warp; s < nsteps; s += kWarps, ++it) {
+            const int slot = static_cast<int>(it % S);
+            if (!mbar_wait_sleep(&bars[slot], (it / S) & 1)) {
+                if (lane == 0) atomicOr(&g_wq_error, kErrWaitTimeout);
+                return;
+            }
+            // codes of rows gid and gid+8: 16-byte chunks 2t, 2t+1 of the row (swizzled by row & 7)
+            const uint8_t *cb = codes_ring + slot * kCodesBox;
+            const uint4 a0 = *reinterpret_cast<const uint4 *>(cb + gid * 128 + 16 * ((2 * t) ^ gid));
+            const uint4 a1 = *reinterpret_cast<const uint4 *>(cb + gid * 128 + 16 * ((2 * t + 1) ^ gid));
+            const uint4 b0 = *reinterpret_cast<const uint4 *>(cb + (gid + 8) * 128 + 16 * ((2 * t) ^ gid));
+            const uint4 b1 = *reinterpret_cast<const uint4 *>(cb + (gid + 8) * 128 + 16 * ((2 * t + 1) ^ gid));
+            uint32_t sa = 0, sb = 0;
+            if (kFp4) {
+                const uint8_t *sbx = scales_ring + slot * kScalesBox;
+                sa = *reinterpret_cast<const uint32_t *>(sbx + gid * 16 + 4 * t);
+                sb = *reinterpret_cast<const uint32_t *>(sbx + (gid + 8) * 16 + 4 * t);
+            }
+            __syncwarp();   // the slot is in registers: refill it
+            if (lane == 0 && p_tile < ntiles) issue(slot);
+
+            uint32_t xw[kXWords];
+            if (has_x) {
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) s += red[w][r][m];
-            y[m * N + n] = s * (kFp4 ? g : row_scale[n]);
+                for (int i = 0; i < kXChunks; ++i) {
+                    uint4 v;
+                    if (kXSmem) {
+                        const uint32_t c = static_cast<uint32_t>(s) * (kStepK / 8) + kXChunks * t + i;
+                        v = *reinterpret_cast<const uint4 *>(xs + gid * RS + 16 * xs_chunk(c));
+                    } else {
+                        v = ld_shared_v4(x + gid * K + static_cast<int64_t>(s) * kStepK + (kStepK / 4) * t + 8 * i);
+                    }
+                    xw[4 * i] = v.x;
+                    xw[4 * i + 1] = v.y;
+                    xw[4 * i + 2] = v.z;
+                    xw[4 * i + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < kXWords; ++i) xw[i] = 0u;
+            }
+            const uint32_t cwa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const uint32_t cwb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+            if (kFp4) {
+                // 4 scale bytes: group q covers this lane's codes bytes 8q..8q+7 (k 64t+16q ..).
+                const uint32_t sa01 = e4m3x2_to_f16x2(sa & 0xffffu), sa23 = e4m3x2_to_f16x2(sa >> 16);
+                const uint32_t sb01 = e4m3x2_to_f16x2(sb & 0xffffu), sb23 = e4m3x2_to_f16x2(sb >> 16);
+                const uint32_t sca[4] = {dup_lo16(sa01), dup_hi16(sa01), dup_lo16(sa23), dup_hi16(sa23)};
+                const uint32_t scb[4] = {dup_lo16(sb01), dup_hi16(sb01), dup_lo16(sb23), dup_hi16(sb23)};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    // word i = codes bytes 4i..4i+3 = k 8i..8i+7 of this lane's run; group i/2
+                    uint32_t ha[4], hb[4];
+                    e2m1x8_to_f16x2(cwa[i], ha);
+                    e2m1x8_to_f16x2(cwb[i], hb);
+                    const uint32_t ga = sca[i >> 1], gb = scb[i >> 1];
+                    mma_16816(d, hmul2_u32(ha[0], ga), hmul2_u32(hb[0], gb), hmul2_u32(ha[1], ga),
+                              hmul2_u32(hb[1], gb), xw[4 * i], xw[4 * i + 1]);
+                    mma_16816(d, hmul2_u32(ha[2], ga), hmul2_u32(hb[2], gb), hmul2_u32(ha[3], ga),
+                              hmul2_u32(hb[3], gb), xw[4 * i + 2], xw[4 * i + 3]);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    // word j = codes bytes 4j..4j+3 = k 4j..4j+3 of this lane's run
+                    mma_16816(d, e4m3x2_to_f16x2(cwa[j] & 0xffffu), e4m3x2_to_f16x2(cwb[j] & 0xffffu),
+                              e4m3x2_to_f16x2(cwa[j] >> 16), e4m3x2_to_f16x2(cwb[j] >> 16), xw[2 * j],
+                              xw[2 * j + 1]);
+                }
+            }
         }
+        red[warp][gid][2 * t] = d[0];
+        red[warp][gid][2 * t + 1] = d[1];
+        red[warp][gid + 8][2 * t] = d[2];
+        red[warp][gid + 8][2 * t + 1] = d[3];
+        __syncthreads();
+        if (tid < kRowsPerCta * 8) {
+            const int r = tid >> 3, m = tid & 7;
+            const int64_t n = tile * kRowsPerCta + r;
+            if (m < M && n < N) {
+                float sum = 0.0f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) sum += red[w][r][m];
+                y[m * N + n] = sum * (kFp4 ? g : row_scale[n]);
+            }
+        }
+        __syncthreads();   // red is reused by the next tile
     }
 }
 
@@ -174,9 +277,41 @@ __global__ void __launch_bounds__(kThreads) wq_generic_kernel(const uint8_t *__r
     }
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Row-major byte matrix [rows][cols] (row stride = cols) as a 2-D tensor map with a
+// box of box_cols bytes x 16 rows.
+cudaError_t encode_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, uint32_t box_cols,
+                       CUtensorMapSwizzle swizzle)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+    const cuuint32_t box[2] = {box_cols, static_cast<cuuint32_t>(kRowsPerCta)};
+    const cuuint32_t estride[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estride,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <bool kFp4>
-cudaError_t launch_wq(Route r, const uint8_t *codes, const uint8_t *scales, const float *rs, float g,
-                      const uint16_t *x, float *y, int M, int64_t N, int64_t K, cudaStream_t s)
+cudaError_t launch_wq(Route r, const DeviceInfo &dev, const uint8_t *codes, const uint8_t *scales, const float *rs,
+                      float g, const uint16_t *x, float *y, int M, int64_t N, int64_t K, cudaStream_t s)
 {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = {};
@@ -185,12 +320,38 @@ cudaError_t launch_wq(Route r, const uint8_t *codes, const uint8_t *scales, cons
     cfg.attrs = attr;
     cfg.numAttrs = set_launch_overlap_attr(attr);
     route_hit(r);
-    const bool mma = (r == kRouteNvfp4Mma || r == kRouteFp8Mma);
-    const int64_t grid = mma ? (N + kRowsPerCta - 1) / kRowsPerCta : (N + kWarps - 1) / kWarps;
+    if (r == kRouteNvfp4Mma || r == kRouteFp8Mma) {
+        const int64_t ntiles = (N + kRowsPerCta - 1) / kRowsPerCta;
+        const int S = std::max(1, std::min(8, env_int("QMV_WQ_SLOTS", 4)));
+        // Activations in shared memory when a CTA stays within the SM's opt-in limit.
+        const uint32_t xbytes = static_cast<uint32_t>(M) * xs_row_stride(K);
+        const bool xsmem = wq_layout(S, xbytes).total + 1024 <= static_cast<uint32_t>(dev.smem_optin) &&
+                           xbytes <= static_cast<uint32_t>(env_int("QMV_WQ_XSMEM_MAX", 160 * 1024));
+        const WqLayout L = wq_layout(S, xsmem ? xbytes : 0u);
+        const int per_sm = std::max(1, std::min(4, dev.smem_per_sm / static_cast<int>(L.total + 7 * 1024)));
+        cfg.gridDim =
+            dim3(static_cast<unsigned>(std::min<int64_t>(ntiles, static_cast<int64_t>(dev.sm_count) * per_sm)));
+        CUtensorMap tm_codes, tm_scales;
+        cudaError_t e = encode_map(&tm_codes, codes, N, kFp4 ? K / 2 : K, kStepBytes, CU_TENSOR_MAP_SWIZZLE_128B);
+        if (e != cudaSuccess) return e;
+        if (kFp4) {
+            e = encode_map(&tm_scales, scales, N, K / 16, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+            if (e != cudaSuccess) return e;
+        } else {
+            tm_scales = tm_codes;   // unused
+        }
+        auto kern = xsmem ? wq_mma_kernel<kFp4, true> : wq_mma_kernel<kFp4, false>;
+        cfg.dynamicSmemBytes = L.total + 1024;
+        // shared memory for the rings (and activations); L1 keeps the rest
+        e = ensure_smem_attr(reinterpret_cast<const void *>(kern), static_cast<int>(L.total + 1024),
+                             xsmem ? cudaSharedmemCarveoutMaxShared : -1);
+        if (e != cudaSuccess) return e;
+        return cudaLaunchKernelEx(&cfg, kern, tm_codes, tm_scales, rs, g, x, y, M, N, K, S);
+    }
+    const int64_t grid = (N + kWarps - 1) / kWarps;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    auto kern = mma ? wq_mma_kernel<kFp4> : wq_generic_kernel<kFp4>;
-    // activations are re-read through L1: keep the default L1/shared split
+    auto kern = wq_generic_kernel<kFp4>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), 0, -1);
     if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, kern, codes, scales, rs, g, x, y, M, N, K);
@@ -199,6 +360,14 @@ cudaError_t launch_wq(Route r, const uint8_t *codes, const uint8_t *scales, cons
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
+
+cudaError_t read_error_word_wq(uint32_t *out, bool clear)
+{
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_wq_error, sizeof(uint32_t));
+    if (e != cudaSuccess || !clear) return e;
+    const uint32_t zero = 0;
+    return cudaMemcpyToSymbol(g_wq_error, &zero, sizeof(uint32_t));
+}
 
 Route plan_nvfp4(const uint8_t *codes, const uint8_t *scales, const uint16_t *x, int64_t K)
 {
@@ -211,16 +380,16 @@ Route plan_fp8(const uint8_t *w, const uint16_t *x, int64_t K)
     return (K % 128 == 0 && aligned16(w) && aligned16(x)) ? kRouteFp8Mma : kRouteFp8Generic;
 }
 
-cudaError_t launch_nvfp4(Route r, const DeviceInfo &, const uint8_t *codes, const uint8_t *scales, float g,
+cudaError_t launch_nvfp4(Route r, const DeviceInfo &dev, const uint8_t *codes, const uint8_t *scales, float g,
                          const uint16_t *x, float *y, int M, int64_t N, int64_t K, cudaStream_t s)
 {
-    return launch_wq<true>(r, codes, scales, nullptr, g, x, y, M, N, K, s);
+    return launch_wq<true>(r, dev, codes, scales, nullptr, g, x, y, M, N, K, s);
 }
 
-cudaError_t launch_fp8(Route r, const DeviceInfo &, const uint8_t *w, const float *rs, const uint16_t *x, float *y,
+cudaError_t launch_fp8(Route r, const DeviceInfo &dev, const uint8_t *w, const float *rs, const uint16_t *x, float *y,
                        int M, int64_t N, int64_t K, cudaStream_t s)
 {
-    return launch_wq<false>(r, w, nullptr, rs, 0.0f, x, y, M, N, K, s);
+    return launch_wq<false>(r, dev, w, nullptr, rs, 0.0f, x, y, M, N, K, s);
 }
 
 }  // namespace qmv
