@@ -127,6 +127,44 @@ def dist_env():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+class Dist:
+    """Rank plumbing of a replica run: barrier and max over ranks (no-ops for one rank)."""
+
+    def __init__(self, world: int, backend: str = "nccl", device=None):
+        self.world = world
+        self.device = device
+        self.dist = None
+        if world > 1:
+            import torch.distributed as dist
+            if backend == "nccl":
+                dist.init_process_group(backend, device_id=device)
+            else:
+                dist.init_process_group(backend)
+            self.dist = dist
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, v: float) -> float:
+        if self.dist is None:
+            return v
+        import torch
+        t = torch.tensor([float(v)], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.dist is not None:
+            self.dist.destroy_process_group()
+            self.dist = None
+
+
+def replica_rate(units_per_rank: float, seconds_max: float, world: int) -> float:
+    """Whole-job rate of independent replicas: all ranks' units over the slowest rank's time."""
+    return units_per_rank * world / seconds_max
+
+
 def measured_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -342,21 +380,8 @@ def run_ours(args, rank, world, local_rank):
     import gemm_qmv_quantize_gb300 as q
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-
-    def barrier():
-        if dist is not None:
-            dist.barrier()
-
-    def max_over_ranks(v):
-        if dist is None:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    dist = Dist(world, "nccl", dev)
+    barrier, max_over_ranks = dist.barrier, dist.max
 
     stack = Stack(args.workload, dev, seed=1234 + rank, fused=not args.unfused, grouped=not args.serial)
     stream = torch.cuda.Stream(device=dev)
@@ -364,8 +389,7 @@ def run_ours(args, rank, world, local_rank):
     q.set_launch_overlap(not args.no_overlap)
     with torch.cuda.stream(stream):
         line = _run_ours_on_stream(args, rank, world, local_rank, stack, stream, barrier, max_over_ranks)
-    if dist is not None:
-        dist.destroy_process_group()
+    dist.close()
     return line if rank == 0 else None
 
 
@@ -387,7 +411,7 @@ def _run_ours_on_stream(args, rank, world, local_rank, stack, stream, barrier, m
     t = max_over_ranks(t_step_total)
     ms_per_step = t / args.steps * 1e3
     step_s = t / args.steps
-    gbs = stack.bytes_per_step * world / step_s / 1e9
+    gbs = replica_rate(stack.bytes_per_step, step_s, world) / 1e9
     kernels = stack.kernels_per_step() * args.steps if not args.eager else \
         sum(q.route_counts().values()) - launches0
 

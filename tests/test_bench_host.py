@@ -1,0 +1,82 @@
+"""Host-side logic of bench.py on CPU: the replica plumbing across gloo ranks, the
+workload tables, and the reference (oracle) arm under torchrun."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+from conftest import ROOT
+
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
+    d = bench.Dist(world, backend="gloo")
+    d.barrier()
+    local = 1.0 + rank            # rank 1 is the slow one
+    t = d.max(local)
+    out.put((rank, t, bench.replica_rate(100.0, t, world)))
+    d.close()
+
+
+def test_replicas_take_the_max_over_ranks():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [2.0, 2.0]            # every rank sees the slowest time
+    assert all(abs(r[2] - 100.0) < 1e-12 for r in res)  # 2 ranks x 100 units / 2 s
+
+
+def test_single_rank_is_a_noop():
+    d = bench.Dist(1)
+    d.barrier()
+    assert d.max(3.5) == 3.5
+    d.close()
+
+
+def test_workload_tables():
+    mats = bench.llama2_7b_stack()
+    assert len(mats) == 225
+    assert sum(bench.weight_bytes(*m) for m in mats) == 3_716_481_024
+    st = bench.llama2_7b_stages()
+    assert len(st) == 129 and sorted(i for s in st for i in s) == list(range(225))
+    mixed = bench.dense_27b_stack(True)
+    assert sum(bench.weight_bytes(*m) for m in mixed) == 12_769_615_872
+    dense = bench.dense_27b_stack(False)
+    assert sum(bench.weight_bytes(*m) for m in dense) == 11_890_851_840
+    assert sum(1 for f, _, _ in mixed if f == "fp8") == 32
+
+
+@pytest.mark.timeout(600)
+def test_reference_arm_under_torchrun_prints_once():
+    port = _free_port()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node=2",
+           "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
+           "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "1", "--ref-seconds", "1.5",
+           "--workload", "q4_0_4096sq_m1"]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
