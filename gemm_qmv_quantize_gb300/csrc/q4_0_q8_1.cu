@@ -153,6 +153,16 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+// Division by a kernel-wide divisor 0 < n: q = umulhi(u, ceil(2^32 / n)) equals
+// u / n whenever u * n < 2^32 (the error u * (ceil - 2^32/n) / 2^32 stays below
+// the distance 1/n from u/n to the next integer); the staging indices are bounded
+// by the shared-memory size, far inside that range.
+__device__ __forceinline__ uint32_t div_magic(int n) { return 0xffffffffu / static_cast<uint32_t>(n) + 1u; }
+__device__ __forceinline__ int div_by(int u, uint32_t magic)
+{
+    return static_cast<int>(__umulhi(static_cast<uint32_t>(u), magic));
+}
+
 // Shared-memory record of the unit holding block b of activation row gm (= matrix * M + m).
 __device__ __forceinline__ uint8_t *act_block(uint8_t *smem, const Q4Layout &L, int gm, int b)
 {
@@ -161,21 +171,22 @@ __device__ __forceinline__ uint8_t *act_block(uint8_t *smem, const Q4Layout &L, 
 
 // Quantize the group's fp32 activations to Q8_1 straight into the shared-memory
 // staging layout, a quad of lanes per 32-value block (the quantizer's own code).
-template <int M>
+template <int M, typename AfterLoads>
 __device__ __forceinline__ void stage_fused(const Q4Group &grp, int nb, uint8_t *smem, const Q4Layout &L,
-                                            int nthreads)
+                                            int nthreads, AfterLoads after_loads)
 {
     constexpr int kPasses = 4;   // loads of up to 4 passes are issued before any is used
     const int part = threadIdx.x & 3;
     const int total = grp.count * M * nb;   // blocks over (matrix, row m, block b)
     const int quads = nthreads >> 2;
+    const uint32_t inv_nb = div_magic(nb);
     for (int base = 0; base < total; base += kPasses * quads) {   // uniform trip count: whole warps shuffle
         float v[kPasses][8];
 #pragma unroll
         for (int ps = 0; ps < kPasses; ++ps) {
             const int u = base + ps * quads + static_cast<int>(threadIdx.x >> 2);
             const int uc = u < total ? u : 0;
-            const int gm = uc / nb, b = uc - gm * nb;
+            const int gm = div_by(uc, inv_nb), b = uc - gm * nb;
             const int gi = gm / M, m = gm - gi * M;
             const float *src = static_cast<const float *>(grp.x[gi]) + static_cast<int64_t>(m) * (nb * 32) + b * 32 +
                                8 * part;
@@ -186,13 +197,14 @@ __device__ __forceinline__ void stage_fused(const Q4Group &grp, int nb, uint8_t 
                 v[ps][4] = c.x; v[ps][5] = c.y; v[ps][6] = c.z; v[ps][7] = c.w;
             }
         }
+        if (base == 0) after_loads();
 #pragma unroll
         for (int ps = 0; ps < kPasses; ++ps) {
             if (base + ps * quads >= total) break;   // uniform over the CTA
             const int u = base + ps * quads + static_cast<int>(threadIdx.x >> 2);
             const Q8Quad r = q8_1_quantize_quad(v[ps]);
             if (u < total) {
-                const int gm = u / nb, b = u - gm * nb;
+                const int gm = div_by(u, inv_nb), b = u - gm * nb;
                 uint8_t *rec = act_block(smem, L, gm, b);
                 const int j = b & 7;
                 *reinterpret_cast<uint2 *>(rec + 32 * j + 8 * part) = make_uint2(r.qlo, r.qhi);
@@ -206,13 +218,15 @@ __device__ __forceinline__ void stage_fused(const Q4Group &grp, int nb, uint8_t 
 }
 
 // Copy the group's Q8_1 activations into the staging layout, adding 8 * sum(q) per block.
-template <int M>
+template <int M, typename AfterLoads>
 __device__ __forceinline__ void stage_q8_1(const Q4Group &grp, int nb, uint8_t *smem, const Q4Layout &L,
-                                           int nthreads)
+                                           int nthreads, AfterLoads after_loads)
 {
     const int total = grp.count * M * nb;
+    const uint32_t inv_nb = div_magic(nb);
+    after_loads();
     for (int u = threadIdx.x; u < total; u += nthreads) {
-        const int gm = u / nb, b = u - gm * nb;
+        const int gm = div_by(u, inv_nb), b = u - gm * nb;
         const int gi = gm / M, m = gm - gi * M;
         const uint32_t *src = reinterpret_cast<const uint32_t *>(static_cast<const uint8_t *>(grp.x[gi]) +
                                                                  (static_cast<int64_t>(m) * nb + b) * 36);
@@ -237,7 +251,7 @@ __device__ __forceinline__ void stage_q8_1(const Q4Group &grp, int nb, uint8_t *
 // matrix 0 instead of y (a single-matrix group).
 template <int M, bool kDots, bool kFused>
 __global__ void __launch_bounds__(M == 1 ? kStreamThreads : kStreamThreadsWide) q4_0_stream_kernel(
-    const __grid_constant__ Q4Group grp, int32_t *__restrict__ dots, int64_t K, int S)
+    const __grid_constant__ Q4Group grp, int32_t *__restrict__ dots, int64_t K, int S, int P)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warps = blockDim.x >> 5;
@@ -264,8 +278,7 @@ __global__ void __launch_bounds__(M == 1 ? kStreamThreads : kStreamThreadsWide) 
     const uint8_t *span = grp.w[mi] + r0 * L.rowbytes;
     const uint64_t pol = policy_evict_first();
 
-    auto issue = [&](int c) {   // chunk c into slot c % S
-        const int slot = c % S;
+    auto issue = [&](int c, int slot) {   // chunk c into a free slot
         const uint32_t bytes = static_cast<uint32_t>(min(kChunkUnits, TU - c * kChunkUnits)) * kUnitBytes;
         mbar_arrive_expect_tx(&bars[slot], bytes);
         bulk_copy_g2s(ring + slot * L.slotbytes, span + static_cast<int64_t>(c) * (kChunkUnits * kUnitBytes), bytes,
@@ -274,28 +287,38 @@ __global__ void __launch_bounds__(M == 1 ? kStreamThreads : kStreamThreadsWide) 
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
-        // weights do not depend on the preceding kernel: start streaming them now
-        for (int c = 0; c < S && c < nchunks; ++c) issue(c);
+        // weights do not depend on the preceding kernel: start streaming P slots now
+        for (int c = 0; c < P && c < nchunks; ++c) issue(c, c);
     }
     __syncwarp();
     grid_launch_dependents();
     grid_dependency_wait();
 
+    // the rest of the ring is requested once the activation loads are in flight,
+    // so that they do not queue behind a full ring of weight copies
+    auto fill_ring = [&]() {
+        if (lane == 0)
+            for (int c = P; c < S && c < nchunks; ++c) issue(c, c);
+    };
     if (kFused)
-        stage_fused<M>(grp, nb, smem, L, blockDim.x);
+        stage_fused<M>(grp, nb, smem, L, blockDim.x, fill_ring);
     else
-        stage_q8_1<M>(grp, nb, smem, L, blockDim.x);
+        stage_q8_1<M>(grp, nb, smem, L, blockDim.x, fill_ring);
     __syncthreads();   // the only CTA-wide barrier
 
     const uint8_t *act0 = smem + L.off_act + (mi * M) * L.act_m_stride;
-    float *ym = grp.y[mi];
-    float carry[M];
+    float *ym = grp.y[mi] + r0;
+    // This lane's unit in the chunk: row rr of the span, unit uin of the row. Chunk
+    // c + 1 starts 32 units later, i.e. dr rows and du units further on.
+    int rr = lane / U, uin = lane - rr * U;
+    const int dr = kChunkUnits / U, du = kChunkUnits - dr * U;
+    float carry[M];   // partial sum of the row left open by the previous chunk
 #pragma unroll
     for (int m = 0; m < M; ++m) carry[m] = 0.0f;
-    int carry_row = -1;
+    int slot = 0;
+    uint32_t phase = 0;
     for (int c = 0; c < nchunks; ++c) {
-        const int slot = c % S;
-        if (!mbar_wait_sleep(&bars[slot], (c / S) & 1)) {
+        if (!mbar_wait_sleep(&bars[slot], phase)) {
             if (lane == 0) {
                 atomicOr(&g_q4_error, kErrWaitTimeout);
                 // let this warp's other copies land before the CTA can release its memory
@@ -304,10 +327,7 @@ __global__ void __launch_bounds__(M == 1 ? kStreamThreads : kStreamThreadsWide) 
             }
             return;
         }
-        const int gu = c * kChunkUnits + lane;   // unit index in the span
-        const bool live = gu < TU;
-        const int rr = live ? gu / U : -1;       // row within the span
-        const int uin = live ? gu - rr * U : 0;  // unit within its row
+        const bool live = c * kChunkUnits + lane < TU;
         float v[M];
 #pragma unroll
         for (int m = 0; m < M; ++m) v[m] = 0.0f;
@@ -316,35 +336,45 @@ __global__ void __launch_bounds__(M == 1 ? kStreamThreads : kStreamThreadsWide) 
                               L.act_m_stride, v, kDots ? dots + (r0 + rr) * nb + 8 * uin : nullptr, Nm * nb);
         }
         __syncwarp();   // every lane is done with the slot
-        if (lane == 0 && c + S < nchunks) issue(c + S);
+        if (lane == 0 && c + S < nchunks) issue(c + S, slot);
         if (!kDots) {
-            // segmented inclusive scan over lanes of the same row (rows increase with lane)
+            // Inclusive scan within the row: the lanes of one row are consecutive,
+            // min(uin, lane) of them precede this lane in the chunk.
+            const int before = min(uin, lane);
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
-                const int ro = __shfl_up_sync(0xffffffffu, rr, d);
 #pragma unroll
                 for (int m = 0; m < M; ++m) {
                     const float o = __shfl_up_sync(0xffffffffu, v[m], d);
-                    if (lane >= d && ro == rr) v[m] += o;
+                    if (d <= before) v[m] += o;
                 }
             }
-            const int rnext = __shfl_down_sync(0xffffffffu, rr, 1);
-            const bool tail = live && (lane == 31 || rnext != rr);   // last lane of its row here
-            if (tail && rr == carry_row) {
+            const bool row_end = live && uin == U - 1;
+            // the row that began in an earlier chunk is closed (or carried on) by its last lane here
+            if (live && (row_end || lane == 31) && uin >= lane) {
 #pragma unroll
                 for (int m = 0; m < M; ++m) v[m] += carry[m];
             }
-            const bool row_end = tail && uin == U - 1;
             if (row_end) {
 #pragma unroll
-                for (int m = 0; m < M; ++m) ym[m * Nm + r0 + rr] = v[m];
+                for (int m = 0; m < M; ++m) ym[m * Nm + rr] = v[m];
             }
-            // the chunk's last live lane passes an unfinished row on to the next chunk
-            const int last = min(31, TU - 1 - c * kChunkUnits);
-            const bool open = __shfl_sync(0xffffffffu, static_cast<int>(tail && !row_end), last) != 0;
-            carry_row = open ? __shfl_sync(0xffffffffu, rr, last) : -1;
+            const bool open = (__ballot_sync(0xffffffffu, row_end) >> 31) == 0;   // lane 31's row continues
 #pragma unroll
-            for (int m = 0; m < M; ++m) carry[m] = __shfl_sync(0xffffffffu, v[m], last);
+            for (int m = 0; m < M; ++m) {
+                const float t = __shfl_sync(0xffffffffu, v[m], 31);
+                carry[m] = open ? t : 0.0f;
+            }
+        }
+        uin += du;
+        rr += dr;
+        if (uin >= U) {
+            uin -= U;
+            ++rr;
+        }
+        if (++slot == S) {
+            slot = 0;
+            phase ^= 1u;
         }
     }
 }
@@ -424,7 +454,7 @@ cudaError_t launch_m(const Q4Plan &p, const Q4Group &grp, int32_t *dots, int64_t
         if (e != cudaSuccess) return e;
         cfg.blockDim = dim3(static_cast<unsigned>(p.warps * 32));   // consumers + the producer
         cfg.dynamicSmemBytes = static_cast<size_t>(p.smem_bytes);
-        return cudaLaunchKernelEx(&cfg, kern, grp, dots, K, p.stages);
+        return cudaLaunchKernelEx(&cfg, kern, grp, dots, K, p.stages, p.prefetch);
     }
     if (kFused || grp.count != 1) return cudaErrorInvalidValue;   // these need the streaming kernel
     cfg.blockDim = dim3(kThreads);
@@ -461,6 +491,7 @@ cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t 
     plan->route = kRouteQ4_0Generic;
     plan->warps = kWarps;
     plan->stages = 0;
+    plan->prefetch = 0;
     plan->smem_bytes = 0;
     plan->grid = static_cast<int>((N + kWarps - 1) / kWarps);
     if (!aligned || K % 256 != 0) return cudaSuccess;
@@ -480,6 +511,7 @@ cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t 
     plan->route = kRouteQ4_0Stream;
     plan->warps = warps;
     plan->stages = S;
+    plan->prefetch = std::max(0, std::min(S, env_int("QMV_Q4_PREFETCH", S)));
     plan->chunk_units = kChunkUnits;
     plan->smem_bytes = static_cast<int>(q4_layout(act_rows, K, warps, S).total);
     plan->grid = static_cast<int>(ctas);

@@ -19,8 +19,22 @@ struct Q8Quad {
     int sum;             // sum of the block's 32 values of q (every lane of the quad)
 };
 
+// Four int32 in [-127, 127] packed as int8 bytes, element order.
+__device__ __forceinline__ uint32_t pack_s8x4(int a, int b, int c, int d)
+{
+    return __byte_perm(__byte_perm(a, b, 0x0040), __byte_perm(c, d, 0x0040), 0x5410);
+}
+
 // v: the 8 consecutive values 8p..8p+7 of the block held by quad lane p = lane % 4.
 // Every lane of the warp must call this together (it shuffles within quads).
+//
+// q = roundf(x / d) needs the correctly rounded quotient only where it decides the
+// rounding. |x / d| <= 127 (1 + 2^-23), and x * fl(1/d) is within 2^-15 of fl(x / d)
+// (two roundings of at most 2^-24 relative each), so when x * fl(1/d) lies farther
+// than 2^-13 from a half-integer both round to the same integer, and there round to
+// nearest (rint) and round half away (roundf) agree. Near a tie, or when 1/d
+// overflows, the value is recomputed with the IEEE quotient and roundf. The clamp
+// to [-127, 127] never binds: the largest quotient rounds to 127.
 __device__ __forceinline__ Q8Quad q8_1_quantize_quad(const float (&v)[8])
 {
     float amax = 0.0f;
@@ -30,32 +44,29 @@ __device__ __forceinline__ Q8Quad q8_1_quantize_quad(const float (&v)[8])
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     Q8Quad r;
     r.d = amax / 127.0f;   // IEEE division (the library is built without fast-math)
-    // q = roundf(v / d) needs the correctly rounded quotient only where it decides
-    // the rounding: v * fl(1/d) is within 2^-15 of fl(v / d) (|v / d| <= 127, two
-    // roundings of 2^-24 relative each), so away from a tie (fraction farther than
-    // 2^-13 from 1/2) both round to the same integer; near a tie, divide exactly.
-    const float rcp = 1.0f / r.d;
-    const bool fast = isfinite(rcp);
-    int sum = 0;
-    uint32_t packed[2] = {0u, 0u};
+    const float inv = 1.0f / r.d;
+    const bool fast = isfinite(inv);
+    const float rcp = r.d == 0.0f ? 0.0f : inv;   // d == 0: every q is 0
+    int q[8];
+    uint32_t slow = 0;
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        int q = 0;
-        if (r.d != 0.0f) {
-            float t = v[i] * rcp;
-            const float a = fabsf(t);
-            if (!fast || fabsf((a - floorf(a)) - 0.5f) < 0x1p-13f) t = v[i] / r.d;
-            t = roundf(t);
-            t = fminf(fmaxf(t, -127.0f), 127.0f);
-            q = static_cast<int>(t);
-        }
-        sum += q;
-        packed[i >> 2] |= (static_cast<uint32_t>(q) & 0xffu) << (8 * (i & 3));
+        const float t = v[i] * rcp;
+        const float n = rintf(t);
+        q[i] = static_cast<int>(n);
+        if (fabsf(t - n) > 0.5f - 0x1p-13f) slow |= 1u << i;
     }
+    if (!fast && r.d != 0.0f) slow = 0xffu;
+    if (slow) {   // rare: decide the rounding with the IEEE quotient
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (slow & (1u << i)) q[i] = static_cast<int>(fminf(fmaxf(roundf(v[i] / r.d), -127.0f), 127.0f));
+    }
+    r.qlo = pack_s8x4(q[0], q[1], q[2], q[3]);
+    r.qhi = pack_s8x4(q[4], q[5], q[6], q[7]);
+    int sum = __dp4a(static_cast<int>(r.qlo), 0x01010101, __dp4a(static_cast<int>(r.qhi), 0x01010101, 0));
     sum += __shfl_xor_sync(0xffffffffu, sum, 1);
     sum += __shfl_xor_sync(0xffffffffu, sum, 2);
-    r.qlo = packed[0];
-    r.qhi = packed[1];
     r.sum = sum;
     return r;
 }

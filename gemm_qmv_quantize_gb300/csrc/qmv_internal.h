@@ -42,6 +42,7 @@ struct Q4Plan {
     int warps;         // streaming kernel: warps per CTA
     int stages;        // streaming kernel: ring slots per warp
     int chunk_units;   // 144-byte units per ring slot
+    int prefetch;      // streaming kernel: slots filled before the programmatic-dependency wait
     int grid;
     int smem_bytes;
 };
