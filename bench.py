@@ -109,14 +109,17 @@ def weight_bytes(fmt, n, k):
     return n * k + 4 * n   # fp8 + fp32 row scale
 
 
-def call_bytes(fmt, M, n, k, fused=False):
-    """Algorithmic bytes of one call: weights + scales + activations + outputs.
-    Q4_0 reads Q8_1 activations, or fp32 ones when the quantize is fused in."""
+def act_bytes(fmt, M, k, fused=False):
+    """Activation bytes a call reads: Q4_0 reads Q8_1 activations, or fp32 ones when
+    the quantize is fused in; NVFP4 and FP8 read fp16."""
     if fmt == "q4_0":
-        act = M * k * 4 if fused else M * (k // 32) * Q8_1_BLOCK
-    else:
-        act = M * k * 2
-    return weight_bytes(fmt, n, k) + act + M * n * 4
+        return M * k * 4 if fused else M * (k // 32) * Q8_1_BLOCK
+    return M * k * 2
+
+
+def call_bytes(fmt, M, n, k, fused=False):
+    """Algorithmic bytes of one call: weights + scales + activations + outputs."""
+    return weight_bytes(fmt, n, k) + act_bytes(fmt, M, k, fused) + M * n * 4
 
 
 # ----------------------------------------------------------------------------- host-side plumbing
@@ -267,13 +270,12 @@ class Stack:
         w = WORKLOADS[name]
         self.name, self.M, self.mats, self.device = name, w["M"], w["mats"](), device
         self.fused = fused
-        # Dependent stages: matrices of a stage read the same input and are
+        # Dependent stages: matrices of a stage read the same input tensor and are
         # independent of each other; a grouped launch runs them together.
-        if grouped and fused and "stages" in w:
-            self.stages = w["stages"]()
-        else:
-            self.stages = [[i] for i in range(len(self.mats))]
-        assert sorted(i for st in self.stages for i in st) == list(range(len(self.mats)))
+        deps = w["stages"]() if "stages" in w else [[i] for i in range(len(self.mats))]
+        assert sorted(i for st in deps for i in st) == list(range(len(self.mats)))
+        self.input_of = {i: j for j, st in enumerate(deps) for i in st}
+        self.stages = deps if grouped and fused else [[i] for i in range(len(self.mats))]
         M = self.M
         self.weights = []
         for i, (fmt, n, k) in enumerate(self.mats):
@@ -284,21 +286,25 @@ class Stack:
                 self.weights.append(synth.nvfp4_weights(n, k, s, device))
             else:
                 self.weights.append(synth.fp8_weights(n, k, s, device))
-        # activations and outputs: views into two contiguous buffers (one copy each way for e2e)
-        self.x_is_f32 = [fmt == "q4_0" for fmt, _, _ in self.mats]
-        x_elems = [M * k for _, _, k in self.mats]
-        self.x_bytes = sum(e * (4 if f else 2) for e, f in zip(x_elems, self.x_is_f32))
+        # activations (one per stage input) and outputs: views into two contiguous
+        # buffers (one copy each way for e2e)
+        first = [st[0] for st in deps]
+        for st in deps:
+            assert len({(self.mats[i][0], self.mats[i][2]) for i in st}) == 1, "a shared input has one format and K"
+        x_is_f32 = [self.mats[i][0] == "q4_0" for i in first]
+        x_sizes = [M * self.mats[i][2] * (4 if f else 2) for i, f in zip(first, x_is_f32)]
+        self.x_bytes = sum(x_sizes)
         self.x_buf = torch.empty(self.x_bytes, dtype=torch.uint8, device=device)
-        self.xs, off = [], 0
-        for i, (fmt, n, k) in enumerate(self.mats):
-            nbytes = M * k * (4 if self.x_is_f32[i] else 2)
-            dt = torch.float32 if self.x_is_f32[i] else torch.float16
-            self.xs.append(self.x_buf[off:off + nbytes].view(dt).view(M, k))
+        inputs, off = [], 0
+        for i, f, nbytes in zip(first, x_is_f32, x_sizes):
+            dt = torch.float32 if f else torch.float16
+            inputs.append(self.x_buf[off:off + nbytes].view(dt).view(M, self.mats[i][2]))
             off += nbytes
         g = torch.Generator(device=device)
         g.manual_seed(seed)
-        for x in self.xs:
+        for x in inputs:
             x.copy_(torch.randn(x.shape, generator=g, device=device, dtype=torch.float32))
+        self.xs = [inputs[self.input_of[i]] for i in range(len(self.mats))]
         self.y_elems = sum(M * n for _, n, _ in self.mats)
         self.y_buf = torch.empty(self.y_elems, dtype=torch.float32, device=device)
         self.ys, off = [], 0
@@ -307,7 +313,7 @@ class Stack:
             off += M * n
         self.xqs = [torch.empty((M, k // 32 * Q8_1_BLOCK), dtype=torch.uint8, device=device)
                     if fmt == "q4_0" else None for fmt, _, k in self.mats]
-        self.bytes_per_step = sum(call_bytes(fmt, M, n, k, fused) for fmt, n, k in self.mats)
+        self.bytes_per_step = sum(self.launch_bytes(st) for st in self.stages)
         self.weight_bytes = sum(weight_bytes(fmt, n, k) for fmt, n, k in self.mats)
 
     def run(self, events=None):
@@ -343,6 +349,15 @@ class Stack:
             q.qgemm_fp8_w8a16(wt[0], wt[1], x, out=y)
         if ev is not None:
             ev[1].record()
+
+    def launch_bytes(self, st):
+        """Algorithmic bytes of one launch: weights, scales and outputs of its matrices,
+        and each distinct input once."""
+        b = sum(weight_bytes(fmt, n, k) + self.M * n * 4 for fmt, n, k in (self.mats[i] for i in st))
+        for j in sorted({self.input_of[i] for i in st}):
+            i = next(i for i in st if self.input_of[i] == j)
+            b += act_bytes(self.mats[i][0], self.M, self.mats[i][2], self.fused)
+        return b
 
     def kernels_per_step(self):
         return sum(1 if len(st) > 1 else (2 if (self.mats[st[0]][0] == "q4_0" and not self.fused) else 1)
@@ -485,8 +500,7 @@ def kernel_roofline(args, stack, stream, barrier):
     kname = {"q4_0": "q4_0_stream_fused_quantize" if stack.fused else "q4_0_stream_dp4a",
              "nvfp4": "nvfp4_mma_m16n8k16", "fp8": "fp8_mma_m16n8k16"}[fmt_main]
     sel = [j for j, st in enumerate(stack.stages) if stack.mats[st[0]][0] == fmt_main]
-    stage_bytes = [sum(call_bytes(stack.mats[i][0], stack.M, stack.mats[i][1], stack.mats[i][2], stack.fused)
-                       for i in stack.stages[j]) for j in sel]
+    stage_bytes = [stack.launch_bytes(stack.stages[j]) for j in sel]
     bytes_per_launch = sum(stage_bytes) / len(sel)
     dur = sum(total[j] for j in sel) / (len(sel) * steps)
     achieved = bytes_per_launch / dur / 1e9

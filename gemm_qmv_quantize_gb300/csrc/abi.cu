@@ -160,6 +160,8 @@ static Q4Group single_group(const void *w, const void *x, float *y, int64_t N)
 {
     Q4Group g{};
     g.count = 1;
+    g.nx = 1;
+    g.xslot[0] = 0;
     g.w[0] = static_cast<const uint8_t *>(w);
     g.x[0] = x;
     g.y[0] = y;
@@ -230,8 +232,12 @@ qmv_status qmv_q4_0_q8_1_fused_group(int count, const void *const *w, const floa
         if (!w[i] || !x[i]) return QMV_ERR_NULL;
         if (misaligned(w[i], 16) || misaligned(x[i], 16)) return QMV_ERR_ALIGN;
         grp.w[i] = static_cast<const uint8_t *>(w[i]);
-        grp.x[i] = x[i];
         grp.y[i] = y[i];
+        // matrices given the same activation stage (and quantize) it once
+        int j = 0;
+        while (j < grp.nx && grp.x[j] != x[i]) ++j;
+        if (j == grp.nx) grp.x[grp.nx++] = x[i];
+        grp.xslot[i] = j;
     }
     DeviceInfo dev;
     cudaError_t e = current_device_info(&dev);

@@ -52,7 +52,7 @@ struct Q4Layout {
     uint32_t off_act, act_m_stride, off_ring, ring_warp_stride, off_bar, total;
 };
 
-// Shared memory: staged activations (act_rows = matrices x M rows), then one ring of
+// Shared memory: staged activations (act_rows = distinct activations x M rows), then one ring of
 // S slots of 32 units per warp, then the warps' mbarriers.
 __host__ __device__ inline Q4Layout q4_layout(int act_rows, int64_t K, int warps, int S)
 {
@@ -177,7 +177,7 @@ __device__ __forceinline__ void stage_fused(const Q4Group &grp, int nb, uint8_t 
 {
     constexpr int kPasses = 4;   // loads of up to 4 passes are issued before any is used
     const int part = threadIdx.x & 3;
-    const int total = grp.count * M * nb;   // blocks over (matrix, row m, block b)
+    const int total = grp.nx * M * nb;   // blocks over (activation, row m, block b)
     const int quads = nthreads >> 2;
     const uint32_t inv_nb = div_magic(nb);
     for (int base = 0; base < total; base += kPasses * quads) {   // uniform trip count: whole warps shuffle
@@ -222,7 +222,7 @@ template <int M, typename AfterLoads>
 __device__ __forceinline__ void stage_q8_1(const Q4Group &grp, int nb, uint8_t *smem, const Q4Layout &L,
                                            int nthreads, AfterLoads after_loads)
 {
-    const int total = grp.count * M * nb;
+    const int total = grp.nx * M * nb;
     const uint32_t inv_nb = div_magic(nb);
     after_loads();
     for (int u = threadIdx.x; u < total; u += nthreads) {
@@ -255,7 +255,7 @@ __global__ void __launch_bounds__(M == 1 ? kStreamThreads : kStreamThreadsWide) 
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warps = blockDim.x >> 5;
-    const Q4Layout L = q4_layout(M * grp.count, K, warps, S);
+    const Q4Layout L = q4_layout(M * grp.nx, K, warps, S);
     const int nb = static_cast<int>(K >> 5);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int U = static_cast<int>(L.units);
@@ -277,6 +277,7 @@ __global__ void __launch_bounds__(M == 1 ? kStreamThreads : kStreamThreadsWide) 
     const int nchunks = (TU + kChunkUnits - 1) / kChunkUnits;
     const uint8_t *span = grp.w[mi] + r0 * L.rowbytes;
     const uint64_t pol = policy_evict_first();
+    const int pw = min(S, (P + warps - 1 - warp) / warps);   // this warp's share of the P early chunks
 
     auto issue = [&](int c, int slot) {   // chunk c into a free slot
         const uint32_t bytes = static_cast<uint32_t>(min(kChunkUnits, TU - c * kChunkUnits)) * kUnitBytes;
@@ -287,8 +288,9 @@ __global__ void __launch_bounds__(M == 1 ? kStreamThreads : kStreamThreadsWide) 
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
         fence_barrier_init();
-        // weights do not depend on the preceding kernel: start streaming P slots now
-        for (int c = 0; c < P && c < nchunks; ++c) issue(c, c);
+        // weights do not depend on the preceding kernel: the CTA's first P chunks
+        // (spread over its warps) are requested now
+        for (int c = 0; c < pw && c < nchunks; ++c) issue(c, c);
     }
     __syncwarp();
     grid_launch_dependents();
@@ -298,7 +300,7 @@ __global__ void __launch_bounds__(M == 1 ? kStreamThreads : kStreamThreadsWide) 
     // so that they do not queue behind a full ring of weight copies
     auto fill_ring = [&]() {
         if (lane == 0)
-            for (int c = P; c < S && c < nchunks; ++c) issue(c, c);
+            for (int c = pw; c < S && c < nchunks; ++c) issue(c, c);
     };
     if (kFused)
         stage_fused<M>(grp, nb, smem, L, blockDim.x, fill_ring);
@@ -306,7 +308,7 @@ __global__ void __launch_bounds__(M == 1 ? kStreamThreads : kStreamThreadsWide) 
         stage_q8_1<M>(grp, nb, smem, L, blockDim.x, fill_ring);
     __syncthreads();   // the only CTA-wide barrier
 
-    const uint8_t *act0 = smem + L.off_act + (mi * M) * L.act_m_stride;
+    const uint8_t *act0 = smem + L.off_act + (grp.xslot[mi] * M) * L.act_m_stride;
     float *ym = grp.y[mi] + r0;
     // This lane's unit in the chunk: row rr of the span, unit uin of the row. Chunk
     // c + 1 starts 32 units later, i.e. dr rows and du units further on.
@@ -497,7 +499,7 @@ cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t 
     if (!aligned || K % 256 != 0) return cudaSuccess;
 
     // Warps hide latency (each also issues its own copies); slots are the bytes in flight.
-    const int act_rows = M * grp.count;
+    const int act_rows = M * grp.nx;
     const int cap = (M == 1 ? kStreamThreads : kStreamThreadsWide) / 32;
     int warps = std::max(1, std::min(cap, env_int("QMV_Q4_WARPS", cap)));
     const int S = std::max(1, std::min(8, env_int("QMV_Q4_SLOTS", 2)));
@@ -511,7 +513,7 @@ cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t 
     plan->route = kRouteQ4_0Stream;
     plan->warps = warps;
     plan->stages = S;
-    plan->prefetch = std::max(0, std::min(S, env_int("QMV_Q4_PREFETCH", S)));
+    plan->prefetch = std::max(0, std::min(S * warps, env_int("QMV_Q4_PREFETCH", 4)));
     plan->chunk_units = kChunkUnits;
     plan->smem_bytes = static_cast<int>(q4_layout(act_rows, K, warps, S).total);
     plan->grid = static_cast<int>(ctas);

@@ -42,7 +42,7 @@ struct Q4Plan {
     int warps;         // streaming kernel: warps per CTA
     int stages;        // streaming kernel: ring slots per warp
     int chunk_units;   // 144-byte units per ring slot
-    int prefetch;      // streaming kernel: slots filled before the programmatic-dependency wait
+    int prefetch;      // streaming kernel: chunks per CTA requested before the programmatic-dependency wait
     int grid;
     int smem_bytes;
 };
@@ -62,7 +62,9 @@ constexpr int kMaxGroup = 8;
 struct Q4Group {
     int count;
     const uint8_t *w[kMaxGroup];
-    const void *x[kMaxGroup];      // fp32 [M][K] (fused) or Q8_1 [M][K/32]
+    int nx;                        // distinct activations: matrices reading the same one share it
+    int xslot[kMaxGroup];          // matrix i reads activation x[xslot[i]]
+    const void *x[kMaxGroup];      // fp32 [M][K] (fused) or Q8_1 [M][K/32], x[0 .. nx)
     float *y[kMaxGroup];           // fp32 [M][N_i]
     int64_t row_start[kMaxGroup + 1];
     int cta_start[kMaxGroup + 1];   // streaming kernel: warps of matrix i are [cta_start[i], cta_start[i+1])

@@ -298,17 +298,18 @@ def test_q4_0_fused_rejects_unsupported_shapes(q):
         q.qmv_q4_0_q8_1_fused(wm, synth.activations_f32(1, 512, seed=2, device=DEV))
 
 
-@pytest.mark.parametrize("M", [1, 3, 8])
-def test_q4_0_fused_group_matches_single_calls(q, M):
-    """A grouped launch of independent matrices (q/k/v-like, with one input shared
-    by two of them) is bit-identical to one fused call per matrix."""
+@pytest.mark.parametrize("M,pattern", [(1, (0, 0, 1, 1)), (3, (0, 0, 1, 1)), (8, (0, 0, 1, 1)),
+                                       (1, (0, 1, 2, 3)), (1, (0, 1, 0, 2)), (4, (2, 0, 2, 1))])
+def test_q4_0_fused_group_matches_single_calls(q, M, pattern):
+    """A grouped launch of independent matrices (q/k/v-like; matrices given the same
+    input tensor share its staging) is bit-identical to one fused call per matrix."""
     from gemm_qmv_quantize_gb300 import synth
     K = 4096
     Ns = [4096, 1024, 1024, 11008]
     ws = [synth.q4_0_weights(n, K, seed=900 + i, device=DEV) for i, n in enumerate(Ns)]
-    xa = synth.activations_f32(M, K, seed=990, device=DEV)
-    xb = synth.activations_f32(M, K, seed=991, device=DEV)
-    xs = [xa, xa, xb, xb]
+    inputs = [synth.activations_f32(M, K, seed=990 + j, device=DEV) for j in range(max(pattern) + 1)]
+    xs = [inputs[j] for j in pattern]
+    xb = xs[3]
     q.route_reset()
     outs = q.qmv_q4_0_q8_1_fused_group(ws, xs)
     singles = [q.qmv_q4_0_q8_1_fused(w, x) for w, x in zip(ws, xs)]
