@@ -20,9 +20,11 @@
 //    the order of k, so each lane takes a contiguous 32-byte run of its row
 //    (one 128-byte line per four lanes: full-line, coalesced loads) and the
 //    activation fragment is gathered in the same k order.
-//  * Split K: a persistent CTA walks 16-row tiles; its 8 warps take interleaved
-//    128-byte steps of the tile's rows (adjacent lines in flight together), then
-//    reduce in shared memory.
+//  * Split K: a persistent CTA walks its 16-row tiles in rounds of B tiles; the 8
+//    warps take interleaved 128-byte steps of the round (adjacent lines of the same
+//    rows in flight together, which keeps DRAM pages open), then reduce in shared
+//    memory. B = 8 / gcd(steps per tile, 8), at most 4, makes the steps of a round
+//    a multiple of 8, so every warp gets the same number of steps.
 //  * Weight streaming: each step's 16 x 128-byte box of codes (and 16 x 16-byte box
 //    of E4M3 scales) is one 2-D tensor copy (TMA) into the warp's ring of shared-
 //    memory slots, with the hardware 128-byte swizzle so the fragment reads are
@@ -51,6 +53,7 @@ constexpr int kThreads = 256;
 constexpr int kWarps = 8;
 constexpr int kRowsPerCta = 16;
 constexpr int kStepBytes = 128;   // bytes of one weight row per warp step
+constexpr int kMaxRound = 4;      // tiles per round at most
 
 // Row stride of the staged activations (16 mod 32 bytes) and the chunk swizzle.
 __host__ __device__ inline uint32_t xs_row_stride(int64_t K) { return static_cast<uint32_t>(K * 2 + 16); }
@@ -59,19 +62,23 @@ __device__ __forceinline__ uint32_t xs_chunk(uint32_t c) { return c ^ (2u * ((c 
 constexpr int kCodesBox = kRowsPerCta * kStepBytes;   // 2048 bytes: 16 rows x 128 bytes
 constexpr int kScalesBox = kRowsPerCta * 16;          // 256 bytes: 16 rows x 16 scales
 
+constexpr int kRedPitch = 9;      // floats per partial row (8 columns + pad)
+
 struct WqLayout {
-    uint32_t off_codes, off_scales, off_bar, off_x, total;
+    uint32_t off_codes, off_scales, off_bar, off_red, off_x, total;
 };
 
 // Shared memory: per-warp rings of codes boxes (1024-byte aligned for the swizzle),
-// of scale boxes, their mbarriers, then the staged activations.
-__host__ __device__ inline WqLayout wq_layout(int S, uint32_t xbytes)
+// of scale boxes, their mbarriers, the round's partial sums [warp][B * 16 rows][9],
+// then the staged activations.
+__host__ __device__ inline WqLayout wq_layout(int S, int B, uint32_t xbytes)
 {
     WqLayout L;
     L.off_codes = 0;
     L.off_scales = static_cast<uint32_t>(kWarps * S * kCodesBox);
     L.off_bar = L.off_scales + static_cast<uint32_t>(kWarps * S * kScalesBox);
-    L.off_x = (L.off_bar + static_cast<uint32_t>(kWarps * S) * 8u + 127u) & ~127u;
+    L.off_red = (L.off_bar + static_cast<uint32_t>(kWarps * S) * 8u + 15u) & ~15u;
+    L.off_x = (L.off_red + static_cast<uint32_t>(kWarps * B * kRowsPerCta * kRedPitch) * 4u + 127u) & ~127u;
     L.total = L.off_x + xbytes;
     return L;
 }
@@ -83,10 +90,9 @@ __global__ void __launch_bounds__(kThreads) wq_mma_kernel(const __grid_constant_
                                                          const __grid_constant__ CUtensorMap tm_scales,
                                                          const float *__restrict__ row_scale, float g,
                                                          const uint16_t *__restrict__ x, float *__restrict__ y,
-                                                         int M, int64_t N, int64_t K, int S)
+                                                         int M, int64_t N, int64_t K, int S, int B)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    __shared__ float red[kWarps][kRowsPerCta][9];
     // the 128-byte swizzle needs 1024-byte aligned boxes (1 KB extra is allocated)
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     constexpr int kStepK = kFp4 ? 2 * kStepBytes : kStepBytes;
@@ -99,34 +105,49 @@ __global__ void __launch_bounds__(kThreads) wq_mma_kernel(const __grid_constant_
     const int nsteps = static_cast<int>(K / kStepK);
     const bool has_x = gid < M;
     const uint32_t RS = xs_row_stride(K);
-    const WqLayout L = wq_layout(S, kXSmem ? static_cast<uint32_t>(M) * RS : 0u);
+    const WqLayout L = wq_layout(S, B, kXSmem ? static_cast<uint32_t>(M) * RS : 0u);
     uint8_t *codes_ring = smem + L.off_codes + warp * S * kCodesBox;
     uint8_t *scales_ring = smem + L.off_scales + warp * S * kScalesBox;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.off_bar) + warp * S;
     uint8_t *xs = smem + L.off_x;
+    // partial sums of the round: red(w, row of the round, column)
+    float *red_base = reinterpret_cast<float *>(smem + L.off_red);
+    auto red = [&](int w, int rr, int m) -> float & {
+        return red_base[(w * B * kRowsPerCta + rr) * kRedPitch + m];
+    };
     const uint64_t pol = policy_evict_first();
 
-    // This warp's items: (tile, step) for tiles blockIdx.x, +gridDim.x, ... and
-    // steps warp, warp + 8, ...; lane 0 keeps S of them in flight.
-    int64_t p_tile = blockIdx.x;
-    int p_step = warp;
+    // This CTA's tiles blockIdx.x + gridDim.x * lt, lt < nt, in rounds of B tiles; a
+    // round's items j = tb * nsteps + step (tile tb of the round), and this warp's
+    // are j = warp, warp + 8, ... Lane 0 keeps S of them in flight.
+    const int nt = static_cast<int>((ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x);
+    // first item of a round for this warp: tile warp / nsteps, step warp % nsteps
+    const int tb0 = warp / nsteps, s0 = warp - tb0 * nsteps;
+    int p_lt = tb0, p_step = s0, p_rend = min(B, nt);   // producer: local tile, step, end of its round
     auto issue = [&](int slot) {
-        const int y0 = static_cast<int>(p_tile * kRowsPerCta);
+        const int y0 = static_cast<int>((blockIdx.x + static_cast<int64_t>(gridDim.x) * p_lt) * kRowsPerCta);
         mbar_arrive_expect_tx(&bars[slot], kFp4 ? kCodesBox + kScalesBox : kCodesBox);
         tma_load_2d(codes_ring + slot * kCodesBox, &tm_codes, p_step * kStepBytes, y0, &bars[slot], pol);
         if (kFp4) tma_load_2d(scales_ring + slot * kScalesBox, &tm_scales, p_step * 16, y0, &bars[slot], pol);
         p_step += kWarps;
-        if (p_step >= nsteps) {
-            p_step = warp;
-            p_tile += gridDim.x;
+        while (p_step >= nsteps) {   // once when nsteps >= 8
+            p_step -= nsteps;
+            ++p_lt;
+        }
+        if (p_lt >= p_rend) {   // next round: restart at this warp's first item
+            p_lt = p_rend + tb0;
+            p_step = s0;
+            p_rend = min(p_rend + B, nt);
         }
     };
-    const bool any = warp < nsteps;
+    // rounds before the last hold a multiple of 8 items, so a warp with an item in
+    // one round has one in every round but perhaps the last
+    auto pending = [&]() { return p_lt < p_rend; };
     if (lane == 0) {
         for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
         fence_barrier_init();
         // weights do not depend on the preceding kernel: start streaming them now
-        for (int i = 0; i < S && any && p_tile < ntiles; ++i) issue(i);
+        for (int i = 0; i < S && pending(); ++i) issue(i);
     }
     __syncwarp();
     grid_launch_dependents();
@@ -143,12 +164,29 @@ __global__ void __launch_bounds__(kThreads) wq_mma_kernel(const __grid_constant_
     }
     __syncthreads();
 
-    uint32_t it = 0;   // position in this warp's item sequence
-    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+    int slot = 0;   // ring position of this warp's next item
+    uint32_t phase = 0;
+    for (int round = 0; round * B < nt; ++round) {
+        const int bt = min(B, nt - round * B);
         float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        for (int s = warp; s < nsteps; s += kWarps, ++it) {
-            const int slot = static_cast<int>(it % S);
-            if (!mbar_wait_sleep(&bars[slot], (it / S) & 1)) {
+        int cur = 0;   // tile of the round that d accumulates
+        // zero the partials of this warp for tiles of the round it has no step of
+        auto flush = [&](int upto) {   // store d as tile cur, zeros for cur+1 .. upto-1
+            for (int tb = cur; tb < upto; ++tb) {
+                const bool mine = tb == cur;
+                red(warp, tb * kRowsPerCta + gid, 2 * t) = mine ? d[0] : 0.0f;
+                red(warp, tb * kRowsPerCta + gid, 2 * t + 1) = mine ? d[1] : 0.0f;
+                red(warp, tb * kRowsPerCta + gid + 8, 2 * t) = mine ? d[2] : 0.0f;
+                red(warp, tb * kRowsPerCta + gid + 8, 2 * t + 1) = mine ? d[3] : 0.0f;
+            }
+            d[0] = d[1] = d[2] = d[3] = 0.0f;
+        };
+        for (int tb = tb0, s = s0; tb < bt;) {
+            if (tb != cur) {
+                flush(tb);
+                cur = tb;
+            }
+            if (!mbar_wait_sleep(&bars[slot], phase)) {
                 if (lane == 0) atomicOr(&g_wq_error, kErrWaitTimeout);
                 return;
             }
@@ -165,7 +203,7 @@ __global__ void __launch_bounds__(kThreads) wq_mma_kernel(const __grid_constant_
                 sb = *reinterpret_cast<const uint32_t *>(sbx + (gid + 8) * 16 + 4 * t);
             }
             __syncwarp();   // the slot is in registers: refill it
-            if (lane == 0 && p_tile < ntiles) issue(slot);
+            if (lane == 0 && pending()) issue(slot);
 
             uint32_t xw[kXWords];
             if (has_x) {
@@ -216,23 +254,29 @@ __global__ void __launch_bounds__(kThreads) wq_mma_kernel(const __grid_constant_
                               xw[2 * j + 1]);
                 }
             }
+            if (++slot == S) {
+                slot = 0;
+                phase ^= 1u;
+            }
+            s += kWarps;
+            while (s >= nsteps) {
+                s -= nsteps;
+                ++tb;
+            }
         }
-        red[warp][gid][2 * t] = d[0];
-        red[warp][gid][2 * t + 1] = d[1];
-        red[warp][gid + 8][2 * t] = d[2];
-        red[warp][gid + 8][2 * t + 1] = d[3];
+        flush(bt);
         __syncthreads();
-        if (tid < kRowsPerCta * 8) {
-            const int r = tid >> 3, m = tid & 7;
-            const int64_t n = tile * kRowsPerCta + r;
+        for (int e = tid; e < bt * kRowsPerCta * 8; e += kThreads) {
+            const int rr = e >> 3, m = e & 7, tb = rr / kRowsPerCta, r = rr - tb * kRowsPerCta;
+            const int64_t n = (blockIdx.x + static_cast<int64_t>(gridDim.x) * (round * B + tb)) * kRowsPerCta + r;
             if (m < M && n < N) {
                 float sum = 0.0f;
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w) sum += red[w][r][m];
+                for (int w = 0; w < kWarps; ++w) sum += red(w, rr, m);
                 y[m * N + n] = sum * (kFp4 ? g : row_scale[n]);
             }
         }
-        __syncthreads();   // red is reused by the next tile
+        __syncthreads();   // red is reused by the next round
     }
 }
 
@@ -322,13 +366,47 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const uint8_t *codes, cons
     route_hit(r);
     if (r == kRouteNvfp4Mma || r == kRouteFp8Mma) {
         const int64_t ntiles = (N + kRowsPerCta - 1) / kRowsPerCta;
-        const int S = std::max(1, std::min(8, env_int("QMV_WQ_SLOTS", 4)));
-        // Activations in shared memory when a CTA stays within the SM's opt-in limit.
+        const int64_t nsteps = K / (kFp4 ? 2 * kStepBytes : kStepBytes);
+        int gcd = kWarps;
+        while (nsteps % gcd) gcd >>= 1;   // gcd(nsteps, 8): kWarps is a power of two
+        const int B = std::min(kMaxRound, kWarps / gcd);
+        // Activations go to shared memory whenever they fit (re-read through L1 they
+        // thrash it at M = 8); then the most slots that let two CTAs share an SM, else
+        // the most slots.
         const uint32_t xbytes = static_cast<uint32_t>(M) * xs_row_stride(K);
-        const bool xsmem = wq_layout(S, xbytes).total + 1024 <= static_cast<uint32_t>(dev.smem_optin) &&
-                           xbytes <= static_cast<uint32_t>(env_int("QMV_WQ_XSMEM_MAX", 160 * 1024));
-        const WqLayout L = wq_layout(S, xsmem ? xbytes : 0u);
-        const int per_sm = std::max(1, std::min(4, dev.smem_per_sm / static_cast<int>(L.total + 7 * 1024)));
+        const bool x_ok = xbytes <= static_cast<uint32_t>(env_int("QMV_WQ_XSMEM_MAX", 160 * 1024));
+        const int s_env = env_int("QMV_WQ_SLOTS", 0);
+        struct Cand { int S; bool xs; };
+        const Cand cands[] = {{4, true}, {3, true}, {2, true}, {4, false}, {3, false}, {2, false}};
+        int best = -1, best_occ = 0;
+        for (int c = 0; c < 6; ++c) {
+            if (cands[c].xs && !x_ok) continue;
+            if (best >= 0 && cands[best].xs != cands[c].xs) break;   // x in shared memory fits: stay there
+            const int Sc = s_env > 0 ? std::min(8, s_env) : cands[c].S;
+            const uint32_t dyn = wq_layout(Sc, B, cands[c].xs ? xbytes : 0u).total + 1024;
+            if (dyn > static_cast<uint32_t>(dev.smem_optin)) continue;
+            auto kc = cands[c].xs ? wq_mma_kernel<kFp4, true> : wq_mma_kernel<kFp4, false>;
+            cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kc), dev.smem_optin,
+                                             cands[c].xs ? cudaSharedmemCarveoutMaxShared : -1);
+            if (e != cudaSuccess) return e;
+            int occ = 0;
+            if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kc, kThreads, dyn)) != cudaSuccess) return e;
+            if (occ < 1) continue;
+            if (best < 0) {
+                best = c;
+                best_occ = occ;
+            }
+            if (occ >= 2) {
+                best = c;
+                best_occ = occ;
+                break;
+            }
+        }
+        if (best < 0) return cudaErrorInvalidValue;
+        const int S = s_env > 0 ? std::min(8, s_env) : cands[best].S;
+        const bool xsmem = cands[best].xs;
+        const WqLayout L = wq_layout(S, B, xsmem ? xbytes : 0u);
+        const int per_sm = std::min(4, best_occ);
         cfg.gridDim =
             dim3(static_cast<unsigned>(std::min<int64_t>(ntiles, static_cast<int64_t>(dev.sm_count) * per_sm)));
         CUtensorMap tm_codes, tm_scales;
@@ -342,11 +420,7 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const uint8_t *codes, cons
         }
         auto kern = xsmem ? wq_mma_kernel<kFp4, true> : wq_mma_kernel<kFp4, false>;
         cfg.dynamicSmemBytes = L.total + 1024;
-        // shared memory for the rings (and activations); L1 keeps the rest
-        e = ensure_smem_attr(reinterpret_cast<const void *>(kern), static_cast<int>(L.total + 1024),
-                             xsmem ? cudaSharedmemCarveoutMaxShared : -1);
-        if (e != cudaSuccess) return e;
-        return cudaLaunchKernelEx(&cfg, kern, tm_codes, tm_scales, rs, g, x, y, M, N, K, S);
+        return cudaLaunchKernelEx(&cfg, kern, tm_codes, tm_scales, rs, g, x, y, M, N, K, S, B);
     }
     const int64_t grid = (N + kWarps - 1) / kWarps;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
