@@ -275,7 +275,7 @@ class Stack:
         deps = w["stages"]() if "stages" in w else [[i] for i in range(len(self.mats))]
         assert sorted(i for st in deps for i in st) == list(range(len(self.mats)))
         self.input_of = {i: j for j, st in enumerate(deps) for i in st}
-        self.stages = deps if grouped and fused else [[i] for i in range(len(self.mats))]
+        self.stages = deps if grouped else [[i] for i in range(len(self.mats))]
         M = self.M
         self.weights = []
         for i, (fmt, n, k) in enumerate(self.mats):
@@ -311,8 +311,10 @@ class Stack:
         for _, n, _ in self.mats:
             self.ys.append(self.y_buf[off:off + M * n].view(M, n))
             off += M * n
-        self.xqs = [torch.empty((M, k // 32 * Q8_1_BLOCK), dtype=torch.uint8, device=device)
-                    if fmt == "q4_0" else None for fmt, _, k in self.mats]
+        # Q8_1 activations of the two-call path: one buffer per stage input
+        xq_in = [torch.empty((M, self.mats[i][2] // 32 * Q8_1_BLOCK), dtype=torch.uint8, device=device)
+                 if self.mats[i][0] == "q4_0" else None for i in first]
+        self.xqs = [xq_in[self.input_of[i]] for i in range(len(self.mats))]
         self.bytes_per_step = sum(self.launch_bytes(st) for st in self.stages)
         self.weight_bytes = sum(weight_bytes(fmt, n, k) for fmt, n, k in self.mats)
 
@@ -322,10 +324,16 @@ class Stack:
         import gemm_qmv_quantize_gb300 as q
         for j, st in enumerate(self.stages):
             if len(st) > 1:
+                if not self.fused:   # the stage's matrices share their input: quantize it once
+                    q.qmv_quantize_q8_1(self.xs[st[0]], out=self.xqs[st[0]])
                 if events is not None:
                     events[j][0].record()
-                q.qmv_q4_0_q8_1_fused_group([self.weights[i][0] for i in st], [self.xs[i] for i in st],
-                                            [self.ys[i] for i in st])
+                if self.fused:
+                    q.qmv_q4_0_q8_1_fused_group([self.weights[i][0] for i in st], [self.xs[i] for i in st],
+                                                [self.ys[i] for i in st])
+                else:
+                    q.qmv_q4_0_q8_1_group([self.weights[i][0] for i in st], [self.xqs[i] for i in st],
+                                          self.mats[st[0]][2], [self.ys[i] for i in st])
                 if events is not None:
                     events[j][1].record()
                 continue
@@ -360,8 +368,7 @@ class Stack:
         return b
 
     def kernels_per_step(self):
-        return sum(1 if len(st) > 1 else (2 if (self.mats[st[0]][0] == "q4_0" and not self.fused) else 1)
-                   for st in self.stages)
+        return sum(2 if (self.mats[st[0]][0] == "q4_0" and not self.fused) else 1 for st in self.stages)
 
 
 def capture(fn, stream):
@@ -390,6 +397,15 @@ def timed(replay, steps, barrier, sync):
     return start.elapsed_time(end) * 1e-3
 
 
+def q4_fused(args) -> bool:
+    """Q4_0 path: the quantize fused into the MMVQ prologue at M = 1 (every CTA
+    quantizes the row: cheaper than a launch); at M >= 2 the two-call path (one
+    quantize per input, then MMVQ on Q8_1), unless a flag forces one."""
+    if args.q4_path != "auto":
+        return args.q4_path == "fused"
+    return WORKLOADS[args.workload]["M"] == 1
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import gemm_qmv_quantize_gb300 as q
@@ -398,7 +414,7 @@ def run_ours(args, rank, world, local_rank):
     dist = Dist(world, "nccl", dev)
     barrier, max_over_ranks = dist.barrier, dist.max
 
-    stack = Stack(args.workload, dev, seed=1234 + rank, fused=not args.unfused, grouped=not args.serial)
+    stack = Stack(args.workload, dev, seed=1234 + rank, fused=q4_fused(args), grouped=not args.serial)
     stream = torch.cuda.Stream(device=dev)
     q.route_reset()
     q.set_launch_overlap(not args.no_overlap)
@@ -449,7 +465,8 @@ def _run_ours_on_stream(args, rank, world, local_rank, stack, stream, barrier, m
                    "bytes_per_step": stack.bytes_per_step,
                    "l2": "inputs larger than L2: every step streams all weights (> 129 MB)",
                    "launch": "eager" if args.eager else "cuda_graph", "launch_overlap": not args.no_overlap,
-                   "q8_1_quantize": "two calls" if args.unfused else "fused into the MMVQ prologue",
+                   "q8_1_quantize": "fused into the MMVQ prologue" if stack.fused else
+                   "two calls (quantize once per input, then MMVQ on Q8_1)",
                    "dependent_stages": len(stack.stages),
                    "schedule": ("one launch per matrix, each after the previous" if len(stack.stages) == len(stack.mats)
                                 else "decode dependency structure: matrices reading the same input share a launch"),
@@ -497,8 +514,13 @@ def kernel_roofline(args, stack, stream, barrier):
             total[j] += a.elapsed_time(b) * 1e-3
     barrier()
     fmt_main = stack.mats[0][0]
-    kname = {"q4_0": "q4_0_stream_fused_quantize" if stack.fused else "q4_0_stream_dp4a",
-             "nvfp4": "nvfp4_mma_m16n8k16", "fp8": "fp8_mma_m16n8k16"}[fmt_main]
+    # the dominant kernel by the route census of one more (eager) step: the GEMV routes
+    import gemm_qmv_quantize_gb300 as q
+    q.route_reset()
+    stack.run()
+    torch.cuda.synchronize()
+    gemv = {k: v for k, v in q.route_counts().items() if v and k.startswith(fmt_main)}
+    kname = max(gemv, key=gemv.get) if gemv else fmt_main
     sel = [j for j, st in enumerate(stack.stages) if stack.mats[st[0]][0] == fmt_main]
     stage_bytes = [stack.launch_bytes(stack.stages[j]) for j in sel]
     bytes_per_launch = sum(stage_bytes) / len(sel)
@@ -662,8 +684,9 @@ def parse_args(argv=None):
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=sorted(WORKLOADS), default=DEFAULT_WORKLOAD)
     p.add_argument("--eager", action="store_true", help="launch every call from Python (no CUDA graph)")
-    p.add_argument("--unfused", action="store_true",
-                   help="Q4_0: qmv_quantize_q8_1 + qmv_q4_0_q8_1 per call instead of the fused entry point")
+    p.add_argument("--q4-path", choices=["auto", "fused", "two_call"], default="auto",
+                   help="Q4_0: quantize fused into the MMVQ prologue, or qmv_quantize_q8_1 then MMVQ on Q8_1; "
+                        "auto = fused at M = 1, two calls from M = 2")
     p.add_argument("--serial", action="store_true",
                    help="one launch per matrix in stream order (no grouped launches of independent matrices)")
     p.add_argument("--no-overlap", action="store_true",

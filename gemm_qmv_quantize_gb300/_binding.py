@@ -32,6 +32,8 @@ SIGNATURES = {
     "qmv_q4_0_q8_1_fused": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _vp]),
     "qmv_q4_0_q8_1_fused_group": (_i32, [_i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
                                          ctypes.POINTER(_i64), _i32, _i64, _vp]),
+    "qmv_q4_0_q8_1_group": (_i32, [_i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                   ctypes.POINTER(_i64), _i32, _i64, _vp]),
     "qgemm_nvfp4_w4a16": (_i32, [_vp, _vp, _f32, _vp, _vp, _i32, _i64, _i64, _vp]),
     "qgemm_fp8_w8a16": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _vp]),
     "qmv_debug_q4_0_block_dots": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _vp]),
@@ -160,6 +162,27 @@ def qmv_q4_0_q8_1_fused_group(ws, xs, outs=None, stream=None):
     npa = (ctypes.c_int64 * count)(*Ns)
     _check("qmv_q4_0_q8_1_fused_group",
            lib().qmv_q4_0_q8_1_fused_group(count, wp, xp, yp, npa, M, K, _stream(stream)))
+    return outs
+
+
+def qmv_q4_0_q8_1_group(ws, xqs, K: int, outs=None, stream=None):
+    """Several independent calls on Q8_1 activations (same M, K) in one launch."""
+    count = len(ws)
+    if count != len(xqs) or not 1 <= count <= 8:
+        raise ValueError("need 1..8 matrices and as many activations")
+    M = xqs[0].shape[0]
+    Ns = [w.shape[0] for w in ws]
+    for i, (w, xq) in enumerate(zip(ws, xqs)):
+        _need(xq, f"xq[{i}]", torch.uint8, (M, K // 32 * 36))
+        _need(w, f"w[{i}]", torch.uint8, (Ns[i], K // 32 * 18))
+    if outs is None:
+        outs = [torch.empty((M, n), dtype=torch.float32, device=xqs[0].device) for n in Ns]
+    for i, o in enumerate(outs):
+        _need(o, f"out[{i}]", torch.float32, (M, Ns[i]))
+    arr = ctypes.c_void_p * count
+    wp, xp, yp = arr(*[w.data_ptr() for w in ws]), arr(*[x.data_ptr() for x in xqs]), arr(*[o.data_ptr() for o in outs])
+    npa = (ctypes.c_int64 * count)(*Ns)
+    _check("qmv_q4_0_q8_1_group", lib().qmv_q4_0_q8_1_group(count, wp, xp, yp, npa, M, K, _stream(stream)))
     return outs
 
 

@@ -16,7 +16,7 @@ std::atomic<int64_t> g_route_launches[kRouteCount];
 constexpr const char *kRouteNames[kRouteCount] = {
     "quantize_q8_1", "q4_0_stream_dp4a", "q4_0_generic", "q4_0_stream_fused_quantize", "nvfp4_mma_m16n8k16",
     "nvfp4_generic",
-    "fp8_mma_m16n8k16", "fp8_generic", "zero_fill",
+    "fp8_mma_m16n8k16", "fp8_generic", "zero_fill", "q4_0_mma_m16n8k32", "q4_0_mma_fused_quantize",
 };
 
 constexpr int kMaxDevices = 64;
@@ -201,8 +201,10 @@ qmv_status qmv_debug_q4_0_block_dots(const void *w, const void *xq, int32_t *dot
     return q4_0_common(w, xq, nullptr, dots, M, N, K, stream);
 }
 
-qmv_status qmv_q4_0_q8_1_fused_group(int count, const void *const *w, const float *const *x, float *const *y,
-                                     const int64_t *N, int M, int64_t K, qmv_stream_t stream)
+// Grouped launch of `count` matrices with the same M and K: fused, x[i] are fp32
+// [M][K] (16-byte aligned); else Q8_1 [M][K/32] (4-byte aligned).
+static qmv_status q4_0_group(int count, const void *const *w, const void *const *x, float *const *y,
+                             const int64_t *N, int M, int64_t K, bool fused, qmv_stream_t stream)
 {
     if (count < 1 || count > kMaxGroup) return QMV_ERR_SHAPE;
     if (!w || !x || !y || !N) return QMV_ERR_NULL;
@@ -230,7 +232,7 @@ qmv_status qmv_q4_0_q8_1_fused_group(int count, const void *const *w, const floa
     }
     for (int i = 0; i < count; ++i) {
         if (!w[i] || !x[i]) return QMV_ERR_NULL;
-        if (misaligned(w[i], 16) || misaligned(x[i], 16)) return QMV_ERR_ALIGN;
+        if (misaligned(w[i], 16) || misaligned(x[i], fused ? 16 : 4)) return QMV_ERR_ALIGN;
         grp.w[i] = static_cast<const uint8_t *>(w[i]);
         grp.y[i] = y[i];
         // matrices given the same activation stage (and quantize) it once
@@ -244,8 +246,21 @@ qmv_status qmv_q4_0_q8_1_fused_group(int count, const void *const *w, const floa
     if (e != cudaSuccess) return QMV_ERR_CUDA;
     Q4Plan plan;
     if ((e = plan_q4_0(dev, grp, M, K, &plan)) != cudaSuccess) return QMV_ERR_CUDA;
-    if (plan.route != kRouteQ4_0Stream) return QMV_ERR_SHAPE;   // does not fit the streaming kernel
-    return from_cuda(launch_q4_0(plan, grp, nullptr, M, K, true, stream));
+    if (plan.route != kRouteQ4_0Stream && plan.route != kRouteQ4_0Mma)
+        return QMV_ERR_SHAPE;   // the activations do not fit in shared memory
+    return from_cuda(launch_q4_0(plan, grp, nullptr, M, K, fused, stream));
+}
+
+qmv_status qmv_q4_0_q8_1_fused_group(int count, const void *const *w, const float *const *x, float *const *y,
+                                     const int64_t *N, int M, int64_t K, qmv_stream_t stream)
+{
+    return q4_0_group(count, w, reinterpret_cast<const void *const *>(x), y, N, M, K, true, stream);
+}
+
+qmv_status qmv_q4_0_q8_1_group(int count, const void *const *w, const void *const *xq, float *const *y,
+                               const int64_t *N, int M, int64_t K, qmv_stream_t stream)
+{
+    return q4_0_group(count, w, xq, y, N, M, K, false, stream);
 }
 
 qmv_status qmv_q4_0_q8_1_fused(const void *w, const float *x, float *y, int M, int64_t N, int64_t K,
@@ -310,10 +325,11 @@ qmv_status qmv_error_flags(uint32_t *flags, int clear)
 {
     if (!flags) return QMV_ERR_NULL;
     if (cudaDeviceSynchronize() != cudaSuccess) return QMV_ERR_CUDA;
-    uint32_t w = 0, w2 = 0;
+    uint32_t w = 0, w2 = 0, w3 = 0;
     if (read_error_word_q4_0(&w, clear != 0) != cudaSuccess) return QMV_ERR_CUDA;
     if (read_error_word_wq(&w2, clear != 0) != cudaSuccess) return QMV_ERR_CUDA;
-    *flags = w | w2;
+    if (read_error_word_q4_0_mma(&w3, clear != 0) != cudaSuccess) return QMV_ERR_CUDA;
+    *flags = w | w2 | w3;
     return QMV_OK;
 }
 

@@ -494,9 +494,15 @@ cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t 
     plan->warps = kWarps;
     plan->stages = 0;
     plan->prefetch = 0;
+    plan->round = 0;
     plan->smem_bytes = 0;
     plan->grid = static_cast<int>((N + kWarps - 1) / kWarps);
     if (!aligned || K % 256 != 0) return cudaSuccess;
+    // from a few activation rows on, the tensor cores
+    if (M >= env_int("QMV_Q4_MMA_MIN_M", 5)) {
+        cudaError_t e = plan_q4_0_mma(dev, grp, M, K, plan);
+        if (e != cudaSuccess || plan->route == kRouteQ4_0Mma) return e;
+    }
 
     // Warps hide latency (each also issues its own copies); slots are the bytes in flight.
     const int act_rows = M * grp.nx;
@@ -543,6 +549,7 @@ void assign_ctas(Q4Group &grp, int total)
 cudaError_t launch_q4_0(const Q4Plan &plan, const Q4Group &grp_in, int32_t *dots, int M, int64_t K, bool fused,
                         cudaStream_t s)
 {
+    if (plan.route == kRouteQ4_0Mma) return launch_q4_0_mma(plan, grp_in, dots, M, K, fused, s);
     if (fused && plan.route != kRouteQ4_0Stream) return cudaErrorInvalidValue;
     Q4Group grp = grp_in;
     if (plan.route == kRouteQ4_0Stream) assign_ctas(grp, plan.grid * plan.warps);   // per warp

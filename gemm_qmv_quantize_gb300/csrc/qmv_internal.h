@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace qmv {
@@ -18,6 +19,8 @@ enum Route : int {
     kRouteFp8Mma,         // FP8: register-fed m16n8k16, K % 128 == 0
     kRouteFp8Generic,     // FP8: any K
     kRouteZeroFill,       // K == 0: y = 0
+    kRouteQ4_0Mma,        // Q4_0: tensor cores (m16n8k32 int8), larger M
+    kRouteQ4_0MmaFused,   // ... with the Q8_1 quantize in the prologue
     kRouteCount
 };
 
@@ -43,6 +46,7 @@ struct Q4Plan {
     int stages;        // streaming kernel: ring slots per warp
     int chunk_units;   // 144-byte units per ring slot
     int prefetch;      // streaming kernel: chunks per CTA requested before the programmatic-dependency wait
+    int round;         // tensor-core kernel: tiles per reduction round
     int grid;
     int smem_bytes;
 };
@@ -71,6 +75,11 @@ struct Q4Group {
 };
 
 cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t K, Q4Plan *plan);
+// The tensor-core kernel's plan (route kRouteQ4_0Mma), or route kRouteQ4_0Generic
+// when it does not apply.
+cudaError_t plan_q4_0_mma(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t K, Q4Plan *plan);
+cudaError_t launch_q4_0_mma(const Q4Plan &plan, const Q4Group &grp, int32_t *dots, int M, int64_t K, bool fused,
+                            cudaStream_t s);
 cudaError_t launch_q4_0(const Q4Plan &plan, const Q4Group &grp, int32_t *dots, int M, int64_t K, bool fused,
                         cudaStream_t s);
 
@@ -85,5 +94,11 @@ cudaError_t launch_fp8(Route r, const DeviceInfo &dev, const uint8_t *w, const f
 // Device error words of each translation unit (read synchronously; optionally cleared).
 cudaError_t read_error_word_q4_0(uint32_t *out, bool clear);
 cudaError_t read_error_word_wq(uint32_t *out, bool clear);
+cudaError_t read_error_word_q4_0_mma(uint32_t *out, bool clear);
+
+// Row-major byte matrix [rows][cols] (row stride = cols, a multiple of 16) as a 2-D
+// tensor map with a box of box_cols bytes x box_rows rows; zero fill outside.
+cudaError_t encode_map_2d(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, uint32_t box_cols,
+                          uint32_t box_rows, CUtensorMapSwizzle swizzle);
 
 }  // namespace qmv

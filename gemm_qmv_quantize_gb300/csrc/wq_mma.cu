@@ -47,13 +47,48 @@
 namespace qmv {
 namespace {
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+cudaError_t encode_map_2d(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, uint32_t box_cols,
+                          uint32_t box_rows, CUtensorMapSwizzle swizzle)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
+    const cuuint32_t box[2] = {box_cols, box_rows};
+    const cuuint32_t estride[2] = {1, 1};
+    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estride,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+
+namespace {
+
 __device__ uint32_t g_wq_error;
 
 constexpr int kThreads = 256;
 constexpr int kWarps = 8;
 constexpr int kRowsPerCta = 16;
 constexpr int kStepBytes = 128;   // bytes of one weight row per warp step
-constexpr int kMaxRound = 4;      // tiles per round at most
+constexpr int kMaxRound = 8;      // tiles per round at most
 
 // Row stride of the staged activations (16 mod 32 bytes) and the chunk swizzle.
 __host__ __device__ inline uint32_t xs_row_stride(int64_t K) { return static_cast<uint32_t>(K * 2 + 16); }
@@ -321,38 +356,6 @@ __global__ void __launch_bounds__(kThreads) wq_generic_kernel(const uint8_t *__r
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
-{
-    static std::once_flag once;
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// Row-major byte matrix [rows][cols] (row stride = cols) as a 2-D tensor map with a
-// box of box_cols bytes x 16 rows.
-cudaError_t encode_map(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, uint32_t box_cols,
-                       CUtensorMapSwizzle swizzle)
-{
-    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-    if (!enc) return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols)};
-    const cuuint32_t box[2] = {box_cols, static_cast<cuuint32_t>(kRowsPerCta)};
-    const cuuint32_t estride[2] = {1, 1};
-    const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estride,
-                           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 template <bool kFp4>
 cudaError_t launch_wq(Route r, const DeviceInfo &dev, const uint8_t *codes, const uint8_t *scales, const float *rs,
                       float g, const uint16_t *x, float *y, int M, int64_t N, int64_t K, cudaStream_t s)
@@ -367,9 +370,13 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const uint8_t *codes, cons
     if (r == kRouteNvfp4Mma || r == kRouteFp8Mma) {
         const int64_t ntiles = (N + kRowsPerCta - 1) / kRowsPerCta;
         const int64_t nsteps = K / (kFp4 ? 2 * kStepBytes : kStepBytes);
+        // tiles per round: a multiple of 8 / gcd(steps, 8), so every warp gets the same
+        // number of steps, and enough for 8 steps per warp between the round's barriers
         int gcd = kWarps;
         while (nsteps % gcd) gcd >>= 1;   // gcd(nsteps, 8): kWarps is a power of two
-        const int B = std::min(kMaxRound, kWarps / gcd);
+        const int unit = static_cast<int>(kWarps / gcd);
+        int B = unit;
+        while (B * nsteps < 8 * kWarps && B + unit <= kMaxRound) B += unit;
         // Activations go to shared memory whenever they fit (re-read through L1 they
         // thrash it at M = 8); then the most slots that let two CTAs share an SM, else
         // the most slots.
@@ -410,10 +417,10 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const uint8_t *codes, cons
         cfg.gridDim =
             dim3(static_cast<unsigned>(std::min<int64_t>(ntiles, static_cast<int64_t>(dev.sm_count) * per_sm)));
         CUtensorMap tm_codes, tm_scales;
-        cudaError_t e = encode_map(&tm_codes, codes, N, kFp4 ? K / 2 : K, kStepBytes, CU_TENSOR_MAP_SWIZZLE_128B);
+        cudaError_t e = encode_map_2d(&tm_codes, codes, N, kFp4 ? K / 2 : K, kStepBytes, kRowsPerCta, CU_TENSOR_MAP_SWIZZLE_128B);
         if (e != cudaSuccess) return e;
         if (kFp4) {
-            e = encode_map(&tm_scales, scales, N, K / 16, 16, CU_TENSOR_MAP_SWIZZLE_NONE);
+            e = encode_map_2d(&tm_scales, scales, N, K / 16, 16, kRowsPerCta, CU_TENSOR_MAP_SWIZZLE_NONE);
             if (e != cudaSuccess) return e;
         } else {
             tm_scales = tm_codes;   // unused

@@ -77,7 +77,8 @@ QMV_API qmv_status qmv_quantize_q8_1(const float *x, void *xq, int M, int64_t K,
  *   w   Q4_0 [N][K/32] blocks of 18 bytes: fp16 scale d4, then 16 bytes qs;
  *       element j of the block is qs[j] & 15, element j+16 is qs[j] >> 4;
  *       weight value d4 * (q - 8). 2-byte aligned (16-byte aligned and K a
- *       multiple of 256 select the streaming kernel).
+ *       multiple of 256 select the streaming kernels: dp4a at small M, the tensor
+ *       cores -- m16n8k32 int8, the nibbles as 16 (q - 8) -- from M = 5).
  *   xq  Q8_1 [M][K/32] (as written by qmv_quantize_q8_1), 4-byte aligned.
  *   y   fp32 [M][N]: y[m][n] = sum_b d4[n][b] * d8[m][b] * (S - 8 T), with the
  *       exact integer block sums S = sum_j q4_j * q8_j and T = sum_j q8_j
@@ -94,8 +95,9 @@ QMV_API qmv_status qmv_q4_0_q8_1(const void *w, const void *xq, float *y, int M,
  * Saves one launch and the Q8_1 round trip per call.
  *   w  Q4_0 as in qmv_q4_0_q8_1, 16-byte aligned; K a multiple of 256.
  *   x  fp32 [M][K], 16-byte aligned.   y  fp32 [M][N].
- * Returns QMV_ERR_SHAPE for shapes the streaming kernel cannot take (use the
- * two-call path there) and QMV_ERR_ALIGN for a misaligned w or x.
+ * Returns QMV_ERR_SHAPE for shapes the streaming kernels cannot take (their
+ * staged activations do not fit in shared memory; use the two-call path there)
+ * and QMV_ERR_ALIGN for a misaligned w or x.
  */
 QMV_API qmv_status qmv_q4_0_q8_1_fused(const void *w, const float *x, float *y, int M, int64_t N, int64_t K,
                                        qmv_stream_t stream);
@@ -115,6 +117,20 @@ QMV_API qmv_status qmv_q4_0_q8_1_fused(const void *w, const float *x, float *y, 
 QMV_API qmv_status qmv_q4_0_q8_1_fused_group(int count, const void *const *w, const float *const *x,
                                              float *const *y, const int64_t *N, int M, int64_t K,
                                              qmv_stream_t stream);
+
+/*
+ * The grouped launch on Q8_1 activations: call i computes y[i] exactly as
+ * qmv_q4_0_q8_1(w[i], xq[i], y[i], M, N[i], K) would (bit-identical). With several
+ * activation rows this is the faster path: qmv_quantize_q8_1 quantizes each input
+ * once, where the fused entry points quantize it again in every CTA.
+ *   count        1..8 matrices.
+ *   w, xq, y, N  HOST arrays of `count` entries; w[i] Q4_0 16-byte aligned, xq[i]
+ *                Q8_1 [M][K/32] 4-byte aligned (each may equal another xq[j]),
+ *                y[i] fp32 [M][N[i]]. K a multiple of 256.
+ * Errors as in qmv_q4_0_q8_1_fused_group.
+ */
+QMV_API qmv_status qmv_q4_0_q8_1_group(int count, const void *const *w, const void *const *xq, float *const *y,
+                                       const int64_t *N, int M, int64_t K, qmv_stream_t stream);
 
 /*
  * NVFP4 W4A16 skinny GEMM ("v100-skinny README", section "How QPN works": QPN2).

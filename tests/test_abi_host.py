@@ -120,6 +120,26 @@ def test_fp8_validation(lib, args, status):
     assert lib.qgemm_fp8_w8a16(*args) == status
 
 
+@pytest.mark.parametrize("fn", ["qmv_q4_0_q8_1_fused_group", "qmv_q4_0_q8_1_group"])
+def test_group_validation(lib, fn):
+    import ctypes
+    arr = ctypes.c_void_p * 9
+    n = (ctypes.c_int64 * 9)(*([64] * 9))
+    z = arr(*([P] * 9))
+    f = getattr(lib, f"{fn}")
+    assert f(9, z, z, z, n, 1, 4096, None) == SHAPE        # count > 8
+    assert f(0, z, z, z, n, 1, 4096, None) == SHAPE
+    assert f(2, z, z, z, n, 1, 4000, None) == SHAPE        # K % 256
+    assert f(2, z, z, z, n, 9, 4096, None) == SHAPE        # M > 8
+    assert f(2, None, z, z, n, 1, 4096, None) == NULL
+    assert f(2, arr(P, P + 8), z, z, n, 1, 4096, None) == ALIGN     # w not 16-aligned
+    assert f(2, z, z, arr(P, P + 2), n, 1, 4096, None) == ALIGN     # y not 4-aligned
+    assert f(2, z, z, z, n, 0, 4096, None) == OK           # M == 0
+    x_off = 4 if fn == "qmv_q4_0_q8_1_group" else 16       # Q8_1 needs 4 bytes, fp32 fused 16
+    assert f(2, z, arr(P, P + 2), z, n, 1, 4096, None) == ALIGN
+    assert f(2, z, arr(P, P + x_off // 2), z, n, 1, 4096, None) == ALIGN
+
+
 def test_debug_dots_validation(lib):
     assert lib.qmv_debug_q4_0_block_dots(P, P, 0, 1, 64, 4096, None) == NULL
     assert lib.qmv_debug_q4_0_block_dots(P, P, P, 9, 64, 4096, None) == SHAPE

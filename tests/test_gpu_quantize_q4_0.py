@@ -278,7 +278,8 @@ def test_q4_0_fused_matches_two_calls(q, M, N, K):
     y2 = q.qmv_q4_0_q8_1(w, q.qmv_quantize_q8_1(x), K)
     y1 = q.qmv_q4_0_q8_1_fused(w, x)
     assert torch.equal(y1, y2)
-    assert q.route_counts()["q4_0_stream_fused_quantize"] == 1
+    rc = q.route_counts()
+    assert rc["q4_0_stream_fused_quantize"] + rc["q4_0_mma_fused_quantize"] == 1
     rows = synth.sample_rows(N, 64, seed=M).numpy()
     xq_ref = oracle.quantize_q8_1(x.cpu().numpy())
     y_ref, bound = oracle.q4_0_q8_1(np.ascontiguousarray(w.cpu().numpy()[rows]), xq_ref, K)
@@ -315,7 +316,8 @@ def test_q4_0_fused_group_matches_single_calls(q, M, pattern):
     singles = [q.qmv_q4_0_q8_1_fused(w, x) for w, x in zip(ws, xs)]
     for a, b in zip(outs, singles):
         assert torch.equal(a, b)
-    assert q.route_counts()["q4_0_stream_fused_quantize"] == 5
+    rc = q.route_counts()
+    assert rc["q4_0_stream_fused_quantize"] + rc["q4_0_mma_fused_quantize"] == 5
     rows = synth.sample_rows(Ns[3], 32, seed=M).numpy()
     y_ref, bound = oracle.q4_0_q8_1(np.ascontiguousarray(ws[3].cpu().numpy()[rows]),
                                     oracle.quantize_q8_1(xb.cpu().numpy()), K)
@@ -334,3 +336,64 @@ def test_q4_0_fused_group_validation(q):
     assert L.qmv_q4_0_q8_1_fused_group(2, z, z, z, n, 1, 4000, None) == -2     # K % 256
     bad = P(0x10000, 0x10008)
     assert L.qmv_q4_0_q8_1_fused_group(2, bad, z, z, n, 1, 4096, None) == -3   # w not 16-aligned
+
+
+# ------------------------------------------------ the two Q4_0 kernels at M >= 2
+
+@pytest.fixture(params=["mma", "dp4a"])
+def q4_kernel(request, monkeypatch):
+    """Route M >= 2 to the tensor-core kernel or to the dp4a streaming kernel (the
+    planner's minimum M for the tensor cores set to 2, or raised past 8)."""
+    monkeypatch.setenv("QMV_Q4_MMA_MIN_M", "9" if request.param == "dp4a" else "2")
+    return request.param
+
+
+@pytest.mark.parametrize("M,N,K", [(2, 1000, 4096), (3, 37, 256), (4, 300, 11008), (5, 129, 768),
+                                   (6, 16, 14336), (7, 513, 4096), (8, 1000, 4096), (8, 77, 512)])
+def test_q4_0_both_kernels_match_oracle(q, q4_kernel, M, N, K):
+    """Integer block sums bit-exact and outputs within the bound on either kernel,
+    over ragged tiles, every tile-round shape (K / 256 steps of 1, 2, 3, 16, 43, 56)."""
+    q.route_reset()
+    _check_q4(q, M, N, K, seed=7 * N + K + M)
+    rc = q.route_counts()
+    want = "q4_0_mma_m16n8k32" if q4_kernel == "mma" else "q4_0_stream_dp4a"
+    assert rc[want] == 2, rc
+
+
+@pytest.mark.parametrize("M", [2, 5, 8])
+def test_q4_0_fused_group_both_kernels(q, q4_kernel, M):
+    """Grouped, fused launches (shared and distinct inputs) agree with single calls on either kernel."""
+    from gemm_qmv_quantize_gb300 import synth
+    K = 4096
+    Ns = [1024, 4096, 1000, 16]
+    ws = [synth.q4_0_weights(n, K, seed=1900 + i, device=DEV) for i, n in enumerate(Ns)]
+    inputs = [synth.activations_f32(M, K, seed=1990 + j, device=DEV) for j in range(2)]
+    xs = [inputs[0], inputs[1], inputs[0], inputs[1]]
+    q.route_reset()
+    outs = q.qmv_q4_0_q8_1_fused_group(ws, xs)
+    singles = [q.qmv_q4_0_q8_1_fused(w, x) for w, x in zip(ws, xs)]
+    for a, b in zip(outs, singles):
+        assert torch.equal(a, b)
+    rc = q.route_counts()
+    want = "q4_0_mma_fused_quantize" if q4_kernel == "mma" else "q4_0_stream_fused_quantize"
+    assert rc[want] == 5, rc
+    for i in (1, 3):
+        xq_ref = oracle.quantize_q8_1(xs[i].cpu().numpy())
+        y_ref, bound = oracle.q4_0_q8_1(ws[i].cpu().numpy(), xq_ref, K)
+        assert_close(f"group[{i}]", outs[i].cpu().numpy(), y_ref, bound)
+
+
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_q4_0_group_on_q8_1_matches_single_calls(q, q4_kernel, M):
+    """The grouped launch on Q8_1 activations is bit-identical to one call per matrix."""
+    from gemm_qmv_quantize_gb300 import synth
+    K = 4096
+    Ns = [4096, 1000, 16]
+    ws = [synth.q4_0_weights(n, K, seed=2900 + i, device=DEV) for i, n in enumerate(Ns)]
+    xq = [q.qmv_quantize_q8_1(synth.activations_f32(M, K, seed=2990 + j, device=DEV)) for j in range(2)]
+    xqs = [xq[0], xq[1], xq[0]]
+    outs = q.qmv_q4_0_q8_1_group(ws, xqs, K)
+    for w, x, o in zip(ws, xqs, outs):
+        assert torch.equal(o, q.qmv_q4_0_q8_1(w, x, K))
+    y_ref, bound = oracle.q4_0_q8_1(ws[1].cpu().numpy(), xqs[1].cpu().numpy(), K)
+    assert_close("group[1]", outs[1].cpu().numpy(), y_ref, bound)
