@@ -93,6 +93,8 @@ WORKLOADS["q4_0_4096sq_m1"] = dict(M=1, mats=lambda: [("q4_0", 4096, 4096)] * 48
                                    desc="Q4_0 GEMV M=1, N=K=4096, 48 rotated copies")
 WORKLOADS["q4_0_11008x4096_m1"] = dict(M=1, mats=lambda: [("q4_0", 11008, 4096)] * 16,
                                        desc="Q4_0 GEMV M=1, 11008x4096, 16 rotated copies")
+WORKLOADS["q4_0_14336x4096_m8"] = dict(M=8, mats=lambda: [("q4_0", 14336, 4096)] * 8,
+                                       desc="Q4_0 M=8, 14336x4096 (Llama-3-8B gate), 8 rotated copies")
 for _m in (1, 8):
     WORKLOADS[f"nvfp4_17408x5120_m{_m}"] = dict(M=_m, mats=lambda: [("nvfp4", 17408, 5120)] * 8,
                                                desc=f"NVFP4 W4A16 17408x5120, M={_m}, 8 rotated copies")
@@ -612,18 +614,21 @@ class OracleSampler:
             fmt, n, k = shape
             rows, t_shape, key = 16, 0.0, f"{fmt} {n}x{k}"
             rows_done[key] = 0
-            while t_shape < budget_s * self.share[shape] and rows_done[key] < n:
-                r = min(rows, n - rows_done[key])
-                _, w, x = self._inputs(shape, r)
+            cap = min(n, 8192)   # rows of the seeded matrix, cycled through until the time share is used
+            _, w, x = self._inputs(shape, cap)
+            while t_shape < budget_s * self.share[shape]:
+                off = rows_done[key] % cap
+                r = min(rows, cap - off)
                 if fmt == "q4_0":
                     t0 = time.perf_counter()
-                    oracle.q4_0_q8_1(np.ascontiguousarray(w[0][:r]), oracle.quantize_q8_1(x), k)
+                    oracle.q4_0_q8_1(np.ascontiguousarray(w[0][off:off + r]), oracle.quantize_q8_1(x), k)
                 elif fmt == "nvfp4":
                     t0 = time.perf_counter()
-                    oracle.nvfp4_w4a16(np.ascontiguousarray(w[0][:r]), np.ascontiguousarray(w[1][:r]), w[2], x)
+                    oracle.nvfp4_w4a16(np.ascontiguousarray(w[0][off:off + r]), np.ascontiguousarray(w[1][off:off + r]),
+                                       w[2], x)
                 else:
                     t0 = time.perf_counter()
-                    oracle.fp8_w8a16(np.ascontiguousarray(w[0][:r]), np.ascontiguousarray(w[1][:r]), x)
+                    oracle.fp8_w8a16(np.ascontiguousarray(w[0][off:off + r]), np.ascontiguousarray(w[1][off:off + r]), x)
                 dt = time.perf_counter() - t0
                 # the sampled rows' weights and outputs, plus the activation once per call
                 act = self.M * (k // 32) * Q8_1_BLOCK if fmt == "q4_0" else self.M * k * 2
@@ -632,8 +637,9 @@ class OracleSampler:
                 t_shape += dt
                 rows_done[key] += r
                 rows = min(rows * 2, 2048)
-        sample = ("oracle (plain C, fp64, one thread) on the first rows of one seeded matrix per distinct shape, "
-                  f"time split by the stack's bytes per shape; rows per shape: {rows_done}")
+        sample = ("oracle (plain C, fp64, one thread) on the rows of one seeded matrix per distinct shape (at most "
+                  "8192 rows, cycled), time split by the stack's bytes per shape; rows processed per shape: "
+                  f"{rows_done}")
         return done_bytes / done_time / 1e9, {"bytes": done_bytes, "seconds": round(done_time, 3), "sample": sample}
 
 
