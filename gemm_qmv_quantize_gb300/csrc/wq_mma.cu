@@ -121,7 +121,7 @@ __host__ __device__ inline WqLayout wq_layout(int S, int B, uint32_t xbytes)
 // kFp4: NVFP4 (256 k per step, E4M3 group scales); else FP8 (128 k per step, row scale).
 // kXSmem: activations staged in shared memory.
 template <bool kFp4, bool kXSmem>
-__global__ void __launch_bounds__(kThreads) wq_mma_kernel(const __grid_constant__ CUtensorMap tm_codes,
+__global__ void __launch_bounds__(kThreads, 3) wq_mma_kernel(const __grid_constant__ CUtensorMap tm_codes,
                                                          const __grid_constant__ CUtensorMap tm_scales,
                                                          const float *__restrict__ row_scale, float g,
                                                          const uint16_t *__restrict__ x, float *__restrict__ y,
@@ -377,18 +377,23 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const uint8_t *codes, cons
         const int unit = static_cast<int>(kWarps / gcd);
         int B = unit;
         while (B * nsteps < 8 * kWarps && B + unit <= kMaxRound) B += unit;
-        // Activations go to shared memory whenever they fit (re-read through L1 they
-        // thrash it at M = 8); then the most slots that let two CTAs share an SM, else
-        // the most slots.
+        // Candidates (ring slots, activations in shared memory), scored by the tail they
+        // leave: whole tiles over `grid` CTAs take ceil(tiles / grid) rounds, so the
+        // busiest CTA holds waves * grid / tiles times the mean. Within 15 % of the mean
+        // the deepest ring wins (two CTAs per SM at least); else the least imbalance.
+        // Activations stay in shared memory whenever they fit (re-read through L1 they
+        // thrash it at M = 8); at M <= 2, where they fit in L1, an unstaged candidate may
+        // win on balance.
         const uint32_t xbytes = static_cast<uint32_t>(M) * xs_row_stride(K);
         const bool x_ok = xbytes <= static_cast<uint32_t>(env_int("QMV_WQ_XSMEM_MAX", 160 * 1024));
         const int s_env = env_int("QMV_WQ_SLOTS", 0);
         struct Cand { int S; bool xs; };
         const Cand cands[] = {{4, true}, {3, true}, {2, true}, {4, false}, {3, false}, {2, false}};
         int best = -1, best_occ = 0;
+        double best_score = 1e30;
         for (int c = 0; c < 6; ++c) {
             if (cands[c].xs && !x_ok) continue;
-            if (best >= 0 && cands[best].xs != cands[c].xs) break;   // x in shared memory fits: stay there
+            if (!cands[c].xs && best >= 0 && cands[best].xs && (M > 2 || best_score <= 1.15)) break;
             const int Sc = s_env > 0 ? std::min(8, s_env) : cands[c].S;
             const uint32_t dyn = wq_layout(Sc, B, cands[c].xs ? xbytes : 0u).total + 1024;
             if (dyn > static_cast<uint32_t>(dev.smem_optin)) continue;
@@ -398,15 +403,16 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const uint8_t *codes, cons
             if (e != cudaSuccess) return e;
             int occ = 0;
             if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kc, kThreads, dyn)) != cudaSuccess) return e;
+            occ = std::min(occ, 4);
             if (occ < 1) continue;
-            if (best < 0) {
+            const int64_t g = std::min<int64_t>(ntiles, static_cast<int64_t>(dev.sm_count) * occ);
+            const double imb = static_cast<double>((ntiles + g - 1) / g * g) / static_cast<double>(ntiles);
+            // balanced candidates tie at 1 and the earlier (deeper, staged) one stays
+            const double score = (imb <= 1.15 ? 1.0 : imb) + (occ < 2 ? 0.5 : 0.0);
+            if (score < best_score) {
+                best_score = score;
                 best = c;
                 best_occ = occ;
-            }
-            if (occ >= 2) {
-                best = c;
-                best_occ = occ;
-                break;
             }
         }
         if (best < 0) return cudaErrorInvalidValue;
