@@ -69,6 +69,15 @@ def dense_27b_stack(mixed: bool):
     return mats
 
 
+def dense_27b_stages(mixed: bool):
+    """Per layer {qkv}, {o}, {gate, up} (the same input), {down}; then the lm_head."""
+    st = []
+    for layer in range(64):
+        b = 5 * layer
+        st += [[b], [b + 1], [b + 2, b + 3], [b + 4]]
+    return st + ([[320]] if mixed else [])
+
+
 def llama3_8b_mlp():
     return [("q4_0", 14336, 4096), ("q4_0", 14336, 4096), ("q4_0", 4096, 14336)]
 
@@ -76,11 +85,13 @@ def llama3_8b_mlp():
 WORKLOADS = {
     "llama2_7b_q4_0_m1": dict(M=1, mats=llama2_7b_stack, stages=llama2_7b_stages,
                              desc="Llama-2-7B-shaped Q4_0 decode stack, M=1 (225 matrices + per-call Q8_1 quantize)"),
-    "nvfp4_27b_m1": dict(M=1, mats=lambda: dense_27b_stack(False), desc="27B-class dense NVFP4 W4A16 stack, M=1"),
-    "nvfp4_27b_m8": dict(M=8, mats=lambda: dense_27b_stack(False), desc="27B-class dense NVFP4 W4A16 stack, M=8"),
-    "mixed_27b_m1": dict(M=1, mats=lambda: dense_27b_stack(True),
+    "nvfp4_27b_m1": dict(M=1, mats=lambda: dense_27b_stack(False), stages=lambda: dense_27b_stages(False),
+                         desc="27B-class dense NVFP4 W4A16 stack, M=1"),
+    "nvfp4_27b_m8": dict(M=8, mats=lambda: dense_27b_stack(False), stages=lambda: dense_27b_stages(False),
+                         desc="27B-class dense NVFP4 W4A16 stack, M=8"),
+    "mixed_27b_m1": dict(M=1, mats=lambda: dense_27b_stack(True), stages=lambda: dense_27b_stages(True),
                          desc="27B-class stack, FP8 attention every 4th layer + NVFP4 lm_head, M=1"),
-    "mixed_27b_m8": dict(M=8, mats=lambda: dense_27b_stack(True),
+    "mixed_27b_m8": dict(M=8, mats=lambda: dense_27b_stack(True), stages=lambda: dense_27b_stages(True),
                          desc="27B-class stack, FP8 attention every 4th layer + NVFP4 lm_head, M=8"),
 }
 for _m in range(1, 9):
@@ -326,11 +337,19 @@ class Stack:
         import gemm_qmv_quantize_gb300 as q
         for j, st in enumerate(self.stages):
             if len(st) > 1:
-                if not self.fused:   # the stage's matrices share their input: quantize it once
+                fmt = self.mats[st[0]][0]
+                if fmt == "q4_0" and not self.fused:   # the stage's matrices share their input: quantize it once
                     q.qmv_quantize_q8_1(self.xs[st[0]], out=self.xqs[st[0]])
                 if events is not None:
                     events[j][0].record()
-                if self.fused:
+                if fmt == "nvfp4":
+                    q.qgemm_nvfp4_w4a16_group([self.weights[i][0] for i in st], [self.weights[i][1] for i in st],
+                                              [self.weights[i][2] for i in st], self.xs[st[0]],
+                                              [self.ys[i] for i in st])
+                elif fmt == "fp8":
+                    q.qgemm_fp8_w8a16_group([self.weights[i][0] for i in st], [self.weights[i][1] for i in st],
+                                            self.xs[st[0]], [self.ys[i] for i in st])
+                elif self.fused:
                     q.qmv_q4_0_q8_1_fused_group([self.weights[i][0] for i in st], [self.xs[i] for i in st],
                                                 [self.ys[i] for i in st])
                 else:

@@ -6,11 +6,11 @@ The compute lives in the C-ABI CUDA library ``_build/libqmv.so`` (declared in
 inputs are in ``gemm_qmv_quantize_gb300.synth``.
 """
 from ._binding import (QmvError, QmvLibraryMissing, error_flags, get_launch_overlap, lib, library_path,
-                       qgemm_fp8_w8a16, set_launch_overlap,
+                       qgemm_fp8_w8a16, qgemm_fp8_w8a16_group, qgemm_nvfp4_w4a16_group, set_launch_overlap,
                        qgemm_nvfp4_w4a16, qmv_debug_q4_0_block_dots, qmv_q4_0_q8_1,
                        qmv_q4_0_q8_1_fused, qmv_q4_0_q8_1_fused_group, qmv_q4_0_q8_1_group, qmv_quantize_q8_1,
                        route_counts, route_reset)
 
-__all__ = ["QmvError", "QmvLibraryMissing", "error_flags", "get_launch_overlap", "set_launch_overlap", "lib", "library_path", "qgemm_fp8_w8a16",
+__all__ = ["QmvError", "QmvLibraryMissing", "error_flags", "get_launch_overlap", "set_launch_overlap", "lib", "library_path", "qgemm_fp8_w8a16", "qgemm_fp8_w8a16_group", "qgemm_nvfp4_w4a16_group",
            "qgemm_nvfp4_w4a16", "qmv_debug_q4_0_block_dots", "qmv_q4_0_q8_1", "qmv_q4_0_q8_1_fused", "qmv_q4_0_q8_1_fused_group", "qmv_q4_0_q8_1_group", "qmv_quantize_q8_1",
            "route_counts", "route_reset"]

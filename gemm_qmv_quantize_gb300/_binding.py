@@ -36,6 +36,10 @@ SIGNATURES = {
                                    ctypes.POINTER(_i64), _i32, _i64, _vp]),
     "qgemm_nvfp4_w4a16": (_i32, [_vp, _vp, _f32, _vp, _vp, _i32, _i64, _i64, _vp]),
     "qgemm_fp8_w8a16": (_i32, [_vp, _vp, _vp, _vp, _i32, _i64, _i64, _vp]),
+    "qgemm_nvfp4_w4a16_group": (_i32, [_i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_f32), _vp,
+                                       ctypes.POINTER(_vp), ctypes.POINTER(_i64), _i32, _i64, _vp]),
+    "qgemm_fp8_w8a16_group": (_i32, [_i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, ctypes.POINTER(_vp),
+                                     ctypes.POINTER(_i64), _i32, _i64, _vp]),
     "qmv_debug_q4_0_block_dots": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _vp]),
     "qmv_set_launch_overlap": (None, [_i32]),
     "qmv_get_launch_overlap": (_i32, []),
@@ -214,6 +218,56 @@ def qgemm_nvfp4_w4a16(codes: torch.Tensor, scales: torch.Tensor, global_scale: f
     _check("qgemm_nvfp4_w4a16", lib().qgemm_nvfp4_w4a16(codes.data_ptr(), scales.data_ptr(), float(global_scale),
                                                         x.data_ptr(), out.data_ptr(), M, N, K, _stream(stream)))
     return out
+
+
+def _group_outs(x, Ns, outs):
+    M = x.shape[0]
+    if outs is None:
+        outs = [torch.empty((M, n), dtype=torch.float32, device=x.device) for n in Ns]
+    for i, o in enumerate(outs):
+        _need(o, f"out[{i}]", torch.float32, (M, Ns[i]))
+    return outs
+
+
+def qgemm_nvfp4_w4a16_group(codes, scales, global_scales, x: torch.Tensor, outs=None, stream=None):
+    """Several NVFP4 matrices reading the same x in one launch; returns the outputs."""
+    count = len(codes)
+    if not 1 <= count <= 8 or len(scales) != count or len(global_scales) != count:
+        raise ValueError("need 1..8 matrices with their scales and global scales")
+    _need(x, "x", torch.float16)
+    M, K = x.shape
+    Ns = [c.shape[0] for c in codes]
+    for i in range(count):
+        _need(codes[i], f"codes[{i}]", torch.uint8, (Ns[i], K // 2))
+        _need(scales[i], f"scales[{i}]", torch.uint8, (Ns[i], K // 16))
+    outs = _group_outs(x, Ns, outs)
+    arr = ctypes.c_void_p * count
+    cp, sp, yp = arr(*[c.data_ptr() for c in codes]), arr(*[t.data_ptr() for t in scales]), arr(*[o.data_ptr() for o in outs])
+    gp = (ctypes.c_float * count)(*[float(g) for g in global_scales])
+    npa = (ctypes.c_int64 * count)(*Ns)
+    _check("qgemm_nvfp4_w4a16_group", lib().qgemm_nvfp4_w4a16_group(count, cp, sp, gp, x.data_ptr(), yp, npa, M, K,
+                                                                    _stream(stream)))
+    return outs
+
+
+def qgemm_fp8_w8a16_group(ws, row_scales, x: torch.Tensor, outs=None, stream=None):
+    """Several FP8 matrices reading the same x in one launch; returns the outputs."""
+    count = len(ws)
+    if not 1 <= count <= 8 or len(row_scales) != count:
+        raise ValueError("need 1..8 matrices with their row scales")
+    _need(x, "x", torch.float16)
+    M, K = x.shape
+    Ns = [w.shape[0] for w in ws]
+    for i in range(count):
+        _need(ws[i], f"w[{i}]", torch.uint8, (Ns[i], K))
+        _need(row_scales[i], f"row_scale[{i}]", torch.float32, (Ns[i],))
+    outs = _group_outs(x, Ns, outs)
+    arr = ctypes.c_void_p * count
+    wp, rp, yp = arr(*[w.data_ptr() for w in ws]), arr(*[r.data_ptr() for r in row_scales]), arr(*[o.data_ptr() for o in outs])
+    npa = (ctypes.c_int64 * count)(*Ns)
+    _check("qgemm_fp8_w8a16_group", lib().qgemm_fp8_w8a16_group(count, wp, rp, x.data_ptr(), yp, npa, M, K,
+                                                                _stream(stream)))
+    return outs
 
 
 def qgemm_fp8_w8a16(w: torch.Tensor, row_scale: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None,

@@ -283,7 +283,14 @@ qmv_status qgemm_nvfp4_w4a16(const uint8_t *codes, const uint8_t *scales_e4m3, f
     DeviceInfo dev;
     if (current_device_info(&dev) != cudaSuccess) return QMV_ERR_CUDA;
     const Route r = plan_nvfp4(codes, scales_e4m3, x, K);
-    return from_cuda(launch_nvfp4(r, dev, codes, scales_e4m3, global_scale, x, y, M, N, K, stream));
+    WqGroup grp{};
+    grp.count = 1;
+    grp.codes[0] = codes;
+    grp.scales[0] = scales_e4m3;
+    grp.g[0] = global_scale;
+    grp.y[0] = y;
+    grp.N[0] = N;
+    return from_cuda(launch_nvfp4(r, dev, grp, x, M, K, stream));
 }
 
 qmv_status qgemm_fp8_w8a16(const uint8_t *w, const float *row_scale, const uint16_t *x, float *y, int M, int64_t N,
@@ -300,7 +307,76 @@ qmv_status qgemm_fp8_w8a16(const uint8_t *w, const float *row_scale, const uint1
     DeviceInfo dev;
     if (current_device_info(&dev) != cudaSuccess) return QMV_ERR_CUDA;
     const Route r = plan_fp8(w, x, K);
-    return from_cuda(launch_fp8(r, dev, w, row_scale, x, y, M, N, K, stream));
+    WqGroup grp{};
+    grp.count = 1;
+    grp.codes[0] = w;
+    grp.row_scale[0] = row_scale;
+    grp.y[0] = y;
+    grp.N[0] = N;
+    return from_cuda(launch_fp8(r, dev, grp, x, M, K, stream));
+}
+
+// Grouped NVFP4 / FP8 launches (fp4: codes + E4M3 scales + global scales; else E4M3
+// weights + row scales), all matrices reading x: the tensor-core kernel only.
+static qmv_status wq_group(bool fp4, int count, const uint8_t *const *codes, const uint8_t *const *scales,
+                           const float *g, const float *const *row_scale, const uint16_t *x, float *const *y,
+                           const int64_t *N, int M, int64_t K, qmv_stream_t stream)
+{
+    if (count < 1 || count > kMaxGroup) return QMV_ERR_SHAPE;
+    if (!codes || !y || !N || (fp4 ? (!scales || !g) : !row_scale)) return QMV_ERR_NULL;
+    WqGroup grp{};
+    grp.count = count;
+    int64_t total = 0;
+    for (int i = 0; i < count; ++i) {
+        qmv_status st = check_shape(M, N[i], K, fp4 ? 256 : 128);
+        if (st != QMV_OK) return st;
+        total += N[i];
+    }
+    if (total > kMaxDim) return QMV_ERR_SHAPE;
+    if (M == 0 || total == 0) return QMV_OK;
+    for (int i = 0; i < count; ++i) {
+        if (N[i] > 0 && !y[i]) return QMV_ERR_NULL;
+        if (misaligned(y[i], 4)) return QMV_ERR_ALIGN;
+    }
+    if (K == 0) {
+        for (int i = 0; i < count; ++i) {
+            if (N[i] == 0) continue;
+            qmv_status st = zero_fill(y[i], M, N[i], stream);
+            if (st != QMV_OK) return st;
+        }
+        return QMV_OK;
+    }
+    if (!x) return QMV_ERR_NULL;
+    if (misaligned(x, 16)) return QMV_ERR_ALIGN;
+    for (int i = 0; i < count; ++i) {
+        if (!codes[i] || (fp4 ? !scales[i] : !row_scale[i])) return QMV_ERR_NULL;
+        if (misaligned(codes[i], 16) || (fp4 ? misaligned(scales[i], 4) : misaligned(row_scale[i], 4)))
+            return QMV_ERR_ALIGN;
+        grp.codes[i] = codes[i];
+        grp.scales[i] = fp4 ? scales[i] : nullptr;
+        grp.row_scale[i] = fp4 ? nullptr : row_scale[i];
+        grp.g[i] = fp4 ? g[i] : 0.0f;
+        grp.y[i] = y[i];
+        grp.N[i] = N[i];
+    }
+    DeviceInfo dev;
+    if (current_device_info(&dev) != cudaSuccess) return QMV_ERR_CUDA;
+    return fp4 ? from_cuda(launch_nvfp4(kRouteNvfp4Mma, dev, grp, x, M, K, stream))
+               : from_cuda(launch_fp8(kRouteFp8Mma, dev, grp, x, M, K, stream));
+}
+
+qmv_status qgemm_nvfp4_w4a16_group(int count, const uint8_t *const *codes, const uint8_t *const *scales_e4m3,
+                                   const float *global_scale, const uint16_t *x, float *const *y, const int64_t *N,
+                                   int M, int64_t K, qmv_stream_t stream)
+{
+    return wq_group(true, count, codes, scales_e4m3, global_scale, nullptr, x, y, N, M, K, stream);
+}
+
+qmv_status qgemm_fp8_w8a16_group(int count, const uint8_t *const *w, const float *const *row_scale,
+                                 const uint16_t *x, float *const *y, const int64_t *N, int M, int64_t K,
+                                 qmv_stream_t stream)
+{
+    return wq_group(false, count, w, nullptr, nullptr, row_scale, x, y, N, M, K, stream);
 }
 
 void qmv_set_launch_overlap(int enable) { g_launch_overlap.store(enable ? 1 : 0, std::memory_order_relaxed); }

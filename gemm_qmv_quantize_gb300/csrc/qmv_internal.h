@@ -83,13 +83,26 @@ cudaError_t launch_q4_0_mma(const Q4Plan &plan, const Q4Group &grp, int32_t *dot
 cudaError_t launch_q4_0(const Q4Plan &plan, const Q4Group &grp, int32_t *dots, int M, int64_t K, bool fused,
                         cudaStream_t s);
 
+// NVFP4 / FP8: a group of matrices with the same K reading the same activations
+// (count 1 for a single call). codes: NVFP4 [N][K/2] or FP8 [N][K]; scales: NVFP4
+// [N][K/16] E4M3; g: NVFP4 per-tensor scale; row_scale: FP8 [N].
+struct WqGroup {
+    int count;
+    const uint8_t *codes[kMaxGroup];
+    const uint8_t *scales[kMaxGroup];
+    const float *row_scale[kMaxGroup];
+    float g[kMaxGroup];
+    float *y[kMaxGroup];
+    int64_t N[kMaxGroup];
+};
+
 Route plan_nvfp4(const uint8_t *codes, const uint8_t *scales, const uint16_t *x, int64_t K);
-cudaError_t launch_nvfp4(Route r, const DeviceInfo &dev, const uint8_t *codes, const uint8_t *scales, float g,
-                         const uint16_t *x, float *y, int M, int64_t N, int64_t K, cudaStream_t s);
+cudaError_t launch_nvfp4(Route r, const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M, int64_t K,
+                         cudaStream_t s);
 
 Route plan_fp8(const uint8_t *w, const uint16_t *x, int64_t K);
-cudaError_t launch_fp8(Route r, const DeviceInfo &dev, const uint8_t *w, const float *rs, const uint16_t *x,
-                       float *y, int M, int64_t N, int64_t K, cudaStream_t s);
+cudaError_t launch_fp8(Route r, const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M, int64_t K,
+                       cudaStream_t s);
 
 // Device error words of each translation unit (read synchronously; optionally cleared).
 cudaError_t read_error_word_q4_0(uint32_t *out, bool clear);

@@ -118,14 +118,26 @@ __host__ __device__ inline WqLayout wq_layout(int S, int B, uint32_t xbytes)
     return L;
 }
 
+// A group of matrices with the same K reading the same activations (count 1 for a
+// single call): tensor maps of their codes (and NVFP4 scales), scales, outputs, and
+// the first tile of each (tiles of 16 rows, numbered over the matrices in order).
+struct WqParams {
+    CUtensorMap codes[kMaxGroup];
+    CUtensorMap scales[kMaxGroup];
+    const float *row_scale[kMaxGroup];   // FP8
+    float g[kMaxGroup];                  // NVFP4
+    float *y[kMaxGroup];
+    int64_t N[kMaxGroup];
+    int64_t tile_start[kMaxGroup + 1];
+    int count;
+};
+
 // kFp4: NVFP4 (256 k per step, E4M3 group scales); else FP8 (128 k per step, row scale).
 // kXSmem: activations staged in shared memory.
 template <bool kFp4, bool kXSmem>
-__global__ void __launch_bounds__(kThreads, 3) wq_mma_kernel(const __grid_constant__ CUtensorMap tm_codes,
-                                                         const __grid_constant__ CUtensorMap tm_scales,
-                                                         const float *__restrict__ row_scale, float g,
-                                                         const uint16_t *__restrict__ x, float *__restrict__ y,
-                                                         int M, int64_t N, int64_t K, int S, int B)
+__global__ void __launch_bounds__(kThreads, 3) wq_mma_kernel(const __grid_constant__ WqParams p,
+                                                            const uint16_t *__restrict__ x, int M, int64_t K, int S,
+                                                            int B)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the 128-byte swizzle needs 1024-byte aligned boxes (1 KB extra is allocated)
@@ -136,8 +148,16 @@ __global__ void __launch_bounds__(kThreads, 3) wq_mma_kernel(const __grid_consta
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, t = lane & 3;
-    const int64_t ntiles = (N + kRowsPerCta - 1) / kRowsPerCta;
+    const int64_t ntiles = p.tile_start[p.count];
     const int nsteps = static_cast<int>(K / kStepK);
+    // matrix of a tile (tiles are numbered over the group's matrices in order), and its first row
+    auto locate = [&](int64_t tile, int &mi, int64_t &row0) {
+        mi = 0;
+#pragma unroll
+        for (int i = 1; i < kMaxGroup; ++i)
+            if (i < p.count && tile >= p.tile_start[i]) mi = i;
+        row0 = (tile - p.tile_start[mi]) * kRowsPerCta;
+    };
     const bool has_x = gid < M;
     const uint32_t RS = xs_row_stride(K);
     const WqLayout L = wq_layout(S, B, kXSmem ? static_cast<uint32_t>(M) * RS : 0u);
@@ -159,11 +179,18 @@ __global__ void __launch_bounds__(kThreads, 3) wq_mma_kernel(const __grid_consta
     // first item of a round for this warp: tile warp / nsteps, step warp % nsteps
     const int tb0 = warp / nsteps, s0 = warp - tb0 * nsteps;
     int p_lt = tb0, p_step = s0, p_rend = min(B, nt);   // producer: local tile, step, end of its round
+    int64_t p_tile = -1, p_row0 = 0;   // the producer's last located tile
+    int p_mi = 0;
     auto issue = [&](int slot) {
-        const int y0 = static_cast<int>((blockIdx.x + static_cast<int64_t>(gridDim.x) * p_lt) * kRowsPerCta);
+        const int64_t tile = blockIdx.x + static_cast<int64_t>(gridDim.x) * p_lt;
+        if (tile != p_tile) {
+            locate(tile, p_mi, p_row0);
+            p_tile = tile;
+        }
+        const int y0 = static_cast<int>(p_row0);
         mbar_arrive_expect_tx(&bars[slot], kFp4 ? kCodesBox + kScalesBox : kCodesBox);
-        tma_load_2d(codes_ring + slot * kCodesBox, &tm_codes, p_step * kStepBytes, y0, &bars[slot], pol);
-        if (kFp4) tma_load_2d(scales_ring + slot * kScalesBox, &tm_scales, p_step * 16, y0, &bars[slot], pol);
+        tma_load_2d(codes_ring + slot * kCodesBox, &p.codes[p_mi], p_step * kStepBytes, y0, &bars[slot], pol);
+        if (kFp4) tma_load_2d(scales_ring + slot * kScalesBox, &p.scales[p_mi], p_step * 16, y0, &bars[slot], pol);
         p_step += kWarps;
         while (p_step >= nsteps) {   // once when nsteps >= 8
             p_step -= nsteps;
@@ -303,12 +330,15 @@ __global__ void __launch_bounds__(kThreads, 3) wq_mma_kernel(const __grid_consta
         __syncthreads();
         for (int e = tid; e < bt * kRowsPerCta * 8; e += kThreads) {
             const int rr = e >> 3, m = e & 7, tb = rr / kRowsPerCta, r = rr - tb * kRowsPerCta;
-            const int64_t n = (blockIdx.x + static_cast<int64_t>(gridDim.x) * (round * B + tb)) * kRowsPerCta + r;
-            if (m < M && n < N) {
+            int mi;
+            int64_t row0;
+            locate(blockIdx.x + static_cast<int64_t>(gridDim.x) * (round * B + tb), mi, row0);
+            const int64_t n = row0 + r, Nm = p.N[mi];
+            if (m < M && n < Nm) {
                 float sum = 0.0f;
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) sum += red(w, rr, m);
-                y[m * N + n] = sum * (kFp4 ? g : row_scale[n]);
+                p.y[mi][m * Nm + n] = sum * (kFp4 ? p.g[mi] : p.row_scale[mi][n]);
             }
         }
         __syncthreads();   // red is reused by the next round
@@ -357,8 +387,8 @@ __global__ void __launch_bounds__(kThreads) wq_generic_kernel(const uint8_t *__r
 }
 
 template <bool kFp4>
-cudaError_t launch_wq(Route r, const DeviceInfo &dev, const uint8_t *codes, const uint8_t *scales, const float *rs,
-                      float g, const uint16_t *x, float *y, int M, int64_t N, int64_t K, cudaStream_t s)
+cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M, int64_t K,
+                      cudaStream_t s)
 {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = {};
@@ -368,7 +398,9 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const uint8_t *codes, cons
     cfg.numAttrs = set_launch_overlap_attr(attr);
     route_hit(r);
     if (r == kRouteNvfp4Mma || r == kRouteFp8Mma) {
-        const int64_t ntiles = (N + kRowsPerCta - 1) / kRowsPerCta;
+        int64_t ntiles = 0;
+        for (int i = 0; i < grp.count; ++i) ntiles += (grp.N[i] + kRowsPerCta - 1) / kRowsPerCta;
+        if (ntiles == 0) return cudaSuccess;
         const int64_t nsteps = K / (kFp4 ? 2 * kStepBytes : kStepBytes);
         // tiles per round: a multiple of 8 / gcd(steps, 8), so every warp gets the same
         // number of steps, and enough for 8 steps per warp between the round's barriers
@@ -422,26 +454,41 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const uint8_t *codes, cons
         const int per_sm = std::min(4, best_occ);
         cfg.gridDim =
             dim3(static_cast<unsigned>(std::min<int64_t>(ntiles, static_cast<int64_t>(dev.sm_count) * per_sm)));
-        CUtensorMap tm_codes, tm_scales;
-        cudaError_t e = encode_map_2d(&tm_codes, codes, N, kFp4 ? K / 2 : K, kStepBytes, kRowsPerCta, CU_TENSOR_MAP_SWIZZLE_128B);
-        if (e != cudaSuccess) return e;
-        if (kFp4) {
-            e = encode_map_2d(&tm_scales, scales, N, K / 16, 16, kRowsPerCta, CU_TENSOR_MAP_SWIZZLE_NONE);
+        WqParams p{};
+        p.count = grp.count;
+        int64_t t = 0;
+        for (int i = 0; i < grp.count; ++i) {
+            p.tile_start[i] = t;
+            t += (grp.N[i] + kRowsPerCta - 1) / kRowsPerCta;
+            p.row_scale[i] = grp.row_scale[i];
+            p.g[i] = grp.g[i];
+            p.y[i] = grp.y[i];
+            p.N[i] = grp.N[i];
+            if (grp.N[i] == 0) continue;
+            cudaError_t e = encode_map_2d(&p.codes[i], grp.codes[i], grp.N[i], kFp4 ? K / 2 : K, kStepBytes,
+                                          kRowsPerCta, CU_TENSOR_MAP_SWIZZLE_128B);
             if (e != cudaSuccess) return e;
-        } else {
-            tm_scales = tm_codes;   // unused
+            if (kFp4) {
+                e = encode_map_2d(&p.scales[i], grp.scales[i], grp.N[i], K / 16, 16, kRowsPerCta,
+                                  CU_TENSOR_MAP_SWIZZLE_NONE);
+                if (e != cudaSuccess) return e;
+            }
         }
+        for (int i = grp.count; i <= kMaxGroup; ++i) p.tile_start[i] = t;
         auto kern = xsmem ? wq_mma_kernel<kFp4, true> : wq_mma_kernel<kFp4, false>;
         cfg.dynamicSmemBytes = L.total + 1024;
-        return cudaLaunchKernelEx(&cfg, kern, tm_codes, tm_scales, rs, g, x, y, M, N, K, S, B);
+        return cudaLaunchKernelEx(&cfg, kern, p, x, M, K, S, B);
     }
+    if (grp.count != 1) return cudaErrorInvalidValue;   // groups need the tensor-core kernel
+    const int64_t N = grp.N[0];
     const int64_t grid = (N + kWarps - 1) / kWarps;
     if (grid > 0x7fffffff) return cudaErrorInvalidValue;
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     auto kern = wq_generic_kernel<kFp4>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), 0, -1);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, kern, codes, scales, rs, g, x, y, M, N, K);
+    return cudaLaunchKernelEx(&cfg, kern, grp.codes[0], grp.scales[0], grp.row_scale[0], grp.g[0], x, grp.y[0], M, N,
+                              K);
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -467,16 +514,16 @@ Route plan_fp8(const uint8_t *w, const uint16_t *x, int64_t K)
     return (K % 128 == 0 && aligned16(w) && aligned16(x)) ? kRouteFp8Mma : kRouteFp8Generic;
 }
 
-cudaError_t launch_nvfp4(Route r, const DeviceInfo &dev, const uint8_t *codes, const uint8_t *scales, float g,
-                         const uint16_t *x, float *y, int M, int64_t N, int64_t K, cudaStream_t s)
+cudaError_t launch_nvfp4(Route r, const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M, int64_t K,
+                         cudaStream_t s)
 {
-    return launch_wq<true>(r, dev, codes, scales, nullptr, g, x, y, M, N, K, s);
+    return launch_wq<true>(r, dev, grp, x, M, K, s);
 }
 
-cudaError_t launch_fp8(Route r, const DeviceInfo &dev, const uint8_t *w, const float *rs, const uint16_t *x, float *y,
-                       int M, int64_t N, int64_t K, cudaStream_t s)
+cudaError_t launch_fp8(Route r, const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M, int64_t K,
+                       cudaStream_t s)
 {
-    return launch_wq<false>(r, dev, w, nullptr, rs, 0.0f, x, y, M, N, K, s);
+    return launch_wq<false>(r, dev, grp, x, M, K, s);
 }
 
 }  // namespace qmv

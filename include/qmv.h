@@ -164,6 +164,27 @@ QMV_API qmv_status qgemm_fp8_w8a16(const uint8_t *w, const float *row_scale, con
                            int M, int64_t N, int64_t K, qmv_stream_t stream);
 
 /*
+ * Several NVFP4 (or FP8) matrices with the same M and K reading the SAME activations
+ * x in ONE launch -- the gate and up projections of a layer, say: y[i] is matrix i's
+ * product as the single call defines it, within the same error bound (the fp32
+ * partial sums of a tile may be added in another order than in a single call).
+ * The tensor-core kernel only: K a multiple of 256 (NVFP4) or
+ * 128 (FP8), codes / w 16-byte aligned, scales and row scales 4-byte aligned, x
+ * 16-byte aligned (QMV_ERR_SHAPE / QMV_ERR_ALIGN otherwise).
+ *   count                 1..8 matrices.
+ *   codes, scales_e4m3, global_scale, w, row_scale, y, N
+ *                         HOST arrays of `count` entries (device pointers, scales
+ *                         and row counts), read during the call only.
+ */
+QMV_API qmv_status qgemm_nvfp4_w4a16_group(int count, const uint8_t *const *codes,
+                                           const uint8_t *const *scales_e4m3, const float *global_scale,
+                                           const uint16_t *x, float *const *y, const int64_t *N, int M, int64_t K,
+                                           qmv_stream_t stream);
+QMV_API qmv_status qgemm_fp8_w8a16_group(int count, const uint8_t *const *w, const float *const *row_scale,
+                                         const uint16_t *x, float *const *y, const int64_t *N, int M, int64_t K,
+                                         qmv_stream_t stream);
+
+/*
  * Launch overlap between consecutive calls (programmatic dependent launch),
  * process-wide, off by default. When enabled, every kernel of this library is
  * launched so that it may start while the preceding kernel on the stream is

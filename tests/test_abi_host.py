@@ -140,6 +140,24 @@ def test_group_validation(lib, fn):
     assert f(2, z, arr(P, P + x_off // 2), z, n, 1, 4096, None) == ALIGN
 
 
+def test_wq_group_validation(lib):
+    import ctypes
+    arr = ctypes.c_void_p * 9
+    n = (ctypes.c_int64 * 9)(*([64] * 9))
+    z = arr(*([P] * 9))
+    g = (ctypes.c_float * 9)(*([0.01] * 9))
+    nv, f8 = lib.qgemm_nvfp4_w4a16_group, lib.qgemm_fp8_w8a16_group
+    assert nv(9, z, z, g, P, z, n, 1, 512, None) == SHAPE           # count > 8
+    assert nv(2, z, z, g, P, z, n, 1, 528, None) == SHAPE           # K % 256 (the tensor-core kernel only)
+    assert nv(2, z, z, None, P, z, n, 1, 512, None) == NULL         # no global scales
+    assert nv(2, arr(P, P + 8), z, g, P, z, n, 1, 512, None) == ALIGN   # codes not 16-aligned
+    assert nv(2, z, z, g, P + 8, z, n, 1, 512, None) == ALIGN       # x not 16-aligned
+    assert nv(2, z, z, g, P, z, n, 0, 512, None) == OK              # M == 0
+    assert f8(2, z, z, P, z, n, 1, 200, None) == SHAPE              # K % 128
+    assert f8(2, z, arr(P, P + 2), P, z, n, 1, 384, None) == ALIGN  # row scale not 4-aligned
+    assert f8(9, z, z, P, z, n, 1, 384, None) == SHAPE
+
+
 def test_debug_dots_validation(lib):
     assert lib.qmv_debug_q4_0_block_dots(P, P, 0, 1, 64, 4096, None) == NULL
     assert lib.qmv_debug_q4_0_block_dots(P, P, P, 9, 64, 4096, None) == SHAPE

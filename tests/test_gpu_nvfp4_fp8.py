@@ -155,3 +155,44 @@ def test_k0_and_empty(q):
     assert y.shape == (2, 5) and torch.all(y == 0)
     y = q.qgemm_fp8_w8a16(torch.zeros((5, 0), dtype=torch.uint8, device=DEV), torch.ones(5, device=DEV), x)
     assert torch.all(y == 0)
+
+
+# ------------------------------------------------ grouped launches (one shared x)
+
+@pytest.mark.parametrize("M", [1, 3, 8])
+def test_nvfp4_group_matches_oracle(q, M):
+    """gate/up-like groups with ragged row counts: every output within the bound."""
+    synth = _synth()
+    K = 5120
+    Ns = [17408, 5120, 37, 1000]
+    mats = [synth.nvfp4_weights(n, K, seed=700 + i, device=DEV) for i, n in enumerate(Ns)]
+    x = synth.activations_f16(M, K, seed=790, device=DEV, outliers=3)
+    q.route_reset()
+    outs = q.qgemm_nvfp4_w4a16_group([m[0] for m in mats], [m[1] for m in mats], [m[2] for m in mats], x)
+    assert q.route_counts()["nvfp4_mma_m16n8k16"] == 1
+    for i, (c, sc, g) in enumerate(mats):
+        rows = np.arange(Ns[i]) if Ns[i] < 2000 else synth.sample_rows(Ns[i], 64, seed=i).numpy()
+        y_ref, bound = oracle.nvfp4_w4a16(c.cpu().numpy()[rows], sc.cpu().numpy()[rows], g, x.cpu().numpy())
+        assert_close(f"group[{i}]", outs[i].cpu().numpy()[:, rows], y_ref, bound)
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_fp8_group_matches_oracle(q, M):
+    synth = _synth()
+    K = 5120
+    Ns = [7168, 5120, 16, 129]
+    mats = [synth.fp8_weights(n, K, seed=800 + i, device=DEV) for i, n in enumerate(Ns)]
+    x = synth.activations_f16(M, K, seed=890, device=DEV)
+    outs = q.qgemm_fp8_w8a16_group([m[0] for m in mats], [m[1] for m in mats], x)
+    for i, (w, rs) in enumerate(mats):
+        rows = np.arange(Ns[i]) if Ns[i] < 2000 else synth.sample_rows(Ns[i], 64, seed=i).numpy()
+        y_ref, bound = oracle.fp8_w8a16(w.cpu().numpy()[rows], rs.cpu().numpy()[rows], x.cpu().numpy())
+        assert_close(f"fp8 group[{i}]", outs[i].cpu().numpy()[:, rows], y_ref, bound)
+
+
+def test_group_of_one_equals_single_call(q):
+    """A group of one matrix is the single call (same kernel, same tiles)."""
+    synth = _synth()
+    c, sc, g = synth.nvfp4_weights(5120, 17408, seed=3, device=DEV)
+    x = synth.activations_f16(2, 17408, seed=4, device=DEV)
+    assert torch.equal(q.qgemm_nvfp4_w4a16_group([c], [sc], [g], x)[0], q.qgemm_nvfp4_w4a16(c, sc, g, x))
