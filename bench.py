@@ -93,6 +93,10 @@ WORKLOADS = {
                          desc="27B-class stack, FP8 attention every 4th layer + NVFP4 lm_head, M=1"),
     "mixed_27b_m8": dict(M=8, mats=lambda: dense_27b_stack(True), stages=lambda: dense_27b_stages(True),
                          desc="27B-class stack, FP8 attention every 4th layer + NVFP4 lm_head, M=8"),
+    "nvfp4_27b_m16": dict(M=16, mats=lambda: dense_27b_stack(False), stages=lambda: dense_27b_stages(False),
+                          desc="27B-class dense NVFP4 W4A16 stack, M=16"),
+    "mixed_27b_m16": dict(M=16, mats=lambda: dense_27b_stack(True), stages=lambda: dense_27b_stages(True),
+                          desc="27B-class stack, FP8 attention every 4th layer + NVFP4 lm_head, M=16"),
 }
 for _m in range(1, 9):
     WORKLOADS[f"llama3_8b_mlp_q4_0_m{_m}"] = dict(
@@ -106,7 +110,7 @@ WORKLOADS["q4_0_11008x4096_m1"] = dict(M=1, mats=lambda: [("q4_0", 11008, 4096)]
                                        desc="Q4_0 GEMV M=1, 11008x4096, 16 rotated copies")
 WORKLOADS["q4_0_14336x4096_m8"] = dict(M=8, mats=lambda: [("q4_0", 14336, 4096)] * 8,
                                        desc="Q4_0 M=8, 14336x4096 (Llama-3-8B gate), 8 rotated copies")
-for _m in (1, 8):
+for _m in (1, 8, 16):
     WORKLOADS[f"nvfp4_17408x5120_m{_m}"] = dict(M=_m, mats=lambda: [("nvfp4", 17408, 5120)] * 8,
                                                desc=f"NVFP4 W4A16 17408x5120, M={_m}, 8 rotated copies")
     WORKLOADS[f"fp8_7168x5120_m{_m}"] = dict(M=_m, mats=lambda: [("fp8", 7168, 5120)] * 12,

@@ -25,15 +25,16 @@ DeviceInfo g_dev[kMaxDevices];
 bool g_dev_valid[kMaxDevices];
 
 constexpr int64_t kMaxDim = 0x7fffffffLL;
+constexpr int kMaxRowsW = 16;   // activation rows of the NVFP4 / FP8 entry points
 
 bool misaligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
 
 qmv_status from_cuda(cudaError_t e) { return e == cudaSuccess ? QMV_OK : QMV_ERR_CUDA; }
 
-// Shared shape checks: M in 0..8, 0 <= N, K <= 2^31-1, K a multiple of `kblock`.
-qmv_status check_shape(int M, int64_t N, int64_t K, int64_t kblock)
+// Shared shape checks: M in 0..max_m, 0 <= N, K <= 2^31-1, K a multiple of `kblock`.
+qmv_status check_shape(int M, int64_t N, int64_t K, int64_t kblock, int max_m = 8)
 {
-    if (M < 0 || M > 8 || N < 0 || K < 0 || N > kMaxDim || K > kMaxDim) return QMV_ERR_SHAPE;
+    if (M < 0 || M > max_m || N < 0 || K < 0 || N > kMaxDim || K > kMaxDim) return QMV_ERR_SHAPE;
     if (kblock > 1 && K % kblock != 0) return QMV_ERR_SHAPE;
     return QMV_OK;
 }
@@ -272,7 +273,7 @@ qmv_status qmv_q4_0_q8_1_fused(const void *w, const float *x, float *y, int M, i
 qmv_status qgemm_nvfp4_w4a16(const uint8_t *codes, const uint8_t *scales_e4m3, float global_scale,
                              const uint16_t *x, float *y, int M, int64_t N, int64_t K, qmv_stream_t stream)
 {
-    qmv_status st = check_shape(M, N, K, 16);
+    qmv_status st = check_shape(M, N, K, 16, kMaxRowsW);
     if (st != QMV_OK) return st;
     if (M == 0 || N == 0) return QMV_OK;
     if (!y) return QMV_ERR_NULL;
@@ -296,7 +297,7 @@ qmv_status qgemm_nvfp4_w4a16(const uint8_t *codes, const uint8_t *scales_e4m3, f
 qmv_status qgemm_fp8_w8a16(const uint8_t *w, const float *row_scale, const uint16_t *x, float *y, int M, int64_t N,
                            int64_t K, qmv_stream_t stream)
 {
-    qmv_status st = check_shape(M, N, K, 1);
+    qmv_status st = check_shape(M, N, K, 1, kMaxRowsW);
     if (st != QMV_OK) return st;
     if (M == 0 || N == 0) return QMV_OK;
     if (!y) return QMV_ERR_NULL;
@@ -328,7 +329,7 @@ static qmv_status wq_group(bool fp4, int count, const uint8_t *const *codes, con
     grp.count = count;
     int64_t total = 0;
     for (int i = 0; i < count; ++i) {
-        qmv_status st = check_shape(M, N[i], K, fp4 ? 256 : 128);
+        qmv_status st = check_shape(M, N[i], K, fp4 ? 256 : 128, kMaxRowsW);
         if (st != QMV_OK) return st;
         total += N[i];
     }

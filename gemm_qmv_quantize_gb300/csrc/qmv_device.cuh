@@ -116,6 +116,15 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, 
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared (both 16-byte aligned), bypassing L1;
+// cp_async_wait_all waits for all of this thread's outstanding copies.
+__device__ __forceinline__ void cp_async_16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // ---------------------------------------------------------------- programmatic dependent launch
 
 // Wait until the grid this launch depends on has completed and its writes are

@@ -34,8 +34,13 @@
 //  * Activations: staged once per CTA in shared memory when they fit, in an
 //    XOR-swizzled layout (16-byte chunk c of a row stored at c ^ 2((c >> 3) & 3),
 //    row stride 16 mod 32 bytes) that makes the fragment reads bank-conflict free;
-//    else read through L1.
+//    when M x K does not fit, K is cut into P equal passes: the CTA walks all its
+//    tiles over the first K range with that slice of x staged, restages the next
+//    slice, walks them again and adds to the outputs it wrote (its own rows only,
+//    so no other CTA is involved and the sum order is fixed). Read through L1
+//    only where no pass count fits.
 #include <algorithm>
+#include <cstdio>
 #include <mutex>
 
 #include <cuda.h>
@@ -97,7 +102,8 @@ __device__ __forceinline__ uint32_t xs_chunk(uint32_t c) { return c ^ (2u * ((c 
 constexpr int kCodesBox = kRowsPerCta * kStepBytes;   // 2048 bytes: 16 rows x 128 bytes
 constexpr int kScalesBox = kRowsPerCta * 16;          // 256 bytes: 16 rows x 16 scales
 
-constexpr int kRedPitch = 9;      // floats per partial row (8 columns + pad)
+// floats per partial row of the reduction: 8 activation rows per row tile, + pad
+__host__ __device__ constexpr int red_pitch(int mt) { return 8 * mt + 1; }
 
 struct WqLayout {
     uint32_t off_codes, off_scales, off_bar, off_red, off_x, total;
@@ -106,14 +112,14 @@ struct WqLayout {
 // Shared memory: per-warp rings of codes boxes (1024-byte aligned for the swizzle),
 // of scale boxes, their mbarriers, the round's partial sums [warp][B * 16 rows][9],
 // then the staged activations.
-__host__ __device__ inline WqLayout wq_layout(int S, int B, uint32_t xbytes)
+__host__ __device__ inline WqLayout wq_layout(int S, int B, uint32_t xbytes, int mt)
 {
     WqLayout L;
     L.off_codes = 0;
     L.off_scales = static_cast<uint32_t>(kWarps * S * kCodesBox);
     L.off_bar = L.off_scales + static_cast<uint32_t>(kWarps * S * kScalesBox);
     L.off_red = (L.off_bar + static_cast<uint32_t>(kWarps * S) * 8u + 15u) & ~15u;
-    L.off_x = (L.off_red + static_cast<uint32_t>(kWarps * B * kRowsPerCta * kRedPitch) * 4u + 127u) & ~127u;
+    L.off_x = (L.off_red + static_cast<uint32_t>(kWarps * B * kRowsPerCta * red_pitch(mt)) * 4u + 127u) & ~127u;
     L.total = L.off_x + xbytes;
     return L;
 }
@@ -133,11 +139,14 @@ struct WqParams {
 };
 
 // kFp4: NVFP4 (256 k per step, E4M3 group scales); else FP8 (128 k per step, row scale).
+// kMT: 8-row tiles of activations per weight pass (M <= 8 kMT): the decoded weight
+// fragments feed kMT mma each, so up to 16 rows share one weight stream.
 // kXSmem: activations staged in shared memory.
-template <bool kFp4, bool kXSmem>
-__global__ void __launch_bounds__(kThreads, 3) wq_mma_kernel(const __grid_constant__ WqParams p,
+// P: passes over K (staged activations only; 1 otherwise), K / kStepK a multiple of P.
+template <bool kFp4, bool kXSmem, int kMT>
+__global__ void __launch_bounds__(kThreads, kMT == 1 ? 3 : 2) wq_mma_kernel(const __grid_constant__ WqParams p,
                                                             const uint16_t *__restrict__ x, int M, int64_t K, int S,
-                                                            int B)
+                                                            int B, int P)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // the 128-byte swizzle needs 1024-byte aligned boxes (1 KB extra is allocated)
@@ -149,7 +158,8 @@ __global__ void __launch_bounds__(kThreads, 3) wq_mma_kernel(const __grid_consta
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, t = lane & 3;
     const int64_t ntiles = p.tile_start[p.count];
-    const int nsteps = static_cast<int>(K / kStepK);
+    const int nsteps = static_cast<int>(K / kStepK) / P;   // steps of one pass
+    const int64_t Kp = static_cast<int64_t>(nsteps) * kStepK;
     // matrix of a tile (tiles are numbered over the group's matrices in order), and its first row
     auto locate = [&](int64_t tile, int &mi, int64_t &row0) {
         mi = 0;
@@ -158,9 +168,9 @@ __global__ void __launch_bounds__(kThreads, 3) wq_mma_kernel(const __grid_consta
             if (i < p.count && tile >= p.tile_start[i]) mi = i;
         row0 = (tile - p.tile_start[mi]) * kRowsPerCta;
     };
-    const bool has_x = gid < M;
-    const uint32_t RS = xs_row_stride(K);
-    const WqLayout L = wq_layout(S, B, kXSmem ? static_cast<uint32_t>(M) * RS : 0u);
+    constexpr int kPitch = red_pitch(kMT);
+    const uint32_t RS = xs_row_stride(Kp);
+    const WqLayout L = wq_layout(S, B, kXSmem ? static_cast<uint32_t>(M) * RS : 0u, kMT);
     uint8_t *codes_ring = smem + L.off_codes + warp * S * kCodesBox;
     uint8_t *scales_ring = smem + L.off_scales + warp * S * kScalesBox;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.off_bar) + warp * S;
@@ -168,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 3) wq_mma_kernel(const __grid_consta
     // partial sums of the round: red(w, row of the round, column)
     float *red_base = reinterpret_cast<float *>(smem + L.off_red);
     auto red = [&](int w, int rr, int m) -> float & {
-        return red_base[(w * B * kRowsPerCta + rr) * kRedPitch + m];
+        return red_base[(w * B * kRowsPerCta + rr) * kPitch + m];
     };
     const uint64_t pol = policy_evict_first();
 
@@ -178,7 +188,22 @@ __global__ void __launch_bounds__(kThreads, 3) wq_mma_kernel(const __grid_consta
     const int nt = static_cast<int>((ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x);
     // first item of a round for this warp: tile warp / nsteps, step warp % nsteps
     const int tb0 = warp / nsteps, s0 = warp - tb0 * nsteps;
-    int p_lt = tb0, p_step = s0, p_rend = min(B, nt);   // producer: local tile, step, end of its round
+    // producer: pass, local tile, step, end of its round
+    int p_ps = 0, p_lt = tb0, p_step = s0, p_rend = min(B, nt);
+    // past the end of a round: restart at this warp's first item of the next round,
+    // or of the next pass's first round
+    auto settle = [&]() {
+        while (p_ps < P && p_lt >= p_rend) {
+            if (p_rend >= nt) {
+                ++p_ps;
+                p_rend = 0;
+            }
+            p_lt = p_rend + tb0;
+            p_step = s0;
+            p_rend = min(p_rend + B, nt);
+        }
+    };
+    settle();
     int64_t p_tile = -1, p_row0 = 0;   // the producer's last located tile
     int p_mi = 0;
     auto issue = [&](int slot) {
@@ -189,22 +214,19 @@ __global__ void __launch_bounds__(kThreads, 3) wq_mma_kernel(const __grid_consta
         }
         const int y0 = static_cast<int>(p_row0);
         mbar_arrive_expect_tx(&bars[slot], kFp4 ? kCodesBox + kScalesBox : kCodesBox);
-        tma_load_2d(codes_ring + slot * kCodesBox, &p.codes[p_mi], p_step * kStepBytes, y0, &bars[slot], pol);
-        if (kFp4) tma_load_2d(scales_ring + slot * kScalesBox, &p.scales[p_mi], p_step * 16, y0, &bars[slot], pol);
+        const int gs = p_ps * nsteps + p_step;   // step over the whole of K
+        tma_load_2d(codes_ring + slot * kCodesBox, &p.codes[p_mi], gs * kStepBytes, y0, &bars[slot], pol);
+        if (kFp4) tma_load_2d(scales_ring + slot * kScalesBox, &p.scales[p_mi], gs * 16, y0, &bars[slot], pol);
         p_step += kWarps;
         while (p_step >= nsteps) {   // once when nsteps >= 8
             p_step -= nsteps;
             ++p_lt;
         }
-        if (p_lt >= p_rend) {   // next round: restart at this warp's first item
-            p_lt = p_rend + tb0;
-            p_step = s0;
-            p_rend = min(p_rend + B, nt);
-        }
+        settle();
     };
     // rounds before the last hold a multiple of 8 items, so a warp with an item in
-    // one round has one in every round but perhaps the last
-    auto pending = [&]() { return p_lt < p_rend; };
+    // one round has one in every round of the pass but perhaps the last
+    auto pending = [&]() { return p_ps < P && p_lt < p_rend; };
     if (lane == 0) {
         for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
         fence_barrier_init();
@@ -215,133 +237,161 @@ __global__ void __launch_bounds__(kThreads, 3) wq_mma_kernel(const __grid_consta
     grid_launch_dependents();
     grid_dependency_wait();
 
-    if (kXSmem) {
-        // stage x [M][K] fp16, 16-byte chunks, swizzled
-        const int chunks = static_cast<int>(K / 8);
+    // stage x[:, pass ps] as [M][Kp] fp16, 16-byte chunks, swizzled
+    auto stage_x = [&](int ps) {
+        const int chunks = static_cast<int>(Kp / 8);
+        const uint16_t *src = x + ps * Kp;
         for (int i = tid; i < M * chunks; i += kThreads) {
             const int m = i / chunks, c = i - m * chunks;
-            const uint4 v = ld_shared_v4(x + static_cast<int64_t>(m) * K + 8 * c);
-            *reinterpret_cast<uint4 *>(xs + m * RS + 16 * xs_chunk(static_cast<uint32_t>(c))) = v;
+            cp_async_16(xs + m * RS + 16 * xs_chunk(static_cast<uint32_t>(c)), src + static_cast<int64_t>(m) * K + 8 * c);
         }
-    }
+        cp_async_wait_all();
+    };
+    if (kXSmem) stage_x(0);
     __syncthreads();
 
     int slot = 0;   // ring position of this warp's next item
     uint32_t phase = 0;
-    for (int round = 0; round * B < nt; ++round) {
-        const int bt = min(B, nt - round * B);
-        float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-        int cur = 0;   // tile of the round that d accumulates
-        // zero the partials of this warp for tiles of the round it has no step of
-        auto flush = [&](int upto) {   // store d as tile cur, zeros for cur+1 .. upto-1
-            for (int tb = cur; tb < upto; ++tb) {
-                const bool mine = tb == cur;
-                red(warp, tb * kRowsPerCta + gid, 2 * t) = mine ? d[0] : 0.0f;
-                red(warp, tb * kRowsPerCta + gid, 2 * t + 1) = mine ? d[1] : 0.0f;
-                red(warp, tb * kRowsPerCta + gid + 8, 2 * t) = mine ? d[2] : 0.0f;
-                red(warp, tb * kRowsPerCta + gid + 8, 2 * t + 1) = mine ? d[3] : 0.0f;
-            }
-            d[0] = d[1] = d[2] = d[3] = 0.0f;
-        };
-        for (int tb = tb0, s = s0; tb < bt;) {
-            if (tb != cur) {
-                flush(tb);
-                cur = tb;
-            }
-            if (!mbar_wait_sleep(&bars[slot], phase)) {
-                if (lane == 0) atomicOr(&g_wq_error, kErrWaitTimeout);
-                return;
-            }
-            // codes of rows gid and gid+8: 16-byte chunks 2t, 2t+1 of the row (swizzled by row & 7)
-            const uint8_t *cb = codes_ring + slot * kCodesBox;
-            const uint4 a0 = *reinterpret_cast<const uint4 *>(cb + gid * 128 + 16 * ((2 * t) ^ gid));
-            const uint4 a1 = *reinterpret_cast<const uint4 *>(cb + gid * 128 + 16 * ((2 * t + 1) ^ gid));
-            const uint4 b0 = *reinterpret_cast<const uint4 *>(cb + (gid + 8) * 128 + 16 * ((2 * t) ^ gid));
-            const uint4 b1 = *reinterpret_cast<const uint4 *>(cb + (gid + 8) * 128 + 16 * ((2 * t + 1) ^ gid));
-            uint32_t sa = 0, sb = 0;
-            if (kFp4) {
-                const uint8_t *sbx = scales_ring + slot * kScalesBox;
-                sa = *reinterpret_cast<const uint32_t *>(sbx + gid * 16 + 4 * t);
-                sb = *reinterpret_cast<const uint32_t *>(sbx + (gid + 8) * 16 + 4 * t);
-            }
-            __syncwarp();   // the slot is in registers: refill it
-            if (lane == 0 && pending()) issue(slot);
-
-            uint32_t xw[kXWords];
-            if (has_x) {
+    for (int ps = 0; ps < P; ++ps) {
+        if (ps > 0) {   // every warp is past the previous pass (the barrier ending its last round)
+            stage_x(ps);
+            __syncthreads();
+        }
+        for (int round = 0; round * B < nt; ++round) {
+            const int bt = min(B, nt - round * B);
+            float d[kMT][4];
 #pragma unroll
-                for (int i = 0; i < kXChunks; ++i) {
-                    uint4 v;
-                    if (kXSmem) {
-                        const uint32_t c = static_cast<uint32_t>(s) * (kStepK / 8) + kXChunks * t + i;
-                        v = *reinterpret_cast<const uint4 *>(xs + gid * RS + 16 * xs_chunk(c));
-                    } else {
-                        v = ld_shared_v4(x + gid * K + static_cast<int64_t>(s) * kStepK + (kStepK / 4) * t + 8 * i);
+            for (int mt = 0; mt < kMT; ++mt) d[mt][0] = d[mt][1] = d[mt][2] = d[mt][3] = 0.0f;
+            int cur = 0;   // tile of the round that d accumulates
+            // zero the partials of this warp for tiles of the round it has no step of
+            auto flush = [&](int upto) {   // store d as tile cur, zeros for cur+1 .. upto-1
+                for (int tb = cur; tb < upto; ++tb) {
+                    const bool mine = tb == cur;
+#pragma unroll
+                    for (int mt = 0; mt < kMT; ++mt) {
+                        red(warp, tb * kRowsPerCta + gid, 8 * mt + 2 * t) = mine ? d[mt][0] : 0.0f;
+                        red(warp, tb * kRowsPerCta + gid, 8 * mt + 2 * t + 1) = mine ? d[mt][1] : 0.0f;
+                        red(warp, tb * kRowsPerCta + gid + 8, 8 * mt + 2 * t) = mine ? d[mt][2] : 0.0f;
+                        red(warp, tb * kRowsPerCta + gid + 8, 8 * mt + 2 * t + 1) = mine ? d[mt][3] : 0.0f;
                     }
-                    xw[4 * i] = v.x;
-                    xw[4 * i + 1] = v.y;
-                    xw[4 * i + 2] = v.z;
-                    xw[4 * i + 3] = v.w;
                 }
-            } else {
 #pragma unroll
-                for (int i = 0; i < kXWords; ++i) xw[i] = 0u;
-            }
-            const uint32_t cwa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const uint32_t cwb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-            if (kFp4) {
-                // 4 scale bytes: group q covers this lane's codes bytes 8q..8q+7 (k 64t+16q ..).
-                const uint32_t sa01 = e4m3x2_to_f16x2(sa & 0xffffu), sa23 = e4m3x2_to_f16x2(sa >> 16);
-                const uint32_t sb01 = e4m3x2_to_f16x2(sb & 0xffffu), sb23 = e4m3x2_to_f16x2(sb >> 16);
-                const uint32_t sca[4] = {dup_lo16(sa01), dup_hi16(sa01), dup_lo16(sa23), dup_hi16(sa23)};
-                const uint32_t scb[4] = {dup_lo16(sb01), dup_hi16(sb01), dup_lo16(sb23), dup_hi16(sb23)};
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    // word i = codes bytes 4i..4i+3 = k 8i..8i+7 of this lane's run; group i/2
-                    uint32_t ha[4], hb[4];
-                    e2m1x8_to_f16x2(cwa[i], ha);
-                    e2m1x8_to_f16x2(cwb[i], hb);
-                    const uint32_t ga = sca[i >> 1], gb = scb[i >> 1];
-                    mma_16816(d, hmul2_u32(ha[0], ga), hmul2_u32(hb[0], gb), hmul2_u32(ha[1], ga),
-                              hmul2_u32(hb[1], gb), xw[4 * i], xw[4 * i + 1]);
-                    mma_16816(d, hmul2_u32(ha[2], ga), hmul2_u32(hb[2], gb), hmul2_u32(ha[3], ga),
-                              hmul2_u32(hb[3], gb), xw[4 * i + 2], xw[4 * i + 3]);
+                for (int mt = 0; mt < kMT; ++mt) d[mt][0] = d[mt][1] = d[mt][2] = d[mt][3] = 0.0f;
+            };
+            for (int tb = tb0, s = s0; tb < bt;) {
+                if (tb != cur) {
+                    flush(tb);
+                    cur = tb;
                 }
-            } else {
+                if (!mbar_wait_sleep(&bars[slot], phase)) {
+                    if (lane == 0) atomicOr(&g_wq_error, kErrWaitTimeout);
+                    return;
+                }
+                // codes of rows gid and gid+8: 16-byte chunks 2t, 2t+1 of the row (swizzled by row & 7)
+                const uint8_t *cb = codes_ring + slot * kCodesBox;
+                const uint4 a0 = *reinterpret_cast<const uint4 *>(cb + gid * 128 + 16 * ((2 * t) ^ gid));
+                const uint4 a1 = *reinterpret_cast<const uint4 *>(cb + gid * 128 + 16 * ((2 * t + 1) ^ gid));
+                const uint4 b0 = *reinterpret_cast<const uint4 *>(cb + (gid + 8) * 128 + 16 * ((2 * t) ^ gid));
+                const uint4 b1 = *reinterpret_cast<const uint4 *>(cb + (gid + 8) * 128 + 16 * ((2 * t + 1) ^ gid));
+                uint32_t sa = 0, sb = 0;
+                if (kFp4) {
+                    const uint8_t *sbx = scales_ring + slot * kScalesBox;
+                    sa = *reinterpret_cast<const uint32_t *>(sbx + gid * 16 + 4 * t);
+                    sb = *reinterpret_cast<const uint32_t *>(sbx + (gid + 8) * 16 + 4 * t);
+                }
+                __syncwarp();   // the slot is in registers: refill it
+                if (lane == 0 && pending()) issue(slot);
+
+                uint32_t xw[kMT][kXWords];   // B fragments: activation rows gid + 8 mt
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    // word j = codes bytes 4j..4j+3 = k 4j..4j+3 of this lane's run
-                    mma_16816(d, e4m3x2_to_f16x2(cwa[j] & 0xffffu), e4m3x2_to_f16x2(cwb[j] & 0xffffu),
-                              e4m3x2_to_f16x2(cwa[j] >> 16), e4m3x2_to_f16x2(cwb[j] >> 16), xw[2 * j],
-                              xw[2 * j + 1]);
+                for (int mt = 0; mt < kMT; ++mt) {
+                    const int xr = gid + 8 * mt;
+                    if (xr < M) {
+#pragma unroll
+                        for (int i = 0; i < kXChunks; ++i) {
+                            uint4 v;
+                            if (kXSmem) {
+                                const uint32_t c = static_cast<uint32_t>(s) * (kStepK / 8) + kXChunks * t + i;
+                                v = *reinterpret_cast<const uint4 *>(xs + xr * RS + 16 * xs_chunk(c));
+                            } else {
+                                v = ld_shared_v4(x + xr * K + static_cast<int64_t>(ps * nsteps + s) * kStepK +
+                                                 (kStepK / 4) * t + 8 * i);
+                            }
+                            xw[mt][4 * i] = v.x;
+                            xw[mt][4 * i + 1] = v.y;
+                            xw[mt][4 * i + 2] = v.z;
+                            xw[mt][4 * i + 3] = v.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < kXWords; ++i) xw[mt][i] = 0u;
+                    }
+                }
+                const uint32_t cwa[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+                const uint32_t cwb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+                if (kFp4) {
+                    // 4 scale bytes: group q covers this lane's codes bytes 8q..8q+7 (k 64t+16q ..).
+                    const uint32_t sa01 = e4m3x2_to_f16x2(sa & 0xffffu), sa23 = e4m3x2_to_f16x2(sa >> 16);
+                    const uint32_t sb01 = e4m3x2_to_f16x2(sb & 0xffffu), sb23 = e4m3x2_to_f16x2(sb >> 16);
+                    const uint32_t sca[4] = {dup_lo16(sa01), dup_hi16(sa01), dup_lo16(sa23), dup_hi16(sa23)};
+                    const uint32_t scb[4] = {dup_lo16(sb01), dup_hi16(sb01), dup_lo16(sb23), dup_hi16(sb23)};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        // word i = codes bytes 4i..4i+3 = k 8i..8i+7 of this lane's run; group i/2
+                        uint32_t ha[4], hb[4];
+                        e2m1x8_to_f16x2(cwa[i], ha);
+                        e2m1x8_to_f16x2(cwb[i], hb);
+                        const uint32_t ga = sca[i >> 1], gb = scb[i >> 1];
+                        const uint32_t a00 = hmul2_u32(ha[0], ga), a01 = hmul2_u32(hb[0], gb);
+                        const uint32_t a02 = hmul2_u32(ha[1], ga), a03 = hmul2_u32(hb[1], gb);
+                        const uint32_t a10 = hmul2_u32(ha[2], ga), a11 = hmul2_u32(hb[2], gb);
+                        const uint32_t a12 = hmul2_u32(ha[3], ga), a13 = hmul2_u32(hb[3], gb);
+#pragma unroll
+                        for (int mt = 0; mt < kMT; ++mt) {
+                            mma_16816(d[mt], a00, a01, a02, a03, xw[mt][4 * i], xw[mt][4 * i + 1]);
+                            mma_16816(d[mt], a10, a11, a12, a13, xw[mt][4 * i + 2], xw[mt][4 * i + 3]);
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        // word j = codes bytes 4j..4j+3 = k 4j..4j+3 of this lane's run
+                        const uint32_t a0 = e4m3x2_to_f16x2(cwa[j] & 0xffffu), a1 = e4m3x2_to_f16x2(cwb[j] & 0xffffu);
+                        const uint32_t a2 = e4m3x2_to_f16x2(cwa[j] >> 16), a3 = e4m3x2_to_f16x2(cwb[j] >> 16);
+#pragma unroll
+                        for (int mt = 0; mt < kMT; ++mt) mma_16816(d[mt], a0, a1, a2, a3, xw[mt][2 * j], xw[mt][2 * j + 1]);
+                    }
+                }
+                if (++slot == S) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+                s += kWarps;
+                while (s >= nsteps) {
+                    s -= nsteps;
+                    ++tb;
                 }
             }
-            if (++slot == S) {
-                slot = 0;
-                phase ^= 1u;
+            flush(bt);
+            __syncthreads();
+            for (int e = tid; e < bt * kRowsPerCta * 8 * kMT; e += kThreads) {
+                const int rr = e / (8 * kMT), m = e - rr * (8 * kMT), tb = rr / kRowsPerCta, r = rr - tb * kRowsPerCta;
+                int mi;
+                int64_t row0;
+                locate(blockIdx.x + static_cast<int64_t>(gridDim.x) * (round * B + tb), mi, row0);
+                const int64_t n = row0 + r, Nm = p.N[mi];
+                if (m < M && n < Nm) {
+                    float sum = 0.0f;
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) sum += red(w, rr, m);
+                    float *out = &p.y[mi][m * Nm + n];
+                    // later passes add to what this thread wrote for the same element
+                    const float v = sum * (kFp4 ? p.g[mi] : p.row_scale[mi][n]);
+                    *out = ps > 0 ? *out + v : v;
+                }
             }
-            s += kWarps;
-            while (s >= nsteps) {
-                s -= nsteps;
-                ++tb;
-            }
+            __syncthreads();   // red is reused by the next round
         }
-        flush(bt);
-        __syncthreads();
-        for (int e = tid; e < bt * kRowsPerCta * 8; e += kThreads) {
-            const int rr = e >> 3, m = e & 7, tb = rr / kRowsPerCta, r = rr - tb * kRowsPerCta;
-            int mi;
-            int64_t row0;
-            locate(blockIdx.x + static_cast<int64_t>(gridDim.x) * (round * B + tb), mi, row0);
-            const int64_t n = row0 + r, Nm = p.N[mi];
-            if (m < M && n < Nm) {
-                float sum = 0.0f;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) sum += red(w, rr, m);
-                p.y[mi][m * Nm + n] = sum * (kFp4 ? p.g[mi] : p.row_scale[mi][n]);
-            }
-        }
-        __syncthreads();   // red is reused by the next round
     }
 }
 
@@ -398,38 +448,73 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const 
     cfg.numAttrs = set_launch_overlap_attr(attr);
     route_hit(r);
     if (r == kRouteNvfp4Mma || r == kRouteFp8Mma) {
+        // up to 8 activation rows per row tile; 9..16 rows take two tiles per weight pass
+        using Kern = void (*)(WqParams, const uint16_t *, int, int64_t, int, int, int);
+        const int mt = M > 8 ? 2 : 1;
+        auto kernel_of = [mt](bool xs) -> Kern {
+            if (mt == 2) return xs ? wq_mma_kernel<kFp4, true, 2> : wq_mma_kernel<kFp4, false, 2>;
+            return xs ? wq_mma_kernel<kFp4, true, 1> : wq_mma_kernel<kFp4, false, 1>;
+        };
         int64_t ntiles = 0;
         for (int i = 0; i < grp.count; ++i) ntiles += (grp.N[i] + kRowsPerCta - 1) / kRowsPerCta;
         if (ntiles == 0) return cudaSuccess;
-        const int64_t nsteps = K / (kFp4 ? 2 * kStepBytes : kStepBytes);
-        // tiles per round: a multiple of 8 / gcd(steps, 8), so every warp gets the same
-        // number of steps, and enough for 8 steps per warp between the round's barriers
-        int gcd = kWarps;
-        while (nsteps % gcd) gcd >>= 1;   // gcd(nsteps, 8): kWarps is a power of two
-        const int unit = static_cast<int>(kWarps / gcd);
-        int B = unit;
-        while (B * nsteps < 8 * kWarps && B + unit <= kMaxRound) B += unit;
+        constexpr int kStepK = kFp4 ? 2 * kStepBytes : kStepBytes;   // k per step
+        const int64_t nsteps_all = K / kStepK;
+        // tiles per round for `ns` steps per pass: a multiple of 8 / gcd(ns, 8), so every
+        // warp gets the same number of steps, and enough for 8 steps per warp between
+        // the round's barriers
+        auto round_unit = [](int64_t ns) {
+            int gcd = kWarps;
+            while (ns % gcd) gcd >>= 1;   // gcd(ns, 8): kWarps is a power of two
+            return static_cast<int>(kWarps / gcd);
+        };
+        auto round_tiles = [&](int64_t ns) {
+            const int unit = round_unit(ns);
+            int b = unit;
+            while (b * ns < 8 * kWarps && b + unit <= kMaxRound) b += unit;
+            return b;
+        };
         // Candidates (ring slots, activations in shared memory), scored by the tail they
         // leave: whole tiles over `grid` CTAs take ceil(tiles / grid) rounds, so the
         // busiest CTA holds waves * grid / tiles times the mean. Within 15 % of the mean
         // the deepest ring wins (two CTAs per SM at least); else the least imbalance.
         // Activations stay in shared memory whenever they fit (re-read through L1 they
-        // thrash it at M = 8); at M <= 2, where they fit in L1, an unstaged candidate may
-        // win on balance.
-        const uint32_t xbytes = static_cast<uint32_t>(M) * xs_row_stride(K);
-        const bool x_ok = xbytes <= static_cast<uint32_t>(env_int("QMV_WQ_XSMEM_MAX", 160 * 1024));
+        // thrash it at M = 8), in as few passes over K as that takes; at M <= 2, where
+        // they fit in L1, an unstaged candidate may win on balance.
+        const uint32_t x_cap = static_cast<uint32_t>(env_int("QMV_WQ_XSMEM_MAX", 200 * 1024));
+        const int p_env = env_int("QMV_WQ_PASSES", 0);
         const int s_env = env_int("QMV_WQ_SLOTS", 0);
         struct Cand { int S; bool xs; };
         const Cand cands[] = {{4, true}, {3, true}, {2, true}, {4, false}, {3, false}, {2, false}};
-        int best = -1, best_occ = 0;
+        int best = -1, best_occ = 0, best_B = 0, best_P = 1;
         double best_score = 1e30;
         for (int c = 0; c < 6; ++c) {
-            if (cands[c].xs && !x_ok) continue;
             if (!cands[c].xs && best >= 0 && cands[best].xs && (M > 2 || best_score <= 1.15)) break;
             const int Sc = s_env > 0 ? std::min(8, s_env) : cands[c].S;
-            const uint32_t dyn = wq_layout(Sc, B, cands[c].xs ? xbytes : 0u).total + 1024;
-            if (dyn > static_cast<uint32_t>(dev.smem_optin)) continue;
-            auto kc = cands[c].xs ? wq_mma_kernel<kFp4, true> : wq_mma_kernel<kFp4, false>;
+            // staged: the fewest passes (dividing the steps) whose slice of x fits, with
+            // fewer tiles per round (a smaller reduction buffer) where that makes it fit
+            int Pc = 0, Bc = 0;
+            uint32_t dyn = 0;
+            for (int pp = 1; pp <= (cands[c].xs ? 8 : 1) && Pc == 0; ++pp) {
+                if (p_env > 0 && cands[c].xs && pp != p_env) continue;
+                if (nsteps_all % pp) continue;
+                const int64_t ns = nsteps_all / pp;
+                const uint64_t xb = cands[c].xs ? static_cast<uint64_t>(M) * xs_row_stride(ns * kStepK) : 0;
+                if (xb > x_cap) continue;
+                const int unit = round_unit(ns);
+                int b = round_tiles(ns);
+                uint32_t d = wq_layout(Sc, b, static_cast<uint32_t>(xb), mt).total + 1024;
+                while (d > static_cast<uint32_t>(dev.smem_optin) && b > unit) {
+                    b -= unit;
+                    d = wq_layout(Sc, b, static_cast<uint32_t>(xb), mt).total + 1024;
+                }
+                if (d > static_cast<uint32_t>(dev.smem_optin)) continue;
+                Pc = pp;
+                Bc = b;
+                dyn = d;
+            }
+            if (Pc == 0) continue;
+            const Kern kc = kernel_of(cands[c].xs);
             cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kc), dev.smem_optin,
                                              cands[c].xs ? cudaSharedmemCarveoutMaxShared : -1);
             if (e != cudaSuccess) return e;
@@ -445,12 +530,16 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const 
                 best_score = score;
                 best = c;
                 best_occ = occ;
+                best_B = Bc;
+                best_P = Pc;
             }
         }
         if (best < 0) return cudaErrorInvalidValue;
         const int S = s_env > 0 ? std::min(8, s_env) : cands[best].S;
         const bool xsmem = cands[best].xs;
-        const WqLayout L = wq_layout(S, B, xsmem ? xbytes : 0u);
+        const int B = best_B, P = best_P;
+        const uint32_t xbytes = xsmem ? static_cast<uint32_t>(M) * xs_row_stride(K / P) : 0u;
+        const WqLayout L = wq_layout(S, B, xbytes, mt);
         const int per_sm = std::min(4, best_occ);
         cfg.gridDim =
             dim3(static_cast<unsigned>(std::min<int64_t>(ntiles, static_cast<int64_t>(dev.sm_count) * per_sm)));
@@ -475,9 +564,13 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const 
             }
         }
         for (int i = grp.count; i <= kMaxGroup; ++i) p.tile_start[i] = t;
-        auto kern = xsmem ? wq_mma_kernel<kFp4, true> : wq_mma_kernel<kFp4, false>;
+        const Kern kern = kernel_of(xsmem);
         cfg.dynamicSmemBytes = L.total + 1024;
-        return cudaLaunchKernelEx(&cfg, kern, p, x, M, K, S, B);
+        if (env_int("QMV_PLAN_LOG", 0))   // diagnostic: the chosen plan, one line per launch
+            std::fprintf(stderr, "wq plan: fmt=%s M=%d K=%lld tiles=%lld S=%d xsmem=%d P=%d B=%d occ=%d grid=%u smem=%u\n",
+                         kFp4 ? "nvfp4" : "fp8", M, static_cast<long long>(K), static_cast<long long>(ntiles), S,
+                         xsmem ? 1 : 0, P, B, best_occ, cfg.gridDim.x, static_cast<unsigned>(cfg.dynamicSmemBytes));
+        return cudaLaunchKernelEx(&cfg, kern, p, x, M, K, S, B, P);
     }
     if (grp.count != 1) return cudaErrorInvalidValue;   // groups need the tensor-core kernel
     const int64_t N = grp.N[0];
@@ -487,8 +580,13 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const 
     auto kern = wq_generic_kernel<kFp4>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), 0, -1);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, kern, grp.codes[0], grp.scales[0], grp.row_scale[0], grp.g[0], x, grp.y[0], M, N,
-                              K);
+    // 8 activation rows per launch
+    for (int m0 = 0; m0 < M; m0 += 8) {
+        e = cudaLaunchKernelEx(&cfg, kern, grp.codes[0], grp.scales[0], grp.row_scale[0], grp.g[0], x + m0 * K,
+                               grp.y[0] + m0 * N, std::min(8, M - m0), N, K);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -1,7 +1,8 @@
 """GPU parity: NVFP4 W4A16 and FP8 W8A16 skinny GEMM through the C ABI vs the CPU oracle.
 
 fp32 outputs within |y - y_ref| <= 1e-3 * sum|w*x| + 1e-6 on: several tiles with
-a ragged tail at M = 1..8; the full-size matrices of the 27B-class dense stack
+a ragged tail at M = 1..16 (rows 9..16 as a second activation tile of the same
+weight pass); the full-size matrices of the 27B-class dense stack
 and its 151936-row lm_head (sampled rows); fp16 activation outliers up to
 6e4 (the overflow case of "v100-skinny README", section "How QPN works");
 zero scales; K that is not a multiple of the streaming step (generic kernel).
@@ -11,7 +12,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import assert_close
+from gpu_util import TOL_ABS, TOL_REL, assert_close
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -53,65 +54,68 @@ def _fp8(q, M, N, K, seed, outliers=0, rows=None):
     return y
 
 
-@pytest.mark.parametrize("M", range(1, 9))
+@pytest.mark.parametrize("M", range(1, 17))
 def test_nvfp4_multi_tile_ragged(q, M):
     q.route_reset()
     _nvfp4(q, M, 16 * 37 + 5, 5120, seed=300 + M)
     assert q.route_counts()["nvfp4_mma_m16n8k16"] == 1
 
 
-@pytest.mark.parametrize("M", range(1, 9))
+@pytest.mark.parametrize("M", range(1, 17))
 def test_fp8_multi_tile_ragged(q, M):
     q.route_reset()
     _fp8(q, M, 16 * 21 + 11, 5120, seed=400 + M)
     assert q.route_counts()["fp8_mma_m16n8k16"] == 1
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 1, 256), (3, 17, 512), (8, 16, 17408), (2, 100, 768)])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 256), (3, 17, 512), (8, 16, 17408), (2, 100, 768),
+                                   (9, 100, 768), (12, 33, 512), (16, 16, 17408), (16, 1, 256)])
 def test_nvfp4_shapes(q, M, N, K):
     _nvfp4(q, M, N, K, seed=N + K)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 1, 128), (5, 40, 384), (8, 16, 17408), (2, 31, 1152)])
+@pytest.mark.parametrize("M,N,K", [(1, 1, 128), (5, 40, 384), (8, 16, 17408), (2, 31, 1152),
+                                   (13, 31, 1152), (16, 40, 384), (16, 16, 17408)])
 def test_fp8_shapes(q, M, N, K):
     _fp8(q, M, N, K, seed=N + K)
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 33, 16), (4, 19, 80), (8, 40, 5136)])
+@pytest.mark.parametrize("M,N,K", [(1, 33, 16), (4, 19, 80), (8, 40, 5136), (11, 19, 80),
+                                   (16, 40, 5136)])
 def test_nvfp4_generic_k(q, M, N, K):
     q.route_reset()
     _nvfp4(q, M, N, K, seed=K)
     assert q.route_counts()["nvfp4_generic"] == 1
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 9, 1), (3, 21, 100), (8, 33, 5130)])
+@pytest.mark.parametrize("M,N,K", [(1, 9, 1), (3, 21, 100), (8, 33, 5130), (9, 21, 100), (16, 33, 5130)])
 def test_fp8_generic_k(q, M, N, K):
     q.route_reset()
     _fp8(q, M, N, K, seed=K)
     assert q.route_counts()["fp8_generic"] == 1
 
 
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 8, 16])
 def test_outliers(q, M):
     _nvfp4(q, M, 64, 5120, seed=9, outliers=8)
     _fp8(q, M, 64, 5120, seed=10, outliers=8)
 
 
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 8, 16])
 @pytest.mark.parametrize("N,K", [(7168, 5120), (5120, 5120), (17408, 5120), (5120, 17408)])
 def test_nvfp4_27b_shapes_sampled(q, M, N, K):
     rows = _synth().sample_rows(N, 64, seed=N + K).numpy()
     _nvfp4(q, M, N, K, seed=N * 5 + K + M, rows=rows)
 
 
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 8, 16])
 def test_nvfp4_lm_head_sampled(q, M):
     N, K = 151936, 5120
     rows = _synth().sample_rows(N, 48, seed=M).numpy()
     _nvfp4(q, M, N, K, seed=151936 + M, rows=rows)
 
 
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 8, 16])
 @pytest.mark.parametrize("N,K", [(7168, 5120), (5120, 5120)])
 def test_fp8_27b_attention_shapes_sampled(q, M, N, K):
     rows = _synth().sample_rows(N, 64, seed=N + K + 1).numpy()
@@ -159,7 +163,7 @@ def test_k0_and_empty(q):
 
 # ------------------------------------------------ grouped launches (one shared x)
 
-@pytest.mark.parametrize("M", [1, 3, 8])
+@pytest.mark.parametrize("M", [1, 3, 8, 12, 16])
 def test_nvfp4_group_matches_oracle(q, M):
     """gate/up-like groups with ragged row counts: every output within the bound."""
     synth = _synth()
@@ -176,7 +180,7 @@ def test_nvfp4_group_matches_oracle(q, M):
         assert_close(f"group[{i}]", outs[i].cpu().numpy()[:, rows], y_ref, bound)
 
 
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 8, 16])
 def test_fp8_group_matches_oracle(q, M):
     synth = _synth()
     K = 5120
@@ -196,3 +200,59 @@ def test_group_of_one_equals_single_call(q):
     c, sc, g = synth.nvfp4_weights(5120, 17408, seed=3, device=DEV)
     x = synth.activations_f16(2, 17408, seed=4, device=DEV)
     assert torch.equal(q.qgemm_nvfp4_w4a16_group([c], [sc], [g], x)[0], q.qgemm_nvfp4_w4a16(c, sc, g, x))
+
+
+# ------------------------------------------------ 9..16 activation rows
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "fp8"])
+@pytest.mark.parametrize("M,K", [(16, 5120), (12, 2048), (9, 17408)])
+@pytest.mark.parametrize("staged", [True, False])
+def test_two_row_tiles_staged_and_unstaged(q, monkeypatch, fmt, M, K, staged):
+    """Activations in shared memory (when they fit) and read through L1: both within the bound."""
+    monkeypatch.setenv("QMV_WQ_XSMEM_MAX", str(1 << 20) if staged else "0")
+    N = 16 * 45 + 3
+    if fmt == "nvfp4":
+        _nvfp4(q, M, N, K, seed=950 + M)
+    else:
+        _fp8(q, M, N, K, seed=960 + M)
+
+
+def test_rows_beyond_8_do_not_disturb_first_8(q):
+    """Rows 1..8 of an M = 16 call agree with the M = 8 call on the same rows (same bound)."""
+    synth = _synth()
+    codes, scales, g = synth.nvfp4_weights(16 * 30 + 7, 4096, seed=21, device=DEV)
+    x = synth.activations_f16(16, 4096, seed=22, device=DEV)
+    y16 = q.qgemm_nvfp4_w4a16(codes, scales, g, x).cpu().numpy()
+    y8 = q.qgemm_nvfp4_w4a16(codes, scales, g, x[:8].contiguous()).cpu().numpy()
+    _, bound = oracle.nvfp4_w4a16(codes.cpu().numpy(), scales.cpu().numpy(), g, x[:8].cpu().numpy())
+    assert np.all(np.abs(y16[:8] - y8) <= 2 * (TOL_REL * bound + TOL_ABS))
+
+
+@pytest.mark.parametrize("fmt,K,passes", [("nvfp4", 4096, 2), ("nvfp4", 4096, 8), ("nvfp4", 17408, 4),
+                                          ("fp8", 5120, 5), ("fp8", 1024, 8)])
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_k_passes(q, monkeypatch, fmt, K, passes, M):
+    """Activations staged one K slice at a time (outputs accumulated over the passes)."""
+    monkeypatch.setenv("QMV_WQ_PASSES", str(passes))
+    monkeypatch.setenv("QMV_WQ_XSMEM_MAX", str(1 << 20))
+    N = 16 * 23 + 9
+    if fmt == "nvfp4":
+        _nvfp4(q, M, N, K, seed=1000 + M + passes)
+    else:
+        _fp8(q, M, N, K, seed=1100 + M + passes)
+
+
+@pytest.mark.parametrize("M", [4, 16])
+def test_k_passes_group(q, monkeypatch, M):
+    """A gate/up-like group with K cut into passes: each matrix within the bound."""
+    monkeypatch.setenv("QMV_WQ_PASSES", "4")
+    synth = _synth()
+    K = 17408
+    Ns = [5120, 40, 1000]
+    mats = [synth.nvfp4_weights(n, K, seed=1200 + i, device=DEV) for i, n in enumerate(Ns)]
+    x = synth.activations_f16(M, K, seed=1290, device=DEV, outliers=2)
+    outs = q.qgemm_nvfp4_w4a16_group([m[0] for m in mats], [m[1] for m in mats], [m[2] for m in mats], x)
+    for i, (c, sc, g) in enumerate(mats):
+        rows = np.arange(Ns[i]) if Ns[i] < 2000 else synth.sample_rows(Ns[i], 64, seed=i).numpy()
+        y_ref, bound = oracle.nvfp4_w4a16(c.cpu().numpy()[rows], sc.cpu().numpy()[rows], g, x.cpu().numpy())
+        assert_close(f"passes group[{i}]", outs[i].cpu().numpy()[:, rows], y_ref, bound)
