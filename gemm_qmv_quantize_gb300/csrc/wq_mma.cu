@@ -89,7 +89,7 @@ namespace {
 
 __device__ uint32_t g_wq_error;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 256;   // the generic kernel; the tensor-core kernel runs 8 or 16 warps
 constexpr int kWarps = 8;
 constexpr int kRowsPerCta = 16;
 constexpr int kStepBytes = 128;   // bytes of one weight row per warp step
@@ -109,17 +109,17 @@ struct WqLayout {
     uint32_t off_codes, off_scales, off_bar, off_red, off_x, total;
 };
 
-// Shared memory: per-warp rings of codes boxes (1024-byte aligned for the swizzle),
-// of scale boxes, their mbarriers, the round's partial sums [warp][B * 16 rows][9],
-// then the staged activations.
-__host__ __device__ inline WqLayout wq_layout(int S, int B, uint32_t xbytes, int mt)
+// Shared memory of W warps: per-warp rings of codes boxes (1024-byte aligned for the
+// swizzle), of scale boxes, their mbarriers, the round's partial sums
+// [warp][B * 16 rows][8 mt + 1], then the staged activations.
+__host__ __device__ inline WqLayout wq_layout(int S, int B, uint32_t xbytes, int mt, int W)
 {
     WqLayout L;
     L.off_codes = 0;
-    L.off_scales = static_cast<uint32_t>(kWarps * S * kCodesBox);
-    L.off_bar = L.off_scales + static_cast<uint32_t>(kWarps * S * kScalesBox);
-    L.off_red = (L.off_bar + static_cast<uint32_t>(kWarps * S) * 8u + 15u) & ~15u;
-    L.off_x = (L.off_red + static_cast<uint32_t>(kWarps * B * kRowsPerCta * red_pitch(mt)) * 4u + 127u) & ~127u;
+    L.off_scales = static_cast<uint32_t>(W * S * kCodesBox);
+    L.off_bar = L.off_scales + static_cast<uint32_t>(W * S * kScalesBox);
+    L.off_red = (L.off_bar + static_cast<uint32_t>(W * S) * 8u + 15u) & ~15u;
+    L.off_x = (L.off_red + static_cast<uint32_t>(W * B * kRowsPerCta * red_pitch(mt)) * 4u + 127u) & ~127u;
     L.total = L.off_x + xbytes;
     return L;
 }
@@ -142,9 +142,11 @@ struct WqParams {
 // kMT: 8-row tiles of activations per weight pass (M <= 8 kMT): the decoded weight
 // fragments feed kMT mma each, so up to 16 rows share one weight stream.
 // kXSmem: activations staged in shared memory.
+// kW: warps per CTA (8, or 16 sharing one staged copy of large activations).
 // P: passes over K (staged activations only; 1 otherwise), K / kStepK a multiple of P.
-template <bool kFp4, bool kXSmem, int kMT>
-__global__ void __launch_bounds__(kThreads, kMT == 1 ? 3 : 2) wq_mma_kernel(const __grid_constant__ WqParams p,
+template <bool kFp4, bool kXSmem, int kMT, int kW>
+__global__ void __launch_bounds__(32 * kW, kW == 16 ? 1 : (kMT == 1 ? 3 : 2))
+    wq_mma_kernel(const __grid_constant__ WqParams p,
                                                             const uint16_t *__restrict__ x, int M, int64_t K, int S,
                                                             int B, int P)
 {
@@ -170,7 +172,8 @@ __global__ void __launch_bounds__(kThreads, kMT == 1 ? 3 : 2) wq_mma_kernel(cons
     };
     constexpr int kPitch = red_pitch(kMT);
     const uint32_t RS = xs_row_stride(Kp);
-    const WqLayout L = wq_layout(S, B, kXSmem ? static_cast<uint32_t>(M) * RS : 0u, kMT);
+    constexpr int kT = 32 * kW;   // threads
+    const WqLayout L = wq_layout(S, B, kXSmem ? static_cast<uint32_t>(M) * RS : 0u, kMT, kW);
     uint8_t *codes_ring = smem + L.off_codes + warp * S * kCodesBox;
     uint8_t *scales_ring = smem + L.off_scales + warp * S * kScalesBox;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.off_bar) + warp * S;
@@ -184,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, kMT == 1 ? 3 : 2) wq_mma_kernel(cons
 
     // This CTA's tiles blockIdx.x + gridDim.x * lt, lt < nt, in rounds of B tiles; a
     // round's items j = tb * nsteps + step (tile tb of the round), and this warp's
-    // are j = warp, warp + 8, ... Lane 0 keeps S of them in flight.
+    // are j = warp, warp + kW, ... Lane 0 keeps S of them in flight.
     const int nt = static_cast<int>((ntiles - blockIdx.x + gridDim.x - 1) / gridDim.x);
     // first item of a round for this warp: tile warp / nsteps, step warp % nsteps
     const int tb0 = warp / nsteps, s0 = warp - tb0 * nsteps;
@@ -217,14 +220,14 @@ __global__ void __launch_bounds__(kThreads, kMT == 1 ? 3 : 2) wq_mma_kernel(cons
         const int gs = p_ps * nsteps + p_step;   // step over the whole of K
         tma_load_2d(codes_ring + slot * kCodesBox, &p.codes[p_mi], gs * kStepBytes, y0, &bars[slot], pol);
         if (kFp4) tma_load_2d(scales_ring + slot * kScalesBox, &p.scales[p_mi], gs * 16, y0, &bars[slot], pol);
-        p_step += kWarps;
-        while (p_step >= nsteps) {   // once when nsteps >= 8
+        p_step += kW;
+        while (p_step >= nsteps) {   // once when nsteps >= kW
             p_step -= nsteps;
             ++p_lt;
         }
         settle();
     };
-    // rounds before the last hold a multiple of 8 items, so a warp with an item in
+    // rounds before the last hold a multiple of kW items, so a warp with an item in
     // one round has one in every round of the pass but perhaps the last
     auto pending = [&]() { return p_ps < P && p_lt < p_rend; };
     if (lane == 0) {
@@ -241,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, kMT == 1 ? 3 : 2) wq_mma_kernel(cons
     auto stage_x = [&](int ps) {
         const int chunks = static_cast<int>(Kp / 8);
         const uint16_t *src = x + ps * Kp;
-        for (int i = tid; i < M * chunks; i += kThreads) {
+        for (int i = tid; i < M * chunks; i += kT) {
             const int m = i / chunks, c = i - m * chunks;
             cp_async_16(xs + m * RS + 16 * xs_chunk(static_cast<uint32_t>(c)), src + static_cast<int64_t>(m) * K + 8 * c);
         }
@@ -259,9 +262,14 @@ __global__ void __launch_bounds__(kThreads, kMT == 1 ? 3 : 2) wq_mma_kernel(cons
         }
         for (int round = 0; round * B < nt; ++round) {
             const int bt = min(B, nt - round * B);
-            float d[kMT][4];
+            // accumulators; with one row tile the two mma of a word go to d and e, two
+            // independent chains (kMT = 2 has its tiles' chains already)
+            constexpr bool kDual = kMT == 1 && kXSmem;   // (unstaged: no registers to spare)
+            float d[kMT][4], e[kMT][4];
 #pragma unroll
-            for (int mt = 0; mt < kMT; ++mt) d[mt][0] = d[mt][1] = d[mt][2] = d[mt][3] = 0.0f;
+            for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) d[mt][c] = e[mt][c] = 0.0f;
             int cur = 0;   // tile of the round that d accumulates
             // zero the partials of this warp for tiles of the round it has no step of
             auto flush = [&](int upto) {   // store d as tile cur, zeros for cur+1 .. upto-1
@@ -269,14 +277,19 @@ __global__ void __launch_bounds__(kThreads, kMT == 1 ? 3 : 2) wq_mma_kernel(cons
                     const bool mine = tb == cur;
 #pragma unroll
                     for (int mt = 0; mt < kMT; ++mt) {
-                        red(warp, tb * kRowsPerCta + gid, 8 * mt + 2 * t) = mine ? d[mt][0] : 0.0f;
-                        red(warp, tb * kRowsPerCta + gid, 8 * mt + 2 * t + 1) = mine ? d[mt][1] : 0.0f;
-                        red(warp, tb * kRowsPerCta + gid + 8, 8 * mt + 2 * t) = mine ? d[mt][2] : 0.0f;
-                        red(warp, tb * kRowsPerCta + gid + 8, 8 * mt + 2 * t + 1) = mine ? d[mt][3] : 0.0f;
+                        float v[4];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) v[c] = mine ? d[mt][c] + (kDual ? e[mt][c] : 0.0f) : 0.0f;
+                        red(warp, tb * kRowsPerCta + gid, 8 * mt + 2 * t) = v[0];
+                        red(warp, tb * kRowsPerCta + gid, 8 * mt + 2 * t + 1) = v[1];
+                        red(warp, tb * kRowsPerCta + gid + 8, 8 * mt + 2 * t) = v[2];
+                        red(warp, tb * kRowsPerCta + gid + 8, 8 * mt + 2 * t + 1) = v[3];
                     }
                 }
 #pragma unroll
-                for (int mt = 0; mt < kMT; ++mt) d[mt][0] = d[mt][1] = d[mt][2] = d[mt][3] = 0.0f;
+                for (int mt = 0; mt < kMT; ++mt)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) d[mt][c] = e[mt][c] = 0.0f;
             };
             for (int tb = tb0, s = s0; tb < bt;) {
                 if (tb != cur) {
@@ -302,21 +315,29 @@ __global__ void __launch_bounds__(kThreads, kMT == 1 ? 3 : 2) wq_mma_kernel(cons
                 __syncwarp();   // the slot is in registers: refill it
                 if (lane == 0 && pending()) issue(slot);
 
-                uint32_t xw[kMT][kXWords];   // B fragments: activation rows gid + 8 mt
+                // B fragments: activation rows gid + 8 mt. Columns of D past M are never
+                // stored, so their lanes need only finite values: from shared memory they
+                // read row M - 1 (a broadcast, no divergence); from global memory they skip
+                // the load and take zeros (8 lanes load instead of 32 at M = 1, through L1).
+                uint32_t xw[kMT][kXWords];
 #pragma unroll
                 for (int mt = 0; mt < kMT; ++mt) {
-                    const int xr = gid + 8 * mt;
-                    if (xr < M) {
+                    const int xr = min(gid + 8 * mt, M - 1);
+                    if (kXSmem) {
 #pragma unroll
                         for (int i = 0; i < kXChunks; ++i) {
-                            uint4 v;
-                            if (kXSmem) {
-                                const uint32_t c = static_cast<uint32_t>(s) * (kStepK / 8) + kXChunks * t + i;
-                                v = *reinterpret_cast<const uint4 *>(xs + xr * RS + 16 * xs_chunk(c));
-                            } else {
-                                v = ld_shared_v4(x + xr * K + static_cast<int64_t>(ps * nsteps + s) * kStepK +
-                                                 (kStepK / 4) * t + 8 * i);
-                            }
+                            const uint32_t c = static_cast<uint32_t>(s) * (kStepK / 8) + kXChunks * t + i;
+                            const uint4 v = *reinterpret_cast<const uint4 *>(xs + xr * RS + 16 * xs_chunk(c));
+                            xw[mt][4 * i] = v.x;
+                            xw[mt][4 * i + 1] = v.y;
+                            xw[mt][4 * i + 2] = v.z;
+                            xw[mt][4 * i + 3] = v.w;
+                        }
+                    } else if (gid + 8 * mt < M) {
+#pragma unroll
+                        for (int i = 0; i < kXChunks; ++i) {
+                            const uint4 v = ld_shared_v4(x + xr * K + static_cast<int64_t>(ps * nsteps + s) * kStepK +
+                                                         (kStepK / 4) * t + 8 * i);
                             xw[mt][4 * i] = v.x;
                             xw[mt][4 * i + 1] = v.y;
                             xw[mt][4 * i + 2] = v.z;
@@ -349,7 +370,7 @@ __global__ void __launch_bounds__(kThreads, kMT == 1 ? 3 : 2) wq_mma_kernel(cons
 #pragma unroll
                         for (int mt = 0; mt < kMT; ++mt) {
                             mma_16816(d[mt], a00, a01, a02, a03, xw[mt][4 * i], xw[mt][4 * i + 1]);
-                            mma_16816(d[mt], a10, a11, a12, a13, xw[mt][4 * i + 2], xw[mt][4 * i + 3]);
+                            mma_16816(kDual ? e[mt] : d[mt], a10, a11, a12, a13, xw[mt][4 * i + 2], xw[mt][4 * i + 3]);
                         }
                     }
                 } else {
@@ -359,14 +380,15 @@ __global__ void __launch_bounds__(kThreads, kMT == 1 ? 3 : 2) wq_mma_kernel(cons
                         const uint32_t a0 = e4m3x2_to_f16x2(cwa[j] & 0xffffu), a1 = e4m3x2_to_f16x2(cwb[j] & 0xffffu);
                         const uint32_t a2 = e4m3x2_to_f16x2(cwa[j] >> 16), a3 = e4m3x2_to_f16x2(cwb[j] >> 16);
 #pragma unroll
-                        for (int mt = 0; mt < kMT; ++mt) mma_16816(d[mt], a0, a1, a2, a3, xw[mt][2 * j], xw[mt][2 * j + 1]);
+                        for (int mt = 0; mt < kMT; ++mt)
+                            mma_16816(kDual && (j & 1) ? e[mt] : d[mt], a0, a1, a2, a3, xw[mt][2 * j], xw[mt][2 * j + 1]);
                     }
                 }
                 if (++slot == S) {
                     slot = 0;
                     phase ^= 1u;
                 }
-                s += kWarps;
+                s += kW;
                 while (s >= nsteps) {
                     s -= nsteps;
                     ++tb;
@@ -374,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, kMT == 1 ? 3 : 2) wq_mma_kernel(cons
             }
             flush(bt);
             __syncthreads();
-            for (int e = tid; e < bt * kRowsPerCta * 8 * kMT; e += kThreads) {
+            for (int e = tid; e < bt * kRowsPerCta * 8 * kMT; e += kT) {
                 const int rr = e / (8 * kMT), m = e - rr * (8 * kMT), tb = rr / kRowsPerCta, r = rr - tb * kRowsPerCta;
                 int mi;
                 int64_t row0;
@@ -383,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, kMT == 1 ? 3 : 2) wq_mma_kernel(cons
                 if (m < M && n < Nm) {
                     float sum = 0.0f;
 #pragma unroll
-                    for (int w = 0; w < kWarps; ++w) sum += red(w, rr, m);
+                    for (int w = 0; w < kW; ++w) sum += red(w, rr, m);
                     float *out = &p.y[mi][m * Nm + n];
                     // later passes add to what this thread wrote for the same element
                     const float v = sum * (kFp4 ? p.g[mi] : p.row_scale[mi][n]);
@@ -451,45 +473,54 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const 
         // up to 8 activation rows per row tile; 9..16 rows take two tiles per weight pass
         using Kern = void (*)(WqParams, const uint16_t *, int, int64_t, int, int, int);
         const int mt = M > 8 ? 2 : 1;
-        auto kernel_of = [mt](bool xs) -> Kern {
-            if (mt == 2) return xs ? wq_mma_kernel<kFp4, true, 2> : wq_mma_kernel<kFp4, false, 2>;
-            return xs ? wq_mma_kernel<kFp4, true, 1> : wq_mma_kernel<kFp4, false, 1>;
+        auto kernel_of = [mt](bool xs, int W) -> Kern {
+            if (W == 16) return mt == 2 ? wq_mma_kernel<kFp4, true, 2, 16> : wq_mma_kernel<kFp4, true, 1, 16>;
+            if (mt == 2) return xs ? wq_mma_kernel<kFp4, true, 2, 8> : wq_mma_kernel<kFp4, false, 2, 8>;
+            return xs ? wq_mma_kernel<kFp4, true, 1, 8> : wq_mma_kernel<kFp4, false, 1, 8>;
         };
         int64_t ntiles = 0;
         for (int i = 0; i < grp.count; ++i) ntiles += (grp.N[i] + kRowsPerCta - 1) / kRowsPerCta;
         if (ntiles == 0) return cudaSuccess;
         constexpr int kStepK = kFp4 ? 2 * kStepBytes : kStepBytes;   // k per step
         const int64_t nsteps_all = K / kStepK;
-        // tiles per round for `ns` steps per pass: a multiple of 8 / gcd(ns, 8), so every
-        // warp gets the same number of steps, and enough for 8 steps per warp between
-        // the round's barriers
-        auto round_unit = [](int64_t ns) {
-            int gcd = kWarps;
-            while (ns % gcd) gcd >>= 1;   // gcd(ns, 8): kWarps is a power of two
-            return static_cast<int>(kWarps / gcd);
+        // tiles per round for `ns` steps per pass and W warps: a multiple of W / gcd(ns, W),
+        // so every warp gets the same number of steps, and enough for 8 steps per warp
+        // between the round's barriers
+        auto round_unit = [](int64_t ns, int W) {
+            int gcd = W;
+            while (ns % gcd) gcd >>= 1;   // gcd(ns, W): W is a power of two
+            return static_cast<int>(W / gcd);
         };
-        auto round_tiles = [&](int64_t ns) {
-            const int unit = round_unit(ns);
+        auto round_tiles = [&](int64_t ns, int W) {
+            const int unit = round_unit(ns, W);
             int b = unit;
-            while (b * ns < 8 * kWarps && b + unit <= kMaxRound) b += unit;
+            while (b * ns < 8 * W && b + unit <= kMaxRound) b += unit;
             return b;
         };
-        // Candidates (ring slots, activations in shared memory), scored by the tail they
-        // leave: whole tiles over `grid` CTAs take ceil(tiles / grid) rounds, so the
-        // busiest CTA holds waves * grid / tiles times the mean. Within 15 % of the mean
-        // the deepest ring wins (two CTAs per SM at least); else the least imbalance.
-        // Activations stay in shared memory whenever they fit (re-read through L1 they
-        // thrash it at M = 8), in as few passes over K as that takes; at M <= 2, where
-        // they fit in L1, an unstaged candidate may win on balance.
+        // Candidates (warps, ring slots, activations in shared memory), scored by the
+        // tail they leave: whole tiles over `grid` CTAs take ceil(tiles / grid) rounds, so
+        // the busiest CTA holds waves * grid / tiles times the mean. Within 15 % of the mean
+        // a candidate scores 1, else its imbalance; fewer than 16 resident warps per SM
+        // add 0.5 (too few to hide the decode latency), each pass over K beyond the first
+        // adds 1 (a pass repeats the per-round reduction); ties keep the earlier (deeper
+        // ring) candidate. Activations stay in shared memory whenever they fit (re-read
+        // through L1 they thrash it at M = 8); 16 warps share one staged copy where 8-warp
+        // CTAs would fit only one per SM. At M <= 2, where the activations fit in L1, an
+        // unstaged candidate may win on balance.
         const uint32_t x_cap = static_cast<uint32_t>(env_int("QMV_WQ_XSMEM_MAX", 200 * 1024));
         const int p_env = env_int("QMV_WQ_PASSES", 0);
         const int s_env = env_int("QMV_WQ_SLOTS", 0);
-        struct Cand { int S; bool xs; };
-        const Cand cands[] = {{4, true}, {3, true}, {2, true}, {4, false}, {3, false}, {2, false}};
+        const int w_env = env_int("QMV_WQ_WARPS", 0);
+        struct Cand { int W, S; bool xs; };
+        const Cand cands[] = {{8, 4, true}, {8, 3, true}, {8, 2, true}, {16, 3, true}, {16, 2, true},
+                              {8, 4, false}, {8, 3, false}, {8, 2, false}};
+        constexpr int kCands = static_cast<int>(sizeof(cands) / sizeof(cands[0]));
         int best = -1, best_occ = 0, best_B = 0, best_P = 1;
         double best_score = 1e30;
-        for (int c = 0; c < 6; ++c) {
+        for (int c = 0; c < kCands; ++c) {
             if (!cands[c].xs && best >= 0 && cands[best].xs && (M > 2 || best_score <= 1.15)) break;
+            if (w_env > 0 && cands[c].W != w_env) continue;
+            const int Wc = cands[c].W;
             const int Sc = s_env > 0 ? std::min(8, s_env) : cands[c].S;
             // staged: the fewest passes (dividing the steps) whose slice of x fits, with
             // fewer tiles per round (a smaller reduction buffer) where that makes it fit
@@ -501,12 +532,13 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const 
                 const int64_t ns = nsteps_all / pp;
                 const uint64_t xb = cands[c].xs ? static_cast<uint64_t>(M) * xs_row_stride(ns * kStepK) : 0;
                 if (xb > x_cap) continue;
-                const int unit = round_unit(ns);
-                int b = round_tiles(ns);
-                uint32_t d = wq_layout(Sc, b, static_cast<uint32_t>(xb), mt).total + 1024;
+                const int unit = round_unit(ns, Wc);
+                if (unit > kMaxRound) continue;
+                int b = round_tiles(ns, Wc);
+                uint32_t d = wq_layout(Sc, b, static_cast<uint32_t>(xb), mt, Wc).total + 1024;
                 while (d > static_cast<uint32_t>(dev.smem_optin) && b > unit) {
                     b -= unit;
-                    d = wq_layout(Sc, b, static_cast<uint32_t>(xb), mt).total + 1024;
+                    d = wq_layout(Sc, b, static_cast<uint32_t>(xb), mt, Wc).total + 1024;
                 }
                 if (d > static_cast<uint32_t>(dev.smem_optin)) continue;
                 Pc = pp;
@@ -514,18 +546,17 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const 
                 dyn = d;
             }
             if (Pc == 0) continue;
-            const Kern kc = kernel_of(cands[c].xs);
+            const Kern kc = kernel_of(cands[c].xs, Wc);
             cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kc), dev.smem_optin,
                                              cands[c].xs ? cudaSharedmemCarveoutMaxShared : -1);
             if (e != cudaSuccess) return e;
             int occ = 0;
-            if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kc, kThreads, dyn)) != cudaSuccess) return e;
+            if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kc, 32 * Wc, dyn)) != cudaSuccess) return e;
             occ = std::min(occ, 4);
             if (occ < 1) continue;
             const int64_t g = std::min<int64_t>(ntiles, static_cast<int64_t>(dev.sm_count) * occ);
             const double imb = static_cast<double>((ntiles + g - 1) / g * g) / static_cast<double>(ntiles);
-            // balanced candidates tie at 1 and the earlier (deeper, staged) one stays
-            const double score = (imb <= 1.15 ? 1.0 : imb) + (occ < 2 ? 0.5 : 0.0);
+            const double score = (imb <= 1.15 ? 1.0 : imb) + (occ * Wc < 16 ? 0.5 : 0.0) + (Pc - 1);
             if (score < best_score) {
                 best_score = score;
                 best = c;
@@ -535,11 +566,13 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const 
             }
         }
         if (best < 0) return cudaErrorInvalidValue;
+        const int W = cands[best].W;
         const int S = s_env > 0 ? std::min(8, s_env) : cands[best].S;
         const bool xsmem = cands[best].xs;
         const int B = best_B, P = best_P;
         const uint32_t xbytes = xsmem ? static_cast<uint32_t>(M) * xs_row_stride(K / P) : 0u;
-        const WqLayout L = wq_layout(S, B, xbytes, mt);
+        const WqLayout L = wq_layout(S, B, xbytes, mt, W);
+        cfg.blockDim = dim3(static_cast<unsigned>(32 * W));
         const int per_sm = std::min(4, best_occ);
         cfg.gridDim =
             dim3(static_cast<unsigned>(std::min<int64_t>(ntiles, static_cast<int64_t>(dev.sm_count) * per_sm)));
@@ -564,11 +597,11 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const 
             }
         }
         for (int i = grp.count; i <= kMaxGroup; ++i) p.tile_start[i] = t;
-        const Kern kern = kernel_of(xsmem);
+        const Kern kern = kernel_of(xsmem, W);
         cfg.dynamicSmemBytes = L.total + 1024;
         if (env_int("QMV_PLAN_LOG", 0))   // diagnostic: the chosen plan, one line per launch
-            std::fprintf(stderr, "wq plan: fmt=%s M=%d K=%lld tiles=%lld S=%d xsmem=%d P=%d B=%d occ=%d grid=%u smem=%u\n",
-                         kFp4 ? "nvfp4" : "fp8", M, static_cast<long long>(K), static_cast<long long>(ntiles), S,
+            std::fprintf(stderr, "wq plan: fmt=%s M=%d K=%lld tiles=%lld W=%d S=%d xsmem=%d P=%d B=%d occ=%d grid=%u smem=%u\n",
+                         kFp4 ? "nvfp4" : "fp8", M, static_cast<long long>(K), static_cast<long long>(ntiles), W, S,
                          xsmem ? 1 : 0, P, B, best_occ, cfg.gridDim.x, static_cast<unsigned>(cfg.dynamicSmemBytes));
         return cudaLaunchKernelEx(&cfg, kern, p, x, M, K, S, B, P);
     }

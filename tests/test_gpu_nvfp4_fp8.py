@@ -256,3 +256,34 @@ def test_k_passes_group(q, monkeypatch, M):
         rows = np.arange(Ns[i]) if Ns[i] < 2000 else synth.sample_rows(Ns[i], 64, seed=i).numpy()
         y_ref, bound = oracle.nvfp4_w4a16(c.cpu().numpy()[rows], sc.cpu().numpy()[rows], g, x.cpu().numpy())
         assert_close(f"passes group[{i}]", outs[i].cpu().numpy()[:, rows], y_ref, bound)
+
+
+# ------------------------------------------------ 16-warp CTAs sharing one staged activation copy
+
+@pytest.mark.parametrize("fmt", ["nvfp4", "fp8"])
+@pytest.mark.parametrize("M", [1, 3, 8, 9, 16])
+def test_sixteen_warps(q, monkeypatch, fmt, M):
+    """16 warps per CTA (rounds of 16 interleaved steps, 16-way reduction): within the bound."""
+    monkeypatch.setenv("QMV_WQ_WARPS", "16")
+    N = 16 * 45 + 3
+    if fmt == "nvfp4":
+        _nvfp4(q, M, N, 5120, seed=1300 + M)
+    else:
+        _fp8(q, M, N, 5120, seed=1400 + M)
+
+
+@pytest.mark.parametrize("passes", [2, 5])
+def test_sixteen_warps_passes_group(q, monkeypatch, passes):
+    """16 warps, K cut into passes (5 passes: 4 steps per pass, fewer than the warps)."""
+    monkeypatch.setenv("QMV_WQ_WARPS", "16")
+    monkeypatch.setenv("QMV_WQ_PASSES", str(passes))
+    synth = _synth()
+    K = 5120
+    Ns = [17408, 40, 1000]
+    mats = [synth.nvfp4_weights(n, K, seed=1500 + i, device=DEV) for i, n in enumerate(Ns)]
+    x = synth.activations_f16(8, K, seed=1590, device=DEV, outliers=2)
+    outs = q.qgemm_nvfp4_w4a16_group([m[0] for m in mats], [m[1] for m in mats], [m[2] for m in mats], x)
+    for i, (c, sc, g) in enumerate(mats):
+        rows = np.arange(Ns[i]) if Ns[i] < 2000 else synth.sample_rows(Ns[i], 64, seed=i).numpy()
+        y_ref, bound = oracle.nvfp4_w4a16(c.cpu().numpy()[rows], sc.cpu().numpy()[rows], g, x.cpu().numpy())
+        assert_close(f"16 warps, passes group[{i}]", outs[i].cpu().numpy()[:, rows], y_ref, bound)
