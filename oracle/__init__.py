@@ -62,6 +62,15 @@ def _load(path):
     lib.oracle_nvfp4_w4a16.restype = None
     lib.oracle_fp8_w8a16.argtypes = [_u8p, _f32p, _u16p, _i64, _i64, _i64, _f64p, _f64p]
     lib.oracle_fp8_w8a16.restype = None
+    lib.oracle_q4_k_scale_min.argtypes = [_u8p, ctypes.c_int, ctypes.POINTER(ctypes.c_int),
+                                          ctypes.POINTER(ctypes.c_int)]
+    lib.oracle_q4_k_scale_min.restype = None
+    lib.oracle_q4_k_weight.argtypes = [_u8p, ctypes.c_int]
+    lib.oracle_q4_k_weight.restype = ctypes.c_double
+    lib.oracle_q4_k_block_dots.argtypes = [_u8p, _u8p, _i64, _i64, _i64, _i32p]
+    lib.oracle_q4_k_block_dots.restype = None
+    lib.oracle_q4_k_q8_1.argtypes = [_u8p, _u8p, _i64, _i64, _i64, _f64p, _f64p]
+    lib.oracle_q4_k_q8_1.restype = None
     return lib
 
 
@@ -170,5 +179,57 @@ def fp8_w8a16(w: np.ndarray, row_scale: np.ndarray, x_f16: np.ndarray):
     bound = np.zeros((M, N), dtype=np.float64)
     _lib().oracle_fp8_w8a16(_ptr(w, ctypes.c_uint8), _ptr(rs, ctypes.c_float),
                             _ptr(x, ctypes.c_uint16), M, N, K,
+                            _ptr(y, ctypes.c_double), _ptr(bound, ctypes.c_double))
+    return y, bound
+
+
+# ---------------------------------------------------------------- Q4_K
+
+def q4_k_scale_min(packed12: np.ndarray, j: int):
+    """(sc, mn) of sub-block j from the 12 packed scale bytes of a Q4_K super-block."""
+    p = _as(packed12, np.uint8)
+    assert p.shape == (12,)
+    sc, mn = ctypes.c_int(), ctypes.c_int()
+    _lib().oracle_q4_k_scale_min(_ptr(p, ctypes.c_uint8), int(j), ctypes.byref(sc), ctypes.byref(mn))
+    return sc.value, mn.value
+
+
+def q4_k_dequantize(w: np.ndarray, K: int) -> np.ndarray:
+    """Q4_K [N][K/256*144] bytes -> fp64 weights [N][K] (element by element)."""
+    w = _as(w, np.uint8)
+    N, nsb = w.shape[0], K // 256
+    assert w.shape[1] == nsb * 144
+    lib = _lib()
+    out = np.zeros((N, K), dtype=np.float64)
+    for n in range(N):
+        for s in range(nsb):
+            blk = np.ascontiguousarray(w[n, s * 144:(s + 1) * 144])
+            bp = _ptr(blk, ctypes.c_uint8)
+            for i in range(256):
+                out[n, s * 256 + i] = lib.oracle_q4_k_weight(bp, i)
+    return out
+
+
+def q4_k_block_dots(w: np.ndarray, xq: np.ndarray, K: int) -> np.ndarray:
+    """Integer sub-block sums S [M][N][K/32] = sum q4u*q8 (q4u the unsigned nibble)."""
+    w = _as(w, np.uint8)
+    xq = _as(xq, np.uint8)
+    N, M, nb = w.shape[0], xq.shape[0], K // 32
+    assert K % 256 == 0 and w.shape[1] == K // 256 * 144 and xq.shape[1] == nb * 36
+    S = np.zeros((M, N, nb), dtype=np.int32)
+    _lib().oracle_q4_k_block_dots(_ptr(w, ctypes.c_uint8), _ptr(xq, ctypes.c_uint8), M, N, K,
+                                  _ptr(S, ctypes.c_int32))
+    return S
+
+
+def q4_k_q8_1(w: np.ndarray, xq: np.ndarray, K: int):
+    """y [M][N] (fp64) and bound [M][N] for Q4_K weights against Q8_1 activations."""
+    w = _as(w, np.uint8)
+    xq = _as(xq, np.uint8)
+    N, M, nb = w.shape[0], xq.shape[0], K // 32
+    assert K % 256 == 0 and w.shape[1] == K // 256 * 144 and xq.shape[1] == nb * 36
+    y = np.zeros((M, N), dtype=np.float64)
+    bound = np.zeros((M, N), dtype=np.float64)
+    _lib().oracle_q4_k_q8_1(_ptr(w, ctypes.c_uint8), _ptr(xq, ctypes.c_uint8), M, N, K,
                             _ptr(y, ctypes.c_double), _ptr(bound, ctypes.c_double))
     return y, bound

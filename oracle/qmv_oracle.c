@@ -311,3 +311,100 @@ void oracle_fp8_w8a16(const uint8_t *w, const float *rs, const uint16_t *x, int6
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Q4_K x Q8_1                                                              */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The Q4_K super-block ("Machine Learning on NVIDIA CMP", section "llama.cpp
+ * results" names the Q4_K_M models; the pages do not print the layout, which is
+ * llama.cpp's GGUF K-quant format): 256 weights in 144 bytes,
+ *   bytes 0..1    d     (fp16) scale of the sub-block scales
+ *   bytes 2..3    dmin  (fp16) scale of the sub-block minimums
+ *   bytes 4..15   eight 6-bit sub-block scales sc[j] and minimums mn[j], packed:
+ *                 j < 4:  sc = byte[j] & 63,  mn = byte[j+4] & 63
+ *                 j >= 4: sc = (byte[j+4] & 15) | (byte[j-4] >> 6) << 4
+ *                         mn = (byte[j+4] >> 4) | (byte[j]   >> 6) << 4
+ *   bytes 16..143 128 bytes of unsigned nibbles: byte 32c + e holds element
+ *                 64c + e in its low nibble and element 64c + 32 + e in its high
+ *                 nibble (c = 0..3, e = 0..31), i.e. sub-block 2c in the low and
+ *                 sub-block 2c + 1 in the high nibbles of the same 32 bytes.
+ * Element i of sub-block j (32 weights) has the value
+ *   w = d * sc[j] * q - dmin * mn[j].
+ */
+
+/* The 6-bit scale and minimum of sub-block j (0..7) from the 12 packed bytes. */
+void oracle_q4_k_scale_min(const uint8_t *p, int j, int *sc, int *mn)
+{
+    if (j < 4) {
+        *sc = p[j] & 63;
+        *mn = p[j + 4] & 63;
+    } else {
+        *sc = (p[j + 4] & 15) | ((p[j - 4] >> 6) << 4);
+        *mn = (p[j + 4] >> 4) | ((p[j] >> 6) << 4);
+    }
+}
+
+/* Unsigned nibble of element i (0..255) of a super-block's 128 data bytes. */
+static int q4_k_nibble(const uint8_t *qs, int i)
+{
+    int c = i / 64, r = i % 64;
+    return (r < 32) ? (qs[32 * c + r] & 0x0f) : (qs[32 * c + r - 32] >> 4);
+}
+
+/* Dequantized value of element i (0..255) of one 144-byte super-block. */
+double oracle_q4_k_weight(const uint8_t *blk, int i)
+{
+    int sc, mn;
+    oracle_q4_k_scale_min(blk + 4, i / 32, &sc, &mn);
+    double d = oracle_fp16_to_double(read_u16le(blk));
+    double dmin = oracle_fp16_to_double(read_u16le(blk + 2));
+    return d * (double)sc * (double)q4_k_nibble(blk + 16, i) - dmin * (double)mn;
+}
+
+/*
+ * Integer dots of the MMVQ inner loop per 32-weight sub-block b (= Q8_1 block b):
+ *   S[m][n][b] = sum_i q4u_i * q8_i   (q4u the unsigned nibble, 0..15)
+ * w: Q4_K [N][K/256] super-blocks of 144 bytes; xq: Q8_1 [M][K/32] blocks.
+ */
+void oracle_q4_k_block_dots(const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N,
+                            int64_t K, int32_t *S)
+{
+    int64_t nsb = K / 256, nb = K / 32;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            for (int64_t b = 0; b < nb; ++b) {
+                const uint8_t *qs = w + (n * nsb + b / 8) * 144 + 16;
+                const int8_t *q8 = (const int8_t *)(xq + (m * nb + b) * 36 + 4);
+                int32_t s = 0;
+                for (int i = 0; i < 32; ++i) s += q4_k_nibble(qs, (int)(b % 8) * 32 + i) * q8[i];
+                S[(m * N + n) * nb + b] = s;
+            }
+        }
+    }
+}
+
+/*
+ * y[m][n] = sum_k w[n][k] * xhat[m][k] in fp64, w the dequantized Q4_K value above
+ * and xhat = d8 * q8 the dequantized Q8_1 activation; bound = sum_k |w * xhat|.
+ */
+void oracle_q4_k_q8_1(const uint8_t *w, const uint8_t *xq, int64_t M, int64_t N, int64_t K,
+                      double *y, double *bound)
+{
+    int64_t nsb = K / 256, nb = K / 32;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                const uint8_t *xb = xq + (m * nb + k / 32) * 36;
+                double wv = oracle_q4_k_weight(w + (n * nsb + k / 256) * 144, (int)(k % 256));
+                double xv = oracle_fp16_to_double(read_u16le(xb)) * (double)((const int8_t *)(xb + 4))[k % 32];
+                acc += wv * xv;
+                mag += fabs(wv * xv);
+            }
+            y[m * N + n] = acc;
+            bound[m * N + n] = mag;
+        }
+    }
+}

@@ -17,7 +17,7 @@ from conftest import ROOT
 
 SRC = os.path.join(ROOT, "oracle", "qmv_oracle.c")
 PIN_TESTS = ["tests/test_oracle_codecs.py", "tests/test_oracle_quantize.py",
-             "tests/test_oracle_q4_0.py", "tests/test_oracle_nvfp4_fp8.py"]
+             "tests/test_oracle_q4_0.py", "tests/test_oracle_nvfp4_fp8.py", "tests/test_oracle_q4_k.py"]
 
 MUTANTS = {
     "q4_nibble_halves_swapped": ("(j < 16) ? (qs[j] & 0x0f) : (qs[j - 16] >> 4)",
@@ -36,6 +36,20 @@ MUTANTS = {
                            "oracle_e4m3_to_double(scales[n * (K / 16) + k / 32])"),
     "e4m3_bias": ("else v = ldexp((double)(8 + m), e - 10);", "else v = ldexp((double)(8 + m), e - 9);"),
     "e2m1_table": ("{0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0}", "{0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 8.0}"),
+    "q4k_min_sign": ("* (double)q4_k_nibble(blk + 16, i) - dmin * (double)mn;",
+                     "* (double)q4_k_nibble(blk + 16, i) + dmin * (double)mn;"),
+    "q4k_dmin_read_as_d": ("double dmin = oracle_fp16_to_double(read_u16le(blk + 2));",
+                           "double dmin = oracle_fp16_to_double(read_u16le(blk));"),
+    "q4k_scale_min_swapped": ("*sc = p[j] & 63;\n        *mn = p[j + 4] & 63;",
+                              "*sc = p[j + 4] & 63;\n        *mn = p[j] & 63;"),
+    "q4k_high_bits_from_wrong_byte": ("*sc = (p[j + 4] & 15) | ((p[j - 4] >> 6) << 4);",
+                                      "*sc = (p[j + 4] & 15) | ((p[j] >> 6) << 4);"),
+    "q4k_nibble_halves_swapped": ("(r < 32) ? (qs[32 * c + r] & 0x0f) : (qs[32 * c + r - 32] >> 4)",
+                                  "(r < 32) ? (qs[32 * c + r] >> 4) : (qs[32 * c + r - 32] & 0x0f)"),
+    "q4k_adjacent_nibble_pairs": ("(r < 32) ? (qs[32 * c + r] & 0x0f) : (qs[32 * c + r - 32] >> 4)",
+                                  "(r % 2 == 0) ? (qs[32 * c + r / 2] & 0x0f) : (qs[32 * c + r / 2] >> 4)"),
+    "q4k_sub_block_of_next": ("oracle_q4_k_scale_min(blk + 4, i / 32, &sc, &mn);",
+                              "oracle_q4_k_scale_min(blk + 4, (i / 32 + 1) % 8, &sc, &mn);"),
     "fp8_x_transposed": ("double xv = oracle_fp16_to_double(x[m * K + k]);\n                acc += wv * xv;\n                mag += fabs(wv * xv);\n            }\n            y[m * N + n] = acc;\n            bound[m * N + n] = mag;\n        }\n    }\n}\n",
                          "double xv = oracle_fp16_to_double(x[(k * M + m) % (M * K)]);\n                acc += wv * xv;\n                mag += fabs(wv * xv);\n            }\n            y[m * N + n] = acc;\n            bound[m * N + n] = mag;\n        }\n    }\n}\n"),
 }
