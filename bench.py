@@ -35,7 +35,7 @@ if ROOT not in sys.path:
 
 METRIC = "achieved weight-stream GB/s and % of HBM roofline; equiv. decode tok/s (M=1..8)"
 FALLBACK_HBM_GBS = 6800.0
-Q4_0_BLOCK, Q8_1_BLOCK = 18, 36
+Q4_0_BLOCK, Q4_K_BLOCK, Q8_1_BLOCK = 18, 144, 36
 
 # ----------------------------------------------------------------------------- workloads
 
@@ -78,6 +78,24 @@ def dense_27b_stages(mixed: bool):
     return st + ([[320]] if mixed else [])
 
 
+def qwen3_8b_stack():
+    """Qwen3-8B-shaped Q4_K stack ("Machine Learning on NVIDIA CMP", section "llama.cpp
+    results", names Qwen3-8B Q4_K_M; every matrix here is Q4_K): 36 layers of
+    {q 4096x4096, k and v 1024x4096 (8 KV heads of 128), o 4096x4096, gate and up
+    12288x4096, down 4096x12288} plus the 151936x4096 lm_head."""
+    layer = [(4096, 4096), (1024, 4096), (1024, 4096), (4096, 4096), (12288, 4096), (12288, 4096), (4096, 12288)]
+    return [("q4_k", n, k) for _ in range(36) for (n, k) in layer] + [("q4_k", 151936, 4096)]
+
+
+def qwen3_8b_stages():
+    """Per layer {q, k, v}, {o}, {gate, up}, {down}; then the lm_head: 145 stages."""
+    st = []
+    for layer in range(36):
+        b = 7 * layer
+        st += [[b, b + 1, b + 2], [b + 3], [b + 4, b + 5], [b + 6]]
+    return st + [[252]]
+
+
 def llama3_8b_mlp():
     return [("q4_0", 14336, 4096), ("q4_0", 14336, 4096), ("q4_0", 4096, 14336)]
 
@@ -85,6 +103,10 @@ def llama3_8b_mlp():
 WORKLOADS = {
     "llama2_7b_q4_0_m1": dict(M=1, mats=llama2_7b_stack, stages=llama2_7b_stages,
                              desc="Llama-2-7B-shaped Q4_0 decode stack, M=1 (225 matrices + per-call Q8_1 quantize)"),
+    "qwen3_8b_q4_k_m1": dict(M=1, mats=qwen3_8b_stack, stages=qwen3_8b_stages,
+                             desc="Qwen3-8B-shaped Q4_K decode stack, M=1 (253 matrices + per-call Q8_1 quantize)"),
+    "qwen3_8b_q4_k_m8": dict(M=8, mats=qwen3_8b_stack, stages=qwen3_8b_stages,
+                             desc="Qwen3-8B-shaped Q4_K decode stack, M=8"),
     "nvfp4_27b_m1": dict(M=1, mats=lambda: dense_27b_stack(False), stages=lambda: dense_27b_stages(False),
                          desc="27B-class dense NVFP4 W4A16 stack, M=1"),
     "nvfp4_27b_m8": dict(M=8, mats=lambda: dense_27b_stack(False), stages=lambda: dense_27b_stages(False),
@@ -110,6 +132,8 @@ WORKLOADS["q4_0_11008x4096_m1"] = dict(M=1, mats=lambda: [("q4_0", 11008, 4096)]
                                        desc="Q4_0 GEMV M=1, 11008x4096, 16 rotated copies")
 WORKLOADS["q4_0_14336x4096_m8"] = dict(M=8, mats=lambda: [("q4_0", 14336, 4096)] * 8,
                                        desc="Q4_0 M=8, 14336x4096 (Llama-3-8B gate), 8 rotated copies")
+WORKLOADS["q4_k_12288x4096_m1"] = dict(M=1, mats=lambda: [("q4_k", 12288, 4096)] * 16,
+                                       desc="Q4_K GEMV M=1, 12288x4096 (Qwen3-8B gate), 16 rotated copies")
 for _m in (1, 8, 16):
     WORKLOADS[f"nvfp4_17408x5120_m{_m}"] = dict(M=_m, mats=lambda: [("nvfp4", 17408, 5120)] * 8,
                                                desc=f"NVFP4 W4A16 17408x5120, M={_m}, 8 rotated copies")
@@ -121,6 +145,8 @@ DEFAULT_WORKLOAD = "llama2_7b_q4_0_m1"
 def weight_bytes(fmt, n, k):
     if fmt == "q4_0":
         return n * (k // 32) * Q4_0_BLOCK
+    if fmt == "q4_k":
+        return n * (k // 256) * Q4_K_BLOCK
     if fmt == "nvfp4":
         return n * k // 2 + n * k // 16
     return n * k + 4 * n   # fp8 + fp32 row scale
@@ -128,8 +154,8 @@ def weight_bytes(fmt, n, k):
 
 def act_bytes(fmt, M, k, fused=False):
     """Activation bytes a call reads: Q4_0 reads Q8_1 activations, or fp32 ones when
-    the quantize is fused in; NVFP4 and FP8 read fp16."""
-    if fmt == "q4_0":
+    the quantize is fused in (Q4_K likewise); NVFP4 and FP8 read fp16."""
+    if fmt in ("q4_0", "q4_k"):
         return M * k * 4 if fused else M * (k // 32) * Q8_1_BLOCK
     return M * k * 2
 
@@ -299,6 +325,8 @@ class Stack:
             s = seed * 100003 + i
             if fmt == "q4_0":
                 self.weights.append((synth.q4_0_weights(n, k, s, device),))
+            elif fmt == "q4_k":
+                self.weights.append((synth.q4_k_weights(n, k, s, device),))
             elif fmt == "nvfp4":
                 self.weights.append(synth.nvfp4_weights(n, k, s, device))
             else:
@@ -308,7 +336,7 @@ class Stack:
         first = [st[0] for st in deps]
         for st in deps:
             assert len({(self.mats[i][0], self.mats[i][2]) for i in st}) == 1, "a shared input has one format and K"
-        x_is_f32 = [self.mats[i][0] == "q4_0" for i in first]
+        x_is_f32 = [self.mats[i][0] in ("q4_0", "q4_k") for i in first]
         x_sizes = [M * self.mats[i][2] * (4 if f else 2) for i, f in zip(first, x_is_f32)]
         self.x_bytes = sum(x_sizes)
         self.x_buf = torch.empty(self.x_bytes, dtype=torch.uint8, device=device)
@@ -330,7 +358,7 @@ class Stack:
             off += M * n
         # Q8_1 activations of the two-call path: one buffer per stage input
         xq_in = [torch.empty((M, self.mats[i][2] // 32 * Q8_1_BLOCK), dtype=torch.uint8, device=device)
-                 if self.mats[i][0] == "q4_0" else None for i in first]
+                 if self.mats[i][0] in ("q4_0", "q4_k") else None for i in first]
         self.xqs = [xq_in[self.input_of[i]] for i in range(len(self.mats))]
         self.bytes_per_step = sum(self.launch_bytes(st) for st in self.stages)
         self.weight_bytes = sum(weight_bytes(fmt, n, k) for fmt, n, k in self.mats)
@@ -342,7 +370,7 @@ class Stack:
         for j, st in enumerate(self.stages):
             if len(st) > 1:
                 fmt = self.mats[st[0]][0]
-                if fmt == "q4_0" and not self.fused:   # the stage's matrices share their input: quantize it once
+                if fmt in ("q4_0", "q4_k") and not self.fused:   # the stage's matrices share their input: quantize it once
                     q.qmv_quantize_q8_1(self.xs[st[0]], out=self.xqs[st[0]])
                 if events is not None:
                     events[j][0].record()
@@ -353,6 +381,12 @@ class Stack:
                 elif fmt == "fp8":
                     q.qgemm_fp8_w8a16_group([self.weights[i][0] for i in st], [self.weights[i][1] for i in st],
                                             self.xs[st[0]], [self.ys[i] for i in st])
+                elif fmt == "q4_k" and self.fused:
+                    q.qmv_q4_k_q8_1_fused_group([self.weights[i][0] for i in st], [self.xs[i] for i in st],
+                                                [self.ys[i] for i in st])
+                elif fmt == "q4_k":
+                    q.qmv_q4_k_q8_1_group([self.weights[i][0] for i in st], [self.xqs[i] for i in st],
+                                          self.mats[st[0]][2], [self.ys[i] for i in st])
                 elif self.fused:
                     q.qmv_q4_0_q8_1_fused_group([self.weights[i][0] for i in st], [self.xs[i] for i in st],
                                                 [self.ys[i] for i in st])
@@ -368,11 +402,15 @@ class Stack:
         import gemm_qmv_quantize_gb300 as q
         fmt, n, k = self.mats[i]
         x, y, wt = self.xs[i], self.ys[i], self.weights[i]
-        if fmt == "q4_0" and not self.fused:
+        if fmt in ("q4_0", "q4_k") and not self.fused:
             q.qmv_quantize_q8_1(x, out=self.xqs[i])
         if ev is not None:
             ev[0].record()
-        if fmt == "q4_0" and self.fused:
+        if fmt == "q4_k" and self.fused:
+            q.qmv_q4_k_q8_1_fused(wt[0], x, out=y)
+        elif fmt == "q4_k":
+            q.qmv_q4_k_q8_1(wt[0], self.xqs[i], k, out=y)
+        elif fmt == "q4_0" and self.fused:
             q.qmv_q4_0_q8_1_fused(wt[0], x, out=y)
         elif fmt == "q4_0":
             q.qmv_q4_0_q8_1(wt[0], self.xqs[i], k, out=y)
@@ -393,7 +431,7 @@ class Stack:
         return b
 
     def kernels_per_step(self):
-        return sum(2 if (self.mats[st[0]][0] == "q4_0" and not self.fused) else 1 for st in self.stages)
+        return sum(2 if (self.mats[st[0]][0] in ("q4_0", "q4_k") and not self.fused) else 1 for st in self.stages)
 
 
 def capture(fn, stream):
@@ -506,7 +544,7 @@ def _run_ours_on_stream(args, rank, world, local_rank, stack, stream, barrier, m
 
 def dtype_of(stack):
     fmts = {f for f, _, _ in stack.mats}
-    if fmts == {"q4_0"}:
+    if fmts <= {"q4_0", "q4_k"}:
         return "int8 dp4a (int32 block sums) + fp32 scale/accumulate"
     return "fp16 x fp16 tensor-core MMA, fp32 accumulate (exact fp16 decode of e2m1/e4m3)"
 
@@ -617,6 +655,9 @@ class OracleSampler:
             if fmt == "q4_0":
                 w = (synth.q4_0_weights(r, k, self.seed, "cpu").numpy(),)
                 x = synth.activations_f32(self.M, k, self.seed + 1, "cpu").numpy()
+            elif fmt == "q4_k":
+                w = (synth.q4_k_weights(r, k, self.seed, "cpu").numpy(),)
+                x = synth.activations_f32(self.M, k, self.seed + 1, "cpu").numpy()
             elif fmt == "nvfp4":
                 c, sc, g = synth.nvfp4_weights(r, k, self.seed, "cpu")
                 w = (c.numpy(), sc.numpy(), g)
@@ -645,6 +686,9 @@ class OracleSampler:
                 if fmt == "q4_0":
                     t0 = time.perf_counter()
                     oracle.q4_0_q8_1(np.ascontiguousarray(w[0][off:off + r]), oracle.quantize_q8_1(x), k)
+                elif fmt == "q4_k":
+                    t0 = time.perf_counter()
+                    oracle.q4_k_q8_1(np.ascontiguousarray(w[0][off:off + r]), oracle.quantize_q8_1(x), k)
                 elif fmt == "nvfp4":
                     t0 = time.perf_counter()
                     oracle.nvfp4_w4a16(np.ascontiguousarray(w[0][off:off + r]), np.ascontiguousarray(w[1][off:off + r]),
@@ -654,7 +698,7 @@ class OracleSampler:
                     oracle.fp8_w8a16(np.ascontiguousarray(w[0][off:off + r]), np.ascontiguousarray(w[1][off:off + r]), x)
                 dt = time.perf_counter() - t0
                 # the sampled rows' weights and outputs, plus the activation once per call
-                act = self.M * (k // 32) * Q8_1_BLOCK if fmt == "q4_0" else self.M * k * 2
+                act = self.M * (k // 32) * Q8_1_BLOCK if fmt in ("q4_0", "q4_k") else self.M * k * 2
                 done_bytes += weight_bytes(fmt, r, k) + self.M * r * 4 + act
                 done_time += dt
                 t_shape += dt

@@ -1,5 +1,5 @@
 """GB300 (sm_103a) weight-only-quantized skinny matmul: Q8_1 activation quantizer,
-Q4_0 x Q8_1 MMVQ at M = 1..8, NVFP4 W4A16 and FP8 W8A16 at M = 1..16.
+Q4_0 and Q4_K x Q8_1 MMVQ at M = 1..8, NVFP4 W4A16 and FP8 W8A16 at M = 1..16.
 
 The compute lives in the C-ABI CUDA library ``_build/libqmv.so`` (declared in
 ``include/qmv.h``); this package is its thin Python binding. Seeded synthetic
@@ -9,8 +9,10 @@ from ._binding import (QmvError, QmvLibraryMissing, error_flags, get_launch_over
                        qgemm_fp8_w8a16, qgemm_fp8_w8a16_group, qgemm_nvfp4_w4a16_group, set_launch_overlap,
                        qgemm_nvfp4_w4a16, qmv_debug_q4_0_block_dots, qmv_q4_0_q8_1,
                        qmv_q4_0_q8_1_fused, qmv_q4_0_q8_1_fused_group, qmv_q4_0_q8_1_group, qmv_quantize_q8_1,
-                       route_counts, route_reset)
+                       qmv_debug_q4_k_block_dots, qmv_q4_k_q8_1, qmv_q4_k_q8_1_fused, qmv_q4_k_q8_1_fused_group,
+                       qmv_q4_k_q8_1_group, route_counts, route_reset)
 
 __all__ = ["QmvError", "QmvLibraryMissing", "error_flags", "get_launch_overlap", "set_launch_overlap", "lib", "library_path", "qgemm_fp8_w8a16", "qgemm_fp8_w8a16_group", "qgemm_nvfp4_w4a16_group",
            "qgemm_nvfp4_w4a16", "qmv_debug_q4_0_block_dots", "qmv_q4_0_q8_1", "qmv_q4_0_q8_1_fused", "qmv_q4_0_q8_1_fused_group", "qmv_q4_0_q8_1_group", "qmv_quantize_q8_1",
-           "route_counts", "route_reset"]
+           "qmv_debug_q4_k_block_dots", "qmv_q4_k_q8_1", "qmv_q4_k_q8_1_fused", "qmv_q4_k_q8_1_fused_group",
+           "qmv_q4_k_q8_1_group", "route_counts", "route_reset"]

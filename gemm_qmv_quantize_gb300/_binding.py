@@ -41,6 +41,13 @@ SIGNATURES = {
     "qgemm_fp8_w8a16_group": (_i32, [_i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), _vp, ctypes.POINTER(_vp),
                                      ctypes.POINTER(_i64), _i32, _i64, _vp]),
     "qmv_debug_q4_0_block_dots": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _vp]),
+    "qmv_q4_k_q8_1": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _vp]),
+    "qmv_q4_k_q8_1_fused": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _vp]),
+    "qmv_q4_k_q8_1_group": (_i32, [_i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                   ctypes.POINTER(_i64), _i32, _i64, _vp]),
+    "qmv_q4_k_q8_1_fused_group": (_i32, [_i32, ctypes.POINTER(_vp), ctypes.POINTER(_vp), ctypes.POINTER(_vp),
+                                         ctypes.POINTER(_i64), _i32, _i64, _vp]),
+    "qmv_debug_q4_k_block_dots": (_i32, [_vp, _vp, _vp, _i32, _i64, _i64, _vp]),
     "qmv_set_launch_overlap": (None, [_i32]),
     "qmv_get_launch_overlap": (_i32, []),
     "qmv_route_count": (_i32, []),
@@ -201,6 +208,84 @@ def qmv_debug_q4_0_block_dots(w: torch.Tensor, xq: torch.Tensor, K: int, out: to
     _need(out, "out", torch.int32, (M, N, K // 32))
     _check("qmv_debug_q4_0_block_dots",
            lib().qmv_debug_q4_0_block_dots(w.data_ptr(), xq.data_ptr(), out.data_ptr(), M, N, K, _stream(stream)))
+    return out
+
+
+# ---------------------------------------------------------------- Q4_K (144-byte super-blocks: same row bytes as Q4_0)
+
+def qmv_q4_k_q8_1(w: torch.Tensor, xq: torch.Tensor, K: int, out: torch.Tensor | None = None,
+                  stream=None) -> torch.Tensor:
+    """Q4_K uint8 [N, K/256*144] x Q8_1 uint8 [M, K/32*36] -> fp32 [M, N]."""
+    N, M = w.shape[0], xq.shape[0]
+    _need(w, "w", torch.uint8, (N, K // 256 * 144))
+    _need(xq, "xq", torch.uint8, (M, K // 32 * 36))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=w.device)
+    _need(out, "out", torch.float32, (M, N))
+    _check("qmv_q4_k_q8_1", lib().qmv_q4_k_q8_1(w.data_ptr(), xq.data_ptr(), out.data_ptr(), M, N, K,
+                                                _stream(stream)))
+    return out
+
+
+def qmv_q4_k_q8_1_fused(w: torch.Tensor, x: torch.Tensor, out: torch.Tensor | None = None,
+                        stream=None) -> torch.Tensor:
+    """Q4_K uint8 [N, K/256*144] x fp32 [M, K] (quantized to Q8_1 in-kernel) -> fp32 [M, N]."""
+    _need(x, "x", torch.float32)
+    M, K = x.shape
+    N = w.shape[0]
+    _need(w, "w", torch.uint8, (N, K // 256 * 144))
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _need(out, "out", torch.float32, (M, N))
+    _check("qmv_q4_k_q8_1_fused", lib().qmv_q4_k_q8_1_fused(w.data_ptr(), x.data_ptr(), out.data_ptr(), M, N, K,
+                                                            _stream(stream)))
+    return out
+
+
+def _q4_k_group(fn: str, ws, xs, K: int, fused: bool, outs, stream):
+    count = len(ws)
+    if count != len(xs) or not 1 <= count <= 8:
+        raise ValueError("need 1..8 matrices and as many activations")
+    M = xs[0].shape[0]
+    Ns = [w.shape[0] for w in ws]
+    for i, (w, x) in enumerate(zip(ws, xs)):
+        if fused:
+            _need(x, f"x[{i}]", torch.float32, (M, K))
+        else:
+            _need(x, f"xq[{i}]", torch.uint8, (M, K // 32 * 36))
+        _need(w, f"w[{i}]", torch.uint8, (Ns[i], K // 256 * 144))
+    if outs is None:
+        outs = [torch.empty((M, n), dtype=torch.float32, device=xs[0].device) for n in Ns]
+    for i, o in enumerate(outs):
+        _need(o, f"out[{i}]", torch.float32, (M, Ns[i]))
+    arr = ctypes.c_void_p * count
+    wp, xp, yp = arr(*[w.data_ptr() for w in ws]), arr(*[x.data_ptr() for x in xs]), arr(*[o.data_ptr() for o in outs])
+    npa = (ctypes.c_int64 * count)(*Ns)
+    _check(fn, getattr(lib(), fn)(count, wp, xp, yp, npa, M, K, _stream(stream)))
+    return outs
+
+
+def qmv_q4_k_q8_1_group(ws, xqs, K: int, outs=None, stream=None):
+    """Several independent Q4_K calls on Q8_1 activations (same M, K) in one launch."""
+    return _q4_k_group("qmv_q4_k_q8_1_group", ws, xqs, K, False, outs, stream)
+
+
+def qmv_q4_k_q8_1_fused_group(ws, xs, outs=None, stream=None):
+    """Several independent fused Q4_K calls (same M, K) in one launch."""
+    return _q4_k_group("qmv_q4_k_q8_1_fused_group", ws, xs, xs[0].shape[1], True, outs, stream)
+
+
+def qmv_debug_q4_k_block_dots(w: torch.Tensor, xq: torch.Tensor, K: int, out: torch.Tensor | None = None,
+                              stream=None) -> torch.Tensor:
+    """int32 [M, N, K/32]: raw S = sum q * q8 per sub-block, from the product kernel's device code."""
+    N, M = w.shape[0], xq.shape[0]
+    _need(w, "w", torch.uint8, (N, K // 256 * 144))
+    _need(xq, "xq", torch.uint8, (M, K // 32 * 36))
+    if out is None:
+        out = torch.empty((M, N, K // 32), dtype=torch.int32, device=w.device)
+    _need(out, "out", torch.int32, (M, N, K // 32))
+    _check("qmv_debug_q4_k_block_dots",
+           lib().qmv_debug_q4_k_block_dots(w.data_ptr(), xq.data_ptr(), out.data_ptr(), M, N, K, _stream(stream)))
     return out
 
 

@@ -17,6 +17,7 @@ constexpr const char *kRouteNames[kRouteCount] = {
     "quantize_q8_1", "q4_0_stream_dp4a", "q4_0_generic", "q4_0_stream_fused_quantize", "nvfp4_mma_m16n8k16",
     "nvfp4_generic",
     "fp8_mma_m16n8k16", "fp8_generic", "zero_fill", "q4_0_mma_m16n8k32", "q4_0_mma_fused_quantize",
+    "q4_k_stream_dp4a", "q4_k_stream_fused_quantize",
 };
 
 constexpr int kMaxDevices = 64;
@@ -205,7 +206,8 @@ qmv_status qmv_debug_q4_0_block_dots(const void *w, const void *xq, int32_t *dot
 // Grouped launch of `count` matrices with the same M and K: fused, x[i] are fp32
 // [M][K] (16-byte aligned); else Q8_1 [M][K/32] (4-byte aligned).
 static qmv_status q4_0_group(int count, const void *const *w, const void *const *x, float *const *y,
-                             const int64_t *N, int M, int64_t K, bool fused, qmv_stream_t stream)
+                             const int64_t *N, int M, int64_t K, bool fused, qmv_stream_t stream, bool q4k = false,
+                             int32_t *dots = nullptr)
 {
     if (count < 1 || count > kMaxGroup) return QMV_ERR_SHAPE;
     if (!w || !x || !y || !N) return QMV_ERR_NULL;
@@ -220,10 +222,11 @@ static qmv_status q4_0_group(int count, const void *const *w, const void *const 
     if (grp.row_start[count] > kMaxDim) return QMV_ERR_SHAPE;
     if (M == 0 || grp.row_start[count] == 0) return QMV_OK;
     for (int i = 0; i < count; ++i) {
-        if (N[i] > 0 && !y[i]) return QMV_ERR_NULL;
-        if (misaligned(y[i], 4)) return QMV_ERR_ALIGN;
+        if (N[i] > 0 && !y[i] && !dots) return QMV_ERR_NULL;
+        if (misaligned(y[i], 4) || misaligned(dots, 4)) return QMV_ERR_ALIGN;
     }
     if (K == 0) {
+        if (dots) return QMV_OK;
         for (int i = 0; i < count; ++i) {
             if (N[i] == 0) continue;
             qmv_status st = zero_fill(y[i], M, N[i], stream);
@@ -246,10 +249,10 @@ static qmv_status q4_0_group(int count, const void *const *w, const void *const 
     cudaError_t e = current_device_info(&dev);
     if (e != cudaSuccess) return QMV_ERR_CUDA;
     Q4Plan plan;
-    if ((e = plan_q4_0(dev, grp, M, K, &plan)) != cudaSuccess) return QMV_ERR_CUDA;
+    if ((e = plan_q4_0(dev, grp, M, K, &plan, q4k)) != cudaSuccess) return QMV_ERR_CUDA;
     if (plan.route != kRouteQ4_0Stream && plan.route != kRouteQ4_0Mma)
         return QMV_ERR_SHAPE;   // the activations do not fit in shared memory
-    return from_cuda(launch_q4_0(plan, grp, nullptr, M, K, fused, stream));
+    return from_cuda(launch_q4_0(plan, grp, dots, M, K, fused, stream, q4k));
 }
 
 qmv_status qmv_q4_0_q8_1_fused_group(int count, const void *const *w, const float *const *x, float *const *y,
@@ -268,6 +271,40 @@ qmv_status qmv_q4_0_q8_1_fused(const void *w, const float *x, float *y, int M, i
                                qmv_stream_t stream)
 {
     return qmv_q4_0_q8_1_fused_group(1, &w, &x, &y, &N, M, K, stream);
+}
+
+// ---- Q4_K: the grouped streaming path for every call (K % 256, 16-byte aligned rows)
+
+qmv_status qmv_q4_k_q8_1(const void *w, const void *xq, float *y, int M, int64_t N, int64_t K, qmv_stream_t stream)
+{
+    return q4_0_group(1, &w, &xq, &y, &N, M, K, false, stream, true);
+}
+
+qmv_status qmv_q4_k_q8_1_group(int count, const void *const *w, const void *const *xq, float *const *y,
+                               const int64_t *N, int M, int64_t K, qmv_stream_t stream)
+{
+    return q4_0_group(count, w, xq, y, N, M, K, false, stream, true);
+}
+
+qmv_status qmv_q4_k_q8_1_fused(const void *w, const float *x, float *y, int M, int64_t N, int64_t K,
+                               qmv_stream_t stream)
+{
+    const void *xv = x;
+    return q4_0_group(1, &w, &xv, &y, &N, M, K, true, stream, true);
+}
+
+qmv_status qmv_q4_k_q8_1_fused_group(int count, const void *const *w, const float *const *x, float *const *y,
+                                     const int64_t *N, int M, int64_t K, qmv_stream_t stream)
+{
+    return q4_0_group(count, w, reinterpret_cast<const void *const *>(x), y, N, M, K, true, stream, true);
+}
+
+qmv_status qmv_debug_q4_k_block_dots(const void *w, const void *xq, int32_t *dots, int M, int64_t N, int64_t K,
+                                     qmv_stream_t stream)
+{
+    if (!dots && M > 0 && N > 0 && K > 0) return QMV_ERR_NULL;
+    float *no_y = nullptr;
+    return q4_0_group(1, &w, &xq, &no_y, &N, M, K, false, stream, true, dots);
 }
 
 qmv_status qgemm_nvfp4_w4a16(const uint8_t *codes, const uint8_t *scales_e4m3, float global_scale,

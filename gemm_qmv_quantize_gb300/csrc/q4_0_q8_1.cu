@@ -146,6 +146,87 @@ __device__ __forceinline__ void q4_unit(const uint8_t *wu, const uint8_t *act, u
     }
 }
 
+// Dot of one Q4_K super-block (llama.cpp's K-quant layout, 144 bytes = 256
+// weights, the same size as a Q4_0 unit) against M staged activation rows:
+//   bytes 0..3 fp16 d and dmin; 4..15 eight packed 6-bit sub-block scales sc_j and
+//   minimums mn_j; 16..143 nibbles, data byte 32c + e holding element e of
+//   sub-block 2c (low nibble) and of sub-block 2c + 1 (high nibble).
+//   sum_j d8_j (d sc_j S_j - dmin mn_j T_j),  S_j = sum q * q8, T_j = sum q8,
+// with S_j, T_j exact integers and d sc_j, dmin mn_j exact in fp32.
+// dots: the raw S_j (kDots only).
+template <int M, bool kDots>
+__device__ __forceinline__ void q4k_unit(const uint8_t *wu, const uint8_t *act, uint32_t act_stride, float (&acc)[M],
+                                         int32_t *dots, int64_t dots_m_stride)
+{
+    const uint4 *wp = reinterpret_cast<const uint4 *>(wu);
+    uint32_t w[36];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+        const uint4 v = wp[i];
+        w[4 * i] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+    }
+    const float d = f16_bits_to_float(w[0] & 0xffffu), dmin = f16_bits_to_float(w[0] >> 16);
+    // scale bytes p0..p3 = w[1], p4..p7 = w[2], p8..p11 = w[3]: sub-blocks 0..3 keep
+    // their 6 bits in p0..3 (scales) and p4..7 (minimums); 4..7 their low 4 bits in
+    // p8..11 (scale low, minimum high nibble) and their top 2 bits on top of p0..7.
+    const uint32_t sc_lo = w[1] & 0x3f3f3f3fu, mn_lo = w[2] & 0x3f3f3f3fu;
+    const uint32_t sc_hi = (w[3] & 0x0f0f0f0fu) | ((w[1] >> 2) & 0x30303030u);
+    const uint32_t mn_hi = ((w[3] >> 4) & 0x0f0f0f0fu) | ((w[2] >> 2) & 0x30303030u);
+    float dsc[8], dmn[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        dsc[j] = d * static_cast<float>((sc_lo >> (8 * j)) & 0xffu);
+        dsc[j + 4] = d * static_cast<float>((sc_hi >> (8 * j)) & 0xffu);
+        dmn[j] = dmin * static_cast<float>((mn_lo >> (8 * j)) & 0xffu);
+        dmn[j + 4] = dmin * static_cast<float>((mn_hi >> (8 * j)) & 0xffu);
+    }
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        const uint8_t *am = act + m * act_stride;
+        const uint4 *a = reinterpret_cast<const uint4 *>(am);
+        const float4 d8a = *reinterpret_cast<const float4 *>(am + kActD8Off);
+        const float4 d8b = *reinterpret_cast<const float4 *>(am + kActD8Off + 16);
+        const int4 t8a = *reinterpret_cast<const int4 *>(am + kActT8Off);
+        const int4 t8b = *reinterpret_cast<const int4 *>(am + kActT8Off + 16);
+        const float d8[8] = {d8a.x, d8a.y, d8a.z, d8a.w, d8b.x, d8b.y, d8b.z, d8b.w};
+        const int t8[8] = {t8a.x, t8a.y, t8a.z, t8a.w, t8b.x, t8b.y, t8b.z, t8b.w};
+        int sd[8];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            // sub-blocks 2c (low nibbles) and 2c + 1 (high nibbles, summed 16x under a
+            // 0xF0 mask) of data words 8c .. 8c + 7, against activation blocks 2c, 2c + 1
+            const uint4 x0 = a[4 * c], x1 = a[4 * c + 1], x2 = a[4 * c + 2], x3 = a[4 * c + 3];
+            const uint32_t lo_x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            const uint32_t hi_x[8] = {x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+            int lo = 0, hi = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint32_t q = w[4 + 8 * c + i];
+                lo = dp4a_us(q & 0x0f0f0f0fu, lo_x[i], lo);
+                hi = dp4a_us(q & 0xf0f0f0f0u, hi_x[i], hi);
+            }
+            sd[2 * c] = lo;
+            sd[2 * c + 1] = hi >> 4;
+        }
+        if (kDots) {
+            int32_t *dm = dots + m * dots_m_stride;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dm[j] = sd[j];
+        } else {
+            float part = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                part = fmaf(dsc[j] * d8[j], static_cast<float>(sd[j]), part);
+                part = fmaf(-(dmn[j] * d8[j]), 0.125f * static_cast<float>(t8[j]), part);   // 8T / 8, exact
+            }
+            acc[m] += part;
+        }
+    }
+}
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
@@ -248,8 +329,9 @@ __device__ __forceinline__ void stage_q8_1(const Q4Group &grp, int nb, uint8_t *
 
 // kFused: the group's activations are fp32 [M][K], quantized to Q8_1 in the
 // prologue; else they are Q8_1 [M][K/32]. kDots: write the integer block dots of
-// matrix 0 instead of y (a single-matrix group).
-template <int M, bool kDots, bool kFused>
+// matrix 0 instead of y (a single-matrix group). kQ4K: the weights are Q4_K
+// super-blocks (a row is K/256 of 144 bytes, the same units as Q4_0).
+template <int M, bool kDots, bool kFused, bool kQ4K>
 __global__ void __launch_bounds__(M == 1 ? kStreamThreads : kStreamThreadsWide) q4_0_stream_kernel(
     const __grid_constant__ Q4Group grp, int32_t *__restrict__ dots, int64_t K, int S, int P)
 {
@@ -334,8 +416,12 @@ __global__ void __launch_bounds__(M == 1 ? kStreamThreads : kStreamThreadsWide) 
 #pragma unroll
         for (int m = 0; m < M; ++m) v[m] = 0.0f;
         if (live) {
-            q4_unit<M, kDots>(ring + slot * L.slotbytes + lane * kUnitBytes, act0 + uin * kActUnitStride,
-                              L.act_m_stride, v, kDots ? dots + (r0 + rr) * nb + 8 * uin : nullptr, Nm * nb);
+            const uint8_t *wu = ring + slot * L.slotbytes + lane * kUnitBytes;
+            int32_t *du = kDots ? dots + (r0 + rr) * nb + 8 * uin : nullptr;
+            if (kQ4K)
+                q4k_unit<M, kDots>(wu, act0 + uin * kActUnitStride, L.act_m_stride, v, du, Nm * nb);
+            else
+                q4_unit<M, kDots>(wu, act0 + uin * kActUnitStride, L.act_m_stride, v, du, Nm * nb);
         }
         __syncwarp();   // every lane is done with the slot
         if (lane == 0 && c + S < nchunks) issue(c + S, slot);
@@ -441,7 +527,7 @@ __global__ void __launch_bounds__(kThreads) q4_0_generic_kernel(const uint8_t *_
 
 // ---------------------------------------------------------------- host side
 
-template <int M, bool kDots, bool kFused>
+template <int M, bool kDots, bool kFused, bool kQ4K>
 cudaError_t launch_m(const Q4Plan &p, const Q4Group &grp, int32_t *dots, int64_t K, cudaStream_t s)
 {
     cudaLaunchAttribute attr[1];
@@ -451,14 +537,14 @@ cudaError_t launch_m(const Q4Plan &p, const Q4Group &grp, int32_t *dots, int64_t
     cfg.attrs = attr;
     cfg.numAttrs = set_launch_overlap_attr(attr);
     if (p.route == kRouteQ4_0Stream) {
-        auto kern = q4_0_stream_kernel<M, kDots, kFused>;
+        auto kern = q4_0_stream_kernel<M, kDots, kFused, kQ4K>;
         cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), p.smem_bytes);
         if (e != cudaSuccess) return e;
         cfg.blockDim = dim3(static_cast<unsigned>(p.warps * 32));   // consumers + the producer
         cfg.dynamicSmemBytes = static_cast<size_t>(p.smem_bytes);
         return cudaLaunchKernelEx(&cfg, kern, grp, dots, K, p.stages, p.prefetch);
     }
-    if (kFused || grp.count != 1) return cudaErrorInvalidValue;   // these need the streaming kernel
+    if (kQ4K || kFused || grp.count != 1) return cudaErrorInvalidValue;   // these need the streaming kernel
     cfg.blockDim = dim3(kThreads);
     auto gk = q4_0_generic_kernel<M, kDots>;
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(gk), 0);
@@ -467,25 +553,25 @@ cudaError_t launch_m(const Q4Plan &p, const Q4Group &grp, int32_t *dots, int64_t
                               grp.row_start[1], K);
 }
 
-template <bool kDots, bool kFused>
+template <bool kDots, bool kFused, bool kQ4K>
 cudaError_t launch_dispatch(const Q4Plan &p, const Q4Group &grp, int32_t *dots, int M, int64_t K, cudaStream_t s)
 {
     switch (M) {
-    case 1: return launch_m<1, kDots, kFused>(p, grp, dots, K, s);
-    case 2: return launch_m<2, kDots, kFused>(p, grp, dots, K, s);
-    case 3: return launch_m<3, kDots, kFused>(p, grp, dots, K, s);
-    case 4: return launch_m<4, kDots, kFused>(p, grp, dots, K, s);
-    case 5: return launch_m<5, kDots, kFused>(p, grp, dots, K, s);
-    case 6: return launch_m<6, kDots, kFused>(p, grp, dots, K, s);
-    case 7: return launch_m<7, kDots, kFused>(p, grp, dots, K, s);
-    case 8: return launch_m<8, kDots, kFused>(p, grp, dots, K, s);
+    case 1: return launch_m<1, kDots, kFused, kQ4K>(p, grp, dots, K, s);
+    case 2: return launch_m<2, kDots, kFused, kQ4K>(p, grp, dots, K, s);
+    case 3: return launch_m<3, kDots, kFused, kQ4K>(p, grp, dots, K, s);
+    case 4: return launch_m<4, kDots, kFused, kQ4K>(p, grp, dots, K, s);
+    case 5: return launch_m<5, kDots, kFused, kQ4K>(p, grp, dots, K, s);
+    case 6: return launch_m<6, kDots, kFused, kQ4K>(p, grp, dots, K, s);
+    case 7: return launch_m<7, kDots, kFused, kQ4K>(p, grp, dots, K, s);
+    case 8: return launch_m<8, kDots, kFused, kQ4K>(p, grp, dots, K, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t K, Q4Plan *plan)
+cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t K, Q4Plan *plan, bool q4k)
 {
     bool aligned = true;
     for (int i = 0; i < grp.count; ++i) aligned = aligned && (reinterpret_cast<uintptr_t>(grp.w[i]) & 15u) == 0;
@@ -498,8 +584,8 @@ cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t 
     plan->smem_bytes = 0;
     plan->grid = static_cast<int>((N + kWarps - 1) / kWarps);
     if (!aligned || K % 256 != 0) return cudaSuccess;
-    // from a few activation rows on, the tensor cores
-    if (M >= env_int("QMV_Q4_MMA_MIN_M", 5)) {
+    // from a few activation rows on, the tensor cores (Q4_0 only)
+    if (!q4k && M >= env_int("QMV_Q4_MMA_MIN_M", 5)) {
         cudaError_t e = plan_q4_0_mma(dev, grp, M, K, plan);
         if (e != cudaSuccess || plan->route == kRouteQ4_0Mma) return e;
     }
@@ -547,16 +633,23 @@ void assign_ctas(Q4Group &grp, int total)
 }
 
 cudaError_t launch_q4_0(const Q4Plan &plan, const Q4Group &grp_in, int32_t *dots, int M, int64_t K, bool fused,
-                        cudaStream_t s)
+                        cudaStream_t s, bool q4k)
 {
     if (plan.route == kRouteQ4_0Mma) return launch_q4_0_mma(plan, grp_in, dots, M, K, fused, s);
     if (fused && plan.route != kRouteQ4_0Stream) return cudaErrorInvalidValue;
     Q4Group grp = grp_in;
     if (plan.route == kRouteQ4_0Stream) assign_ctas(grp, plan.grid * plan.warps);   // per warp
+    if (q4k) {
+        if (plan.route != kRouteQ4_0Stream) return cudaErrorInvalidValue;   // Q4_K: the streaming kernel only
+        route_hit(fused ? kRouteQ4KStreamFused : kRouteQ4KStream);
+        if (dots) return launch_dispatch<true, false, true>(plan, grp, dots, M, K, s);
+        if (fused) return launch_dispatch<false, true, true>(plan, grp, dots, M, K, s);
+        return launch_dispatch<false, false, true>(plan, grp, dots, M, K, s);
+    }
     route_hit(fused ? kRouteQ4_0StreamFused : plan.route);
-    if (dots) return launch_dispatch<true, false>(plan, grp, dots, M, K, s);
-    if (fused) return launch_dispatch<false, true>(plan, grp, dots, M, K, s);
-    return launch_dispatch<false, false>(plan, grp, dots, M, K, s);
+    if (dots) return launch_dispatch<true, false, false>(plan, grp, dots, M, K, s);
+    if (fused) return launch_dispatch<false, true, false>(plan, grp, dots, M, K, s);
+    return launch_dispatch<false, false, false>(plan, grp, dots, M, K, s);
 }
 
 cudaError_t read_error_word_q4_0(uint32_t *out, bool clear)

@@ -21,6 +21,8 @@ enum Route : int {
     kRouteZeroFill,       // K == 0: y = 0
     kRouteQ4_0Mma,        // Q4_0: tensor cores (m16n8k32 int8), larger M
     kRouteQ4_0MmaFused,   // ... with the Q8_1 quantize in the prologue
+    kRouteQ4KStream,      // Q4_K: the Q4_0 streaming kernel's machinery, K-quant super-blocks
+    kRouteQ4KStreamFused, // ... with the Q8_1 quantize in the prologue
     kRouteCount
 };
 
@@ -74,14 +76,16 @@ struct Q4Group {
     int cta_start[kMaxGroup + 1];   // streaming kernel: warps of matrix i are [cta_start[i], cta_start[i+1])
 };
 
-cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t K, Q4Plan *plan);
+// q4k: the weights are Q4_K super-blocks (streaming kernel only; route
+// kRouteQ4_0Stream when it applies, else kRouteQ4_0Generic = not supported).
+cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t K, Q4Plan *plan, bool q4k = false);
 // The tensor-core kernel's plan (route kRouteQ4_0Mma), or route kRouteQ4_0Generic
 // when it does not apply.
 cudaError_t plan_q4_0_mma(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t K, Q4Plan *plan);
 cudaError_t launch_q4_0_mma(const Q4Plan &plan, const Q4Group &grp, int32_t *dots, int M, int64_t K, bool fused,
                             cudaStream_t s);
 cudaError_t launch_q4_0(const Q4Plan &plan, const Q4Group &grp, int32_t *dots, int M, int64_t K, bool fused,
-                        cudaStream_t s);
+                        cudaStream_t s, bool q4k = false);
 
 // NVFP4 / FP8: a group of matrices with the same K reading the same activations
 // (count 1 for a single call). codes: NVFP4 [N][K/2] or FP8 [N][K]; scales: NVFP4

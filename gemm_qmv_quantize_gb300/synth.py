@@ -51,6 +51,23 @@ def q4_0_weights(N: int, K: int, seed: int, device="cpu") -> torch.Tensor:
     return out.view(N, nb * Q4_0_BLOCK_BYTES)
 
 
+def q4_k_weights(N: int, K: int, seed: int, device="cpu") -> torch.Tensor:
+    """Q4_K matrix as uint8 [N, K/256*144]: per 256-weight super-block fp16 d and
+    dmin = |N(0,1)| * 0.001 and * 0.002, then 12 uniformly random bytes (the packed
+    6-bit sub-block scales and minimums: every byte pattern is valid) and 128
+    uniformly random bytes of nibbles."""
+    assert K % 256 == 0
+    ns = K // 256
+    g = _gen(seed, device)
+    body = torch.randint(0, 256, (N, ns, 140), generator=g, dtype=torch.uint8, device=device)
+    d = (torch.randn((N, ns, 2), generator=g, device=device).abs_() *
+         torch.tensor([0.001, 0.002], device=device)).to(torch.float16)
+    out = torch.empty((N, ns, 144), dtype=torch.uint8, device=device)
+    out[:, :, 0:4] = d.view(torch.uint8).view(N, ns, 4)
+    out[:, :, 4:] = body
+    return out.view(N, ns * 144)
+
+
 def nvfp4_weights(N: int, K: int, seed: int, device="cpu"):
     """(codes uint8 [N, K/2], scales uint8 [N, K/16] E4M3, global scale float)."""
     assert K % 16 == 0

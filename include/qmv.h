@@ -133,6 +133,42 @@ QMV_API qmv_status qmv_q4_0_q8_1_group(int count, const void *const *w, const vo
                                        const int64_t *N, int M, int64_t K, qmv_stream_t stream);
 
 /*
+ * Q4_K x Q8_1 mat-vec, M = 1..8 activation rows: llama.cpp's K-quant super-block,
+ * the format of the Q4_K_M models of "Machine Learning on NVIDIA CMP", section
+ * "llama.cpp results" (the pages name it without printing the layout).
+ *   w   Q4_K [N][K/256] super-blocks of 144 bytes, 16-byte aligned:
+ *       bytes 0..1 d (fp16), 2..3 dmin (fp16), 4..15 eight packed 6-bit
+ *       sub-block scales sc_j and minimums mn_j (j < 4: sc = p[j] & 63,
+ *       mn = p[j+4] & 63; j >= 4: sc = (p[j+4] & 15) | (p[j-4] >> 6) << 4,
+ *       mn = (p[j+4] >> 4) | (p[j] >> 6) << 4), 16..143 nibbles: data byte
+ *       32c + e holds element 64c + e (low nibble) and 64c + 32 + e (high).
+ *       Element i of sub-block j = i / 32: w = d * sc_j * q - dmin * mn_j.
+ *   xq  Q8_1 [M][K/32] as written by qmv_quantize_q8_1, 4-byte aligned.
+ *   y   fp32 [M][N]: y[m][n] = sum_b d8[m][b] * (d sc_j S - dmin mn_j T) over
+ *       the Q8_1 blocks b (= sub-blocks), with the exact integer sums
+ *       S = sum q * q8 and T = sum q8, accumulated in fp32.
+ *   K a multiple of 256. One streaming kernel (dp4a) serves every M; it stages
+ *   the activations in shared memory, so very large K returns QMV_ERR_SHAPE.
+ */
+QMV_API qmv_status qmv_q4_k_q8_1(const void *w, const void *xq, float *y, int M, int64_t N, int64_t K,
+                                 qmv_stream_t stream);
+
+/* Quantize + Q4_K MMVQ in one kernel, as qmv_q4_0_q8_1_fused is for Q4_0:
+ * bit-identical to qmv_quantize_q8_1 followed by qmv_q4_k_q8_1. x fp32 [M][K],
+ * 16-byte aligned; other arguments and errors as in qmv_q4_k_q8_1. */
+QMV_API qmv_status qmv_q4_k_q8_1_fused(const void *w, const float *x, float *y, int M, int64_t N, int64_t K,
+                                       qmv_stream_t stream);
+
+/* Grouped Q4_K launches (1..8 matrices, HOST arrays of device pointers and row
+ * counts), each call i exactly as the single call on (w[i], x[i] or xq[i], y[i],
+ * N[i]); matrices given the same activation pointer stage it once. */
+QMV_API qmv_status qmv_q4_k_q8_1_group(int count, const void *const *w, const void *const *xq, float *const *y,
+                                       const int64_t *N, int M, int64_t K, qmv_stream_t stream);
+QMV_API qmv_status qmv_q4_k_q8_1_fused_group(int count, const void *const *w, const float *const *x,
+                                             float *const *y, const int64_t *N, int M, int64_t K,
+                                             qmv_stream_t stream);
+
+/*
  * NVFP4 W4A16 skinny GEMM ("v100-skinny README", section "How QPN works": QPN2).
  *   codes        [N][K/2] bytes, two E2M1 codes per byte: k even in the low
  *                nibble, k odd in the high nibble (OCP MX E2M1 values).
@@ -213,6 +249,15 @@ QMV_API int qmv_get_launch_overlap(void);
  */
 QMV_API qmv_status qmv_debug_q4_0_block_dots(const void *w, const void *xq, int32_t *dots, int M, int64_t N,
                                      int64_t K, qmv_stream_t stream);
+
+/*
+ * Raw integer sub-block dots of qmv_q4_k_q8_1 from the same device code and
+ * kernel: dots int32 [M][N][K/32], dots[m][n][b] = S = sum q * q8 over the 32
+ * weights of sub-block b (no minimum term). Pointers and alignment as in
+ * qmv_q4_k_q8_1.
+ */
+QMV_API qmv_status qmv_debug_q4_k_block_dots(const void *w, const void *xq, int32_t *dots, int M, int64_t N,
+                                             int64_t K, qmv_stream_t stream);
 
 /*
  * Kernel-choice census: a counter per kernel route, bumped on every launch, so a

@@ -91,6 +91,35 @@ def test_q4_0_validation(lib, args, status):
     assert lib.qmv_q4_0_q8_1(*args) == status
 
 
+@pytest.mark.parametrize("fn", ["qmv_q4_k_q8_1", "qmv_q4_k_q8_1_fused", "qmv_debug_q4_k_block_dots"])
+@pytest.mark.parametrize("args,status", [
+    ((0, P, P, 1, 64, 4096, None), NULL),
+    ((P, 0, P, 1, 64, 4096, None), NULL),
+    ((P, P, P, 9, 64, 4096, None), SHAPE),
+    ((P, P, P, 1, -5, 4096, None), SHAPE),
+    ((P, P, P, 1, 64, 4128, None), SHAPE),     # K % 256
+    ((P + 8, P, P, 1, 64, 4096, None), ALIGN),  # super-block rows need 16-byte alignment
+    ((P, P, P + 2, 1, 64, 4096, None), ALIGN),
+    ((0, 0, 0, 1, 0, 4096, None), OK),          # N == 0
+    ((0, 0, 0, 0, 64, 4096, None), OK),         # M == 0
+])
+def test_q4_k_validation(lib, fn, args, status):
+    assert getattr(lib, fn)(*args) == status
+
+
+def test_q4_k_validation_null_output_and_x_alignment(lib):
+    assert lib.qmv_q4_k_q8_1(P, P, 0, 1, 64, 4096, None) == NULL
+    assert lib.qmv_debug_q4_k_block_dots(P, P, 0, 1, 64, 4096, None) == NULL
+    assert lib.qmv_q4_k_q8_1(P, P + 2, P, 1, 64, 4096, None) == ALIGN        # Q8_1 needs 4 bytes
+    assert lib.qmv_q4_k_q8_1_fused(P, P + 4, P, 1, 64, 4096, None) == ALIGN  # fp32 x needs 16 bytes
+    arr = ctypes.c_void_p * 2
+    n = (ctypes.c_int64 * 2)(64, 64)
+    z = arr(P, P)
+    assert lib.qmv_q4_k_q8_1_group(9, z, z, z, n, 1, 4096, None) == SHAPE
+    assert lib.qmv_q4_k_q8_1_group(2, z, z, z, n, 1, 4128, None) == SHAPE
+    assert lib.qmv_q4_k_q8_1_fused_group(2, arr(P, P + 8), z, z, n, 1, 4096, None) == ALIGN
+
+
 @pytest.mark.parametrize("args,status", [
     ((0, P, 0.01, P, P, 1, 64, 512, None), NULL),
     ((P, 0, 0.01, P, P, 1, 64, 512, None), NULL),
