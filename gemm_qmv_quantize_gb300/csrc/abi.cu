@@ -26,7 +26,7 @@ DeviceInfo g_dev[kMaxDevices];
 bool g_dev_valid[kMaxDevices];
 
 constexpr int64_t kMaxDim = 0x7fffffffLL;
-constexpr int kMaxRowsW = 16;   // activation rows of the NVFP4 / FP8 entry points
+constexpr int kMaxRowsW = 96;   // activation rows of the NVFP4 / FP8 entry points (chunks of <= 16 above 16)
 
 bool misaligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
 

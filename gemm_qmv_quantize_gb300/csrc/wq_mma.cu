@@ -468,8 +468,8 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const 
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = set_launch_overlap_attr(attr);
-    route_hit(r);
     if (r == kRouteNvfp4Mma || r == kRouteFp8Mma) {
+        route_hit(r);
         // up to 8 activation rows per row tile; 9..16 rows take two tiles per weight pass
         using Kern = void (*)(WqParams, const uint16_t *, int, int64_t, int, int, int);
         const int mt = M > 8 ? 2 : 1;
@@ -615,6 +615,7 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const 
     if (e != cudaSuccess) return e;
     // 8 activation rows per launch
     for (int m0 = 0; m0 < M; m0 += 8) {
+        route_hit(r);
         e = cudaLaunchKernelEx(&cfg, kern, grp.codes[0], grp.scales[0], grp.row_scale[0], grp.g[0], x + m0 * K,
                                grp.y[0] + m0 * N, std::min(8, M - m0), N, K);
         if (e != cudaSuccess) return e;
@@ -645,16 +646,44 @@ Route plan_fp8(const uint8_t *w, const uint16_t *x, int64_t K)
     return (K % 128 == 0 && aligned16(w) && aligned16(x)) ? kRouteFp8Mma : kRouteFp8Generic;
 }
 
+namespace {
+
+// More than 16 activation rows (up to 96: the chunked packed-FP8 band of the
+// README's region-dispatch table, "Native mixed-precision checkpoint path"): M
+// is cut into ceil(M / 16) balanced chunks of at most 16 rows, each one launch of
+// the tensor-core kernel (one or two 8-row tiles per weight pass). Chunk c + 1
+// reads the same weights right after chunk c, from L2 when the group's weights fit
+// there. The generic kernel takes any M in 8-row launches already.
+template <bool kFp4>
+cudaError_t launch_wq_chunked(Route r, const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M,
+                              int64_t K, cudaStream_t s)
+{
+    if (M <= 16 || (r != kRouteNvfp4Mma && r != kRouteFp8Mma)) return launch_wq<kFp4>(r, dev, grp, x, M, K, s);
+    const int nch = (M + 15) / 16;
+    int m0 = 0;
+    for (int c = 0; c < nch; ++c) {
+        const int mc = (M - m0 + (nch - c) - 1) / (nch - c);   // ceil(rows left / chunks left) <= 16
+        WqGroup g = grp;
+        for (int i = 0; i < grp.count; ++i) g.y[i] = grp.y[i] + static_cast<int64_t>(m0) * grp.N[i];
+        const cudaError_t e = launch_wq<kFp4>(r, dev, g, x + static_cast<int64_t>(m0) * K, mc, K, s);
+        if (e != cudaSuccess) return e;
+        m0 += mc;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t launch_nvfp4(Route r, const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M, int64_t K,
                          cudaStream_t s)
 {
-    return launch_wq<true>(r, dev, grp, x, M, K, s);
+    return launch_wq_chunked<true>(r, dev, grp, x, M, K, s);
 }
 
 cudaError_t launch_fp8(Route r, const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M, int64_t K,
                        cudaStream_t s)
 {
-    return launch_wq<false>(r, dev, grp, x, M, K, s);
+    return launch_wq_chunked<false>(r, dev, grp, x, M, K, s);
 }
 
 }  // namespace qmv

@@ -17,7 +17,7 @@
  *    current CUDA device, owned by the caller. The library allocates no memory
  *    and keeps no per-call state; it never frees or retains a pointer.
  *  - All arrays are row-major and little-endian. M is the number of activation
- *    rows (1..8 for the Q4_0 / Q8_1 calls, 1..16 for NVFP4 / FP8), N the number of
+ *    rows (1..8 for the Q4_0 / Q4_K / Q8_1 calls, 1..96 for NVFP4 / FP8), N the number of
  *    weight rows (outputs per activation row), K the reduction length. Outputs y are fp32 [M][N] and fully overwritten.
  *  - Every call is asynchronous on `stream` (NULL = the legacy default stream)
  *    and may be captured in a CUDA graph. Arguments are validated on the host
@@ -49,7 +49,7 @@ typedef struct CUstream_st *qmv_stream_t;
 typedef int qmv_status;
 #define QMV_OK                0
 #define QMV_ERR_NULL         -1  /* a required pointer is NULL */
-#define QMV_ERR_SHAPE        -2  /* M outside 0..8 (0..16 NVFP4 / FP8), N or K negative, K not a multiple of the format's block */
+#define QMV_ERR_SHAPE        -2  /* M outside 0..8 (0..96 NVFP4 / FP8), N or K negative, K not a multiple of the format's block */
 #define QMV_ERR_ALIGN        -3  /* a pointer is not aligned to its element type (see each call) */
 #define QMV_ERR_CUDA         -4  /* a CUDA runtime call failed (launch, attribute, device query) */
 #define QMV_ERR_TIMEOUT      -5  /* qmv_error_flags: a bounded device-side wait gave up */
@@ -182,7 +182,10 @@ QMV_API qmv_status qmv_q4_k_q8_1_fused_group(int count, const void *const *w, co
  *   select the tensor-core streaming kernel.
  *   M = 1..16: rows 9..16 ride the same pass over the weights as rows 1..8 (a
  *   second 8-row activation tile of the tensor-core product), so the weights are
- *   read from memory once for all M rows.
+ *   read from memory once for all M rows. M = 17..96 (the chunked band of the
+ *   README's "Native mixed-precision checkpoint path" dispatch table): balanced
+ *   chunks of at most 16 rows, one launch and one weight pass each (passes after
+ *   the first hit L2 when the weights fit there).
  */
 QMV_API qmv_status qgemm_nvfp4_w4a16(const uint8_t *codes, const uint8_t *scales_e4m3, float global_scale,
                              const uint16_t *x, float *y, int M, int64_t N, int64_t K,
@@ -197,7 +200,8 @@ QMV_API qmv_status qgemm_nvfp4_w4a16(const uint8_t *codes, const uint8_t *scales
  *   y          fp32 [M][N]: y[m][n] = row_scale[n] * sum_k e4m3(w[n][k]) * x[m][k],
  *              accumulated in fp32.
  *   Any K >= 0. w, x 16-byte aligned and K a multiple of 128 select the
- *   tensor-core streaming kernel. M = 1..16, one pass over the weights as for NVFP4.
+ *   tensor-core streaming kernel. M = 1..16 in one pass over the weights, 17..96 in
+ *   chunks of at most 16 rows, as for NVFP4.
  */
 QMV_API qmv_status qgemm_fp8_w8a16(const uint8_t *w, const float *row_scale, const uint16_t *x, float *y,
                            int M, int64_t N, int64_t K, qmv_stream_t stream);

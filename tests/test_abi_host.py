@@ -126,7 +126,7 @@ def test_q4_k_validation_null_output_and_x_alignment(lib):
     ((P, P, 0.01, 0, P, 1, 64, 512, None), NULL),
     ((P, P, 0.01, P, 0, 1, 64, 512, None), NULL),
     ((P, P, 0.01, P, P, 1, 64, 520, None), SHAPE),
-    ((P, P, 0.01, P, P, 17, 64, 512, None), SHAPE),   # M > 16
+    ((P, P, 0.01, P, P, 97, 64, 512, None), SHAPE),   # M > 96
     ((P, P, 0.01, P, P, -1, 64, 512, None), SHAPE),
     ((P, P, 0.01, P + 1, P, 1, 64, 512, None), ALIGN),
     ((P, P, 0.01, P, P + 2, 1, 64, 512, None), ALIGN),
@@ -142,7 +142,7 @@ def test_nvfp4_validation(lib, args, status):
     ((P, P, 0, P, 1, 64, 512, None), NULL),
     ((P, P, P, 0, 1, 64, 512, None), NULL),
     ((P, P, P, P, 1, 64, -1, None), SHAPE),
-    ((P, P, P, P, 17, 64, 512, None), SHAPE),         # M > 16
+    ((P, P, P, P, 97, 64, 512, None), SHAPE),         # M > 96
     ((P, P + 2, P, P, 1, 64, 512, None), ALIGN),
     ((P, P, P + 1, P, 1, 64, 512, None), ALIGN),
     ((P, P, P, P + 1, 1, 64, 512, None), ALIGN),
@@ -187,8 +187,8 @@ def test_wq_group_validation(lib):
     assert f8(2, z, z, P, z, n, 1, 200, None) == SHAPE              # K % 128
     assert f8(2, z, arr(P, P + 2), P, z, n, 1, 384, None) == ALIGN  # row scale not 4-aligned
     assert f8(9, z, z, P, z, n, 1, 384, None) == SHAPE
-    assert nv(2, z, z, g, P, z, n, 17, 512, None) == SHAPE          # M > 16
-    assert f8(2, z, z, P, z, n, 17, 384, None) == SHAPE
+    assert nv(2, z, z, g, P, z, n, 97, 512, None) == SHAPE          # M > 96
+    assert f8(2, z, z, P, z, n, 97, 384, None) == SHAPE
 
 
 def test_debug_dots_validation(lib):

@@ -85,14 +85,14 @@ def test_fp8_shapes(q, M, N, K):
 def test_nvfp4_generic_k(q, M, N, K):
     q.route_reset()
     _nvfp4(q, M, N, K, seed=K)
-    assert q.route_counts()["nvfp4_generic"] == 1
+    assert q.route_counts()["nvfp4_generic"] == (M + 7) // 8   # one launch per 8 rows
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 9, 1), (3, 21, 100), (8, 33, 5130), (9, 21, 100), (16, 33, 5130)])
 def test_fp8_generic_k(q, M, N, K):
     q.route_reset()
     _fp8(q, M, N, K, seed=K)
-    assert q.route_counts()["fp8_generic"] == 1
+    assert q.route_counts()["fp8_generic"] == (M + 7) // 8
 
 
 @pytest.mark.parametrize("M", [1, 8, 16])
@@ -287,3 +287,41 @@ def test_sixteen_warps_passes_group(q, monkeypatch, passes):
         rows = np.arange(Ns[i]) if Ns[i] < 2000 else synth.sample_rows(Ns[i], 64, seed=i).numpy()
         y_ref, bound = oracle.nvfp4_w4a16(c.cpu().numpy()[rows], sc.cpu().numpy()[rows], g, x.cpu().numpy())
         assert_close(f"16 warps, passes group[{i}]", outs[i].cpu().numpy()[:, rows], y_ref, bound)
+
+
+# ------------------------------------------------ 17..96 rows: balanced chunks of <= 16 rows
+
+@pytest.mark.parametrize("M", [17, 24, 33, 64, 96])
+def test_chunked_rows(q, M):
+    """ceil(M / 16) launches of <= 16 rows each; every output within the bound."""
+    N = 16 * 21 + 11
+    q.route_reset()
+    _nvfp4(q, M, N, 5120, seed=1600 + M)
+    _fp8(q, M, N, 5120, seed=1700 + M)
+    c = q.route_counts()
+    assert c["nvfp4_mma_m16n8k16"] == (M + 15) // 16 and c["fp8_mma_m16n8k16"] == (M + 15) // 16
+
+
+@pytest.mark.parametrize("M", [40, 96])
+@pytest.mark.parametrize("N,K", [(7168, 5120), (5120, 5120)])
+def test_fp8_chunked_27b_attention_sampled(q, M, N, K):
+    rows = _synth().sample_rows(N, 24, seed=N + K + M).numpy()
+    _fp8(q, M, N, K, seed=N * 11 + K + M, rows=rows)
+
+
+@pytest.mark.parametrize("M", [17, 96])
+def test_chunked_group_and_generic(q, M):
+    """A gate/up-like group chunked by rows, and the generic kernel (K % 256 != 0) at M > 16."""
+    synth = _synth()
+    K = 5120
+    Ns = [1000, 40]
+    mats = [synth.nvfp4_weights(n, K, seed=1800 + i, device=DEV) for i, n in enumerate(Ns)]
+    x = synth.activations_f16(M, K, seed=1890, device=DEV, outliers=2)
+    outs = q.qgemm_nvfp4_w4a16_group([m[0] for m in mats], [m[1] for m in mats], [m[2] for m in mats], x)
+    for i, (c, sc, g) in enumerate(mats):
+        y_ref, bound = oracle.nvfp4_w4a16(c.cpu().numpy(), sc.cpu().numpy(), g, x.cpu().numpy())
+        assert_close(f"chunked group[{i}]", outs[i].cpu().numpy(), y_ref, bound)
+    q.route_reset()
+    _nvfp4(q, M, 33, 1040, seed=1900 + M)
+    _fp8(q, M, 21, 1000, seed=1950 + M)
+    assert q.route_counts()["nvfp4_generic"] == (M + 7) // 8 and q.route_counts()["fp8_generic"] == (M + 7) // 8
