@@ -36,8 +36,13 @@ __device__ uint32_t g_q4_error;
 
 constexpr int kThreads = 256;        // generic kernel
 constexpr int kWarps = kThreads / 32;
-constexpr int kStreamThreads = 512;      // streaming kernel, M == 1: up to 16 warps
-constexpr int kStreamThreadsWide = 256;  // streaming kernel, M > 1: up to 8 warps
+constexpr int kStreamThreads = 512;      // streaming kernel, M <= kWideFromM - 1: up to 16 warps
+constexpr int kStreamThreadsWide = 256;  // streaming kernel, larger M: up to 8 warps
+#ifndef QMV_Q4_WIDE_FROM_M
+#define QMV_Q4_WIDE_FROM_M 3
+#endif
+constexpr int kWideFromM = QMV_Q4_WIDE_FROM_M;   // first M whose registers allow only 8 warps
+__host__ __device__ constexpr int stream_threads(int M) { return M < kWideFromM ? kStreamThreads : kStreamThreadsWide; }
 // Staged activations, per activation row, one record per unit (8 blocks):
 // q8[256] (bytes 0..255), d8[8] as fp32 (256..287), 8*sum(q8)[8] (288..319),
 // padded to 336 bytes (21 x 16, odd) so 16-byte reads of consecutive records by
@@ -332,7 +337,7 @@ __device__ __forceinline__ void stage_q8_1(const Q4Group &grp, int nb, uint8_t *
 // matrix 0 instead of y (a single-matrix group). kQ4K: the weights are Q4_K
 // super-blocks (a row is K/256 of 144 bytes, the same units as Q4_0).
 template <int M, bool kDots, bool kFused, bool kQ4K>
-__global__ void __launch_bounds__(M == 1 ? kStreamThreads : kStreamThreadsWide) q4_0_stream_kernel(
+__global__ void __launch_bounds__(stream_threads(M)) q4_0_stream_kernel(
     const __grid_constant__ Q4Group grp, int32_t *__restrict__ dots, int64_t K, int S, int P)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -592,7 +597,7 @@ cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t 
 
     // Warps hide latency (each also issues its own copies); slots are the bytes in flight.
     const int act_rows = M * grp.nx;
-    const int cap = (M == 1 ? kStreamThreads : kStreamThreadsWide) / 32;
+    const int cap = stream_threads(M) / 32;
     int warps = std::max(1, std::min(cap, env_int("QMV_Q4_WARPS", cap)));
     const int S = std::max(1, std::min(8, env_int("QMV_Q4_SLOTS", 2)));
     const int budget = env_int("QMV_Q4_PAIR_SMEM", 0) ? dev.smem_per_sm / 2 - 2048 : dev.smem_optin;
