@@ -17,7 +17,7 @@ constexpr const char *kRouteNames[kRouteCount] = {
     "quantize_q8_1", "q4_0_stream_dp4a", "q4_0_generic", "q4_0_stream_fused_quantize", "nvfp4_mma_m16n8k16",
     "nvfp4_generic",
     "fp8_mma_m16n8k16", "fp8_generic", "zero_fill", "q4_0_mma_m16n8k32", "q4_0_mma_fused_quantize",
-    "q4_k_stream_dp4a", "q4_k_stream_fused_quantize",
+    "q4_k_stream_dp4a", "q4_k_stream_fused_quantize", "q4_k_mma_m16n8k32", "q4_k_mma_fused_quantize",
 };
 
 constexpr int kMaxDevices = 64;

@@ -46,8 +46,9 @@ constexpr int kMaxRound = 8;
 constexpr int kRedPitch = 9;                    // floats per partial row (8 columns + pad)
 // Staged activations, per (distinct input, block): the q8 bytes of the M rows,
 // 32 bytes each with the words in the order 0 4 1 5 2 6 3 7 (lane t's words t and
-// 4 + t adjacent), then d8 / 16 of rows 0..7 as fp32 (zero from row M on).
-__host__ __device__ inline int act_block_bytes(int M) { return 32 * M + 32; }
+// 4 + t adjacent), then the scale of rows 0..7 as fp32 (zero from row M on): d8 / 16
+// for Q4_0, d8 for Q4_K, which also stores d8 * T of rows 0..7 (T = sum q8).
+__host__ __device__ inline int act_block_bytes(int M, bool q4k) { return 32 * M + (q4k ? 64 : 32); }
 
 struct MmaParams {
     CUtensorMap tm[kMaxGroup];     // weights of matrix i: [N_i][K / 32 * 18] bytes, box 144 x 16
@@ -66,12 +67,12 @@ struct MmaLayout {
 
 // Shared memory: per-warp rings of boxes, their mbarriers, the staged activations,
 // the round's partial sums [warp][B * 16 rows][9].
-__host__ __device__ inline MmaLayout mma_layout(int S, int B, int nx, int nb, int M)
+__host__ __device__ inline MmaLayout mma_layout(int S, int B, int nx, int nb, int M, bool q4k)
 {
     MmaLayout L;
     L.off_bar = static_cast<uint32_t>(kWarps * S * kBox);
     L.off_act = (L.off_bar + static_cast<uint32_t>(kWarps * S) * 8u + 15u) & ~15u;
-    L.off_red = L.off_act + static_cast<uint32_t>(nx) * static_cast<uint32_t>(nb) * act_block_bytes(M);
+    L.off_red = L.off_act + static_cast<uint32_t>(nx) * static_cast<uint32_t>(nb) * act_block_bytes(M, q4k);
     L.total = L.off_red + static_cast<uint32_t>(kWarps * B * kTile * kRedPitch) * 4u;
     return L;
 }
@@ -82,10 +83,11 @@ __device__ __forceinline__ int act_word_pos(int w) { return 2 * (w & 3) + (w >> 
 // Stage the activations: fused, quantize fp32 [M][K] to Q8_1 with a quad of lanes per
 // block (loads of four passes in flight before any is used); else copy Q8_1
 // [M][K/32]. Rows M..7 of every record are zero.
-template <bool kFused>
+template <bool kFused, bool kQ4K>
 __device__ __forceinline__ void stage_act(const MmaParams &p, int nb, uint8_t *act)
 {
-    const int M = p.M, rb = act_block_bytes(M);
+    const int M = p.M, rb = act_block_bytes(M, kQ4K);
+    const float dscale = kQ4K ? 1.0f : 0.0625f;   // Q4_0's product is 16 (S - 8 T)
     const int total = p.nx * M * nb;   // (input, row < M, block)
     if (kFused) {
         constexpr int kPasses = 4;
@@ -118,8 +120,11 @@ __device__ __forceinline__ void stage_act(const MmaParams &p, int nb, uint8_t *a
                     uint32_t *q = reinterpret_cast<uint32_t *>(rec + 32 * m);
                     q[act_word_pos(2 * part)] = r.qlo;
                     q[act_word_pos(2 * part + 1)] = r.qhi;
-                    if (part == 0)
-                        reinterpret_cast<float *>(rec + 32 * M)[m] = f16_bits_to_float(q8_1_d8_bits(r)) * 0.0625f;
+                    if (part == 0) {
+                        const float d8 = f16_bits_to_float(q8_1_d8_bits(r));
+                        reinterpret_cast<float *>(rec + 32 * M)[m] = d8 * dscale;
+                        if (kQ4K) reinterpret_cast<float *>(rec + 32 * M + 32)[m] = d8 * static_cast<float>(r.sum);
+                    }
                 }
             }
         }
@@ -135,12 +140,20 @@ __device__ __forceinline__ void stage_act(const MmaParams &p, int nb, uint8_t *a
             uint32_t *q = reinterpret_cast<uint32_t *>(rec + 32 * m);
 #pragma unroll
             for (int i = 0; i < 8; ++i) q[act_word_pos(i)] = w[1 + i];
-            reinterpret_cast<float *>(rec + 32 * M)[m] = f16_bits_to_float(w[0] & 0xffffu) * 0.0625f;
+            const float d8 = f16_bits_to_float(w[0] & 0xffffu);
+            reinterpret_cast<float *>(rec + 32 * M)[m] = d8 * dscale;
+            if (kQ4K) {
+                int tsum = 0;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) tsum = __dp4a(static_cast<int>(w[1 + i]), 0x01010101, tsum);
+                reinterpret_cast<float *>(rec + 32 * M + 32)[m] = d8 * static_cast<float>(tsum);   // exact
+            }
         }
     }
-    for (int u = threadIdx.x; u < p.nx * nb * (8 - M); u += kThreads) {   // d8 of rows M..7
+    for (int u = threadIdx.x; u < p.nx * nb * (8 - M); u += kThreads) {   // d8 (and d8 T) of rows M..7
         const int rec_i = u / (8 - M), k = u - rec_i * (8 - M);
         reinterpret_cast<float *>(act + static_cast<int64_t>(rec_i) * rb + 32 * M)[M + k] = 0.0f;
+        if (kQ4K) reinterpret_cast<float *>(act + static_cast<int64_t>(rec_i) * rb + 32 * M + 32)[M + k] = 0.0f;
     }
 }
 
@@ -181,7 +194,10 @@ __device__ __forceinline__ WeightFrag weight_block(const uint8_t *row, int j, in
     return f;
 }
 
-template <bool kFused, bool kDots>
+// kQ4K: the weights are Q4_K super-blocks (144 bytes per row per step, like eight
+// Q4_0 blocks): per sub-block j one mma of the unsigned nibbles (D = S exactly),
+// y += d8 (d sc_j S - dmin mn_j T) with d8 and d8 T from the staged record.
+template <bool kFused, bool kDots, bool kQ4K>
 __global__ void __launch_bounds__(kThreads, 1) q4_0_mma_kernel(const __grid_constant__ MmaParams p, int64_t K)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -191,8 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4_0_mma_kernel(const __grid_cons
     const int nb = static_cast<int>(K >> 5);
     const int nsteps = nb >> 3;   // 8 blocks per step
     const int ntiles = p.tile_start[p.count];
-    const MmaLayout L = mma_layout(S, B, p.nx, nb, p.M);
-    const int rb = act_block_bytes(p.M);
+    const MmaLayout L = mma_layout(S, B, p.nx, nb, p.M, kQ4K);
+    const int rb = act_block_bytes(p.M, kQ4K);
     uint8_t *ring = smem + warp * S * kBox;
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.off_bar) + warp * S;
     uint8_t *act = smem + L.off_act;
@@ -240,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4_0_mma_kernel(const __grid_cons
     __syncwarp();
     grid_launch_dependents();
     grid_dependency_wait();
-    stage_act<kFused>(p, nb, act);
+    stage_act<kFused, kQ4K>(p, nb, act);
     __syncthreads();
 
     int slot = 0;
@@ -287,6 +303,59 @@ __global__ void __launch_bounds__(kThreads, 1) q4_0_mma_kernel(const __grid_cons
             }
             const uint8_t *box = ring + slot * kBox;
             const uint8_t *rg = box + gid * kUnitBytes, *rh = box + (gid + 8) * kUnitBytes;
+            if constexpr (kQ4K) {
+                // super-block headers of rows gid, gid + 8 (16-byte aligned: 144-byte pitch)
+                const uint4 hg = *reinterpret_cast<const uint4 *>(rg), hh = *reinterpret_cast<const uint4 *>(rh);
+                const float dg = f16_bits_to_float(hg.x & 0xffffu), mg = f16_bits_to_float(hg.x >> 16);
+                const float dh = f16_bits_to_float(hh.x & 0xffffu), mh = f16_bits_to_float(hh.x >> 16);
+                // six-bit scales and minimums: sub-blocks 0..3 in the low bits of bytes 0..7,
+                // 4..7 from a nibble of bytes 8..11 and the top two bits of bytes 0..7
+                const uint32_t scg[2] = {hg.y & 0x3f3f3f3fu, (hg.w & 0x0f0f0f0fu) | ((hg.y >> 2) & 0x30303030u)};
+                const uint32_t mng[2] = {hg.z & 0x3f3f3f3fu, ((hg.w >> 4) & 0x0f0f0f0fu) | ((hg.z >> 2) & 0x30303030u)};
+                const uint32_t sch[2] = {hh.y & 0x3f3f3f3fu, (hh.w & 0x0f0f0f0fu) | ((hh.y >> 2) & 0x30303030u)};
+                const uint32_t mnh[2] = {hh.z & 0x3f3f3f3fu, ((hh.w >> 4) & 0x0f0f0f0fu) | ((hh.z >> 2) & 0x30303030u)};
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    // data words t and 4 + t of sub-block pair c: k 4t.. and 16 + 4t.. of
+                    // sub-block 2c (low nibbles) and 2c + 1 (high nibbles)
+                    const uint32_t g0 = *reinterpret_cast<const uint32_t *>(rg + 16 + 32 * c + 4 * t);
+                    const uint32_t g1 = *reinterpret_cast<const uint32_t *>(rg + 32 + 32 * c + 4 * t);
+                    const uint32_t h0 = *reinterpret_cast<const uint32_t *>(rh + 16 + 32 * c + 4 * t);
+                    const uint32_t h1 = *reinterpret_cast<const uint32_t *>(rh + 32 + 32 * c + 4 * t);
+#pragma unroll
+                    for (int hi = 0; hi < 2; ++hi) {
+                        const int j = 2 * c + hi;
+                        const int sh = 4 * hi;
+                        const int b = s * 8 + j;
+                        const uint8_t *rec = xa + static_cast<int64_t>(b) * rb;
+                        const uint2 bw = gid < p.M ? *reinterpret_cast<const uint2 *>(rec + 32 * gid + 8 * t)
+                                                   : make_uint2(0u, 0u);
+                        int d[4];
+                        mma_16832_s8(d, (g0 >> sh) & 0x0f0f0f0fu, (h0 >> sh) & 0x0f0f0f0fu, (g1 >> sh) & 0x0f0f0f0fu,
+                                     (h1 >> sh) & 0x0f0f0f0fu, bw.x, bw.y);
+                        if (kDots) {
+                            const int64_t n0 = row0 + gid, n1 = n0 + 8, N0 = p.N[0];
+                            const int m0 = 2 * t, m1 = m0 + 1;
+                            if (m0 < p.M && n0 < N0) p.dots[(m0 * N0 + n0) * nb + b] = d[0];
+                            if (m1 < p.M && n0 < N0) p.dots[(m1 * N0 + n0) * nb + b] = d[1];
+                            if (m0 < p.M && n1 < N0) p.dots[(m0 * N0 + n1) * nb + b] = d[2];
+                            if (m1 < p.M && n1 < N0) p.dots[(m1 * N0 + n1) * nb + b] = d[3];
+                        } else {
+                            const int wi = j >> 2, by = 8 * (j & 3);
+                            const float dsg = dg * static_cast<float>((scg[wi] >> by) & 0xffu);
+                            const float dmg = mg * static_cast<float>((mng[wi] >> by) & 0xffu);
+                            const float dsh = dh * static_cast<float>((sch[wi] >> by) & 0xffu);
+                            const float dmh = mh * static_cast<float>((mnh[wi] >> by) & 0xffu);
+                            const float2 d8 = *reinterpret_cast<const float2 *>(rec + 32 * p.M + 8 * t);
+                            const float2 d8t = *reinterpret_cast<const float2 *>(rec + 32 * p.M + 32 + 8 * t);
+                            acc[0] = fmaf(static_cast<float>(d[0]), dsg * d8.x, fmaf(-dmg, d8t.x, acc[0]));
+                            acc[1] = fmaf(static_cast<float>(d[1]), dsg * d8.y, fmaf(-dmg, d8t.y, acc[1]));
+                            acc[2] = fmaf(static_cast<float>(d[2]), dsh * d8.x, fmaf(-dmh, d8t.x, acc[2]));
+                            acc[3] = fmaf(static_cast<float>(d[3]), dsh * d8.y, fmaf(-dmh, d8t.y, acc[3]));
+                        }
+                    }
+                }
+            } else {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const WeightFrag fg = weight_block(rg, j, t), fh = weight_block(rh, j, t);
@@ -312,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4_0_mma_kernel(const __grid_cons
                     acc[2] = fmaf(static_cast<float>(d[2]), fh.d4 * d8.x, acc[2]);
                     acc[3] = fmaf(static_cast<float>(d[3]), fh.d4 * d8.y, acc[3]);
                 }
+            }
             }
             __syncwarp();   // every lane is done with the box: refill the slot
             if (lane == 0 && pending()) issue(slot);
@@ -347,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4_0_mma_kernel(const __grid_cons
 
 }  // namespace
 
-cudaError_t plan_q4_0_mma(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t K, Q4Plan *plan)
+cudaError_t plan_q4_0_mma(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t K, Q4Plan *plan, bool q4k)
 {
     plan->route = kRouteQ4_0Generic;   // "not planned"
     if (K % 256 != 0 || M < 1 || M > 8) return cudaSuccess;
@@ -356,7 +426,7 @@ cudaError_t plan_q4_0_mma(const DeviceInfo &dev, const Q4Group &grp, int M, int6
     const int64_t nb = K / 32, nsteps = nb / 8;
     int64_t ntiles = 0;
     for (int i = 0; i < grp.count; ++i) ntiles += (grp.row_start[i + 1] - grp.row_start[i] + kTile - 1) / kTile;
-    if (ntiles == 0 || ntiles > 0x7fffffff || nb > 0x7fffffff / act_block_bytes(M)) return cudaSuccess;
+    if (ntiles == 0 || ntiles > 0x7fffffff || nb > 0x7fffffff / act_block_bytes(M, q4k)) return cudaSuccess;
     // tiles per round: a multiple of 8 / gcd(steps, 8), so every warp gets the same
     // number of steps, and enough for 8 steps per warp between the round's barriers
     int gcd = kWarps;
@@ -370,9 +440,9 @@ cudaError_t plan_q4_0_mma(const DeviceInfo &dev, const Q4Group &grp, int M, int6
     int best_s = 0, best_occ = 0;
     for (int c = 0; c < 3; ++c) {
         const int S = s_env > 0 ? std::min(8, s_env) : cands[c];
-        const uint32_t dyn = mma_layout(S, B, grp.nx, static_cast<int>(nb), M).total;
+        const uint32_t dyn = mma_layout(S, B, grp.nx, static_cast<int>(nb), M, q4k).total;
         if (dyn > static_cast<uint32_t>(dev.smem_optin)) continue;
-        auto k = q4_0_mma_kernel<true, false>;   // the variants share their resources
+        auto k = q4k ? q4_0_mma_kernel<true, false, true> : q4_0_mma_kernel<true, false, false>;
         cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(k), dev.smem_optin);
         if (e != cudaSuccess) return e;
         int occ = 0;
@@ -396,12 +466,12 @@ cudaError_t plan_q4_0_mma(const DeviceInfo &dev, const Q4Group &grp, int M, int6
     plan->prefetch = 0;
     plan->chunk_units = 1;
     plan->grid = static_cast<int>(std::min<int64_t>(ntiles, static_cast<int64_t>(dev.sm_count) * std::min(4, best_occ)));
-    plan->smem_bytes = static_cast<int>(mma_layout(best_s, B, grp.nx, static_cast<int>(nb), M).total);
+    plan->smem_bytes = static_cast<int>(mma_layout(best_s, B, grp.nx, static_cast<int>(nb), M, q4k).total);
     return cudaSuccess;
 }
 
 cudaError_t launch_q4_0_mma(const Q4Plan &plan, const Q4Group &grp, int32_t *dots, int M, int64_t K, bool fused,
-                            cudaStream_t s)
+                            cudaStream_t s, bool q4k)
 {
     MmaParams p{};
     p.count = grp.count;
@@ -436,11 +506,13 @@ cudaError_t launch_q4_0_mma(const Q4Plan &plan, const Q4Group &grp, int32_t *dot
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = set_launch_overlap_attr(attr);
-    auto kern = dots ? q4_0_mma_kernel<false, true>
-                     : (fused ? q4_0_mma_kernel<true, false> : q4_0_mma_kernel<false, false>);
+    auto kern = q4k ? (dots ? q4_0_mma_kernel<false, true, true>
+                            : (fused ? q4_0_mma_kernel<true, false, true> : q4_0_mma_kernel<false, false, true>))
+                    : (dots ? q4_0_mma_kernel<false, true, false>
+                            : (fused ? q4_0_mma_kernel<true, false, false> : q4_0_mma_kernel<false, false, false>));
     cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), plan.smem_bytes);
     if (e != cudaSuccess) return e;
-    route_hit(fused ? kRouteQ4_0MmaFused : kRouteQ4_0Mma);
+    route_hit(q4k ? (fused ? kRouteQ4KMmaFused : kRouteQ4KMma) : (fused ? kRouteQ4_0MmaFused : kRouteQ4_0Mma));
     return cudaLaunchKernelEx(&cfg, kern, p, K);
 }
 

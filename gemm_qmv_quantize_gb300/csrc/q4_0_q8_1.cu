@@ -589,9 +589,9 @@ cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t 
     plan->smem_bytes = 0;
     plan->grid = static_cast<int>((N + kWarps - 1) / kWarps);
     if (!aligned || K % 256 != 0) return cudaSuccess;
-    // from a few activation rows on, the tensor cores (Q4_0 only)
-    if (!q4k && M >= env_int("QMV_Q4_MMA_MIN_M", 5)) {
-        cudaError_t e = plan_q4_0_mma(dev, grp, M, K, plan);
+    // from a few activation rows on, the tensor cores
+    if (M >= env_int(q4k ? "QMV_Q4K_MMA_MIN_M" : "QMV_Q4_MMA_MIN_M", 5)) {
+        cudaError_t e = plan_q4_0_mma(dev, grp, M, K, plan, q4k);
         if (e != cudaSuccess || plan->route == kRouteQ4_0Mma) return e;
     }
 
@@ -640,12 +640,12 @@ void assign_ctas(Q4Group &grp, int total)
 cudaError_t launch_q4_0(const Q4Plan &plan, const Q4Group &grp_in, int32_t *dots, int M, int64_t K, bool fused,
                         cudaStream_t s, bool q4k)
 {
-    if (plan.route == kRouteQ4_0Mma) return launch_q4_0_mma(plan, grp_in, dots, M, K, fused, s);
+    if (plan.route == kRouteQ4_0Mma) return launch_q4_0_mma(plan, grp_in, dots, M, K, fused, s, q4k);
     if (fused && plan.route != kRouteQ4_0Stream) return cudaErrorInvalidValue;
     Q4Group grp = grp_in;
     if (plan.route == kRouteQ4_0Stream) assign_ctas(grp, plan.grid * plan.warps);   // per warp
     if (q4k) {
-        if (plan.route != kRouteQ4_0Stream) return cudaErrorInvalidValue;   // Q4_K: the streaming kernel only
+        if (plan.route != kRouteQ4_0Stream) return cudaErrorInvalidValue;   // Q4_K: the streaming kernels only
         route_hit(fused ? kRouteQ4KStreamFused : kRouteQ4KStream);
         if (dots) return launch_dispatch<true, false, true>(plan, grp, dots, M, K, s);
         if (fused) return launch_dispatch<false, true, true>(plan, grp, dots, M, K, s);

@@ -23,6 +23,8 @@ enum Route : int {
     kRouteQ4_0MmaFused,   // ... with the Q8_1 quantize in the prologue
     kRouteQ4KStream,      // Q4_K: the Q4_0 streaming kernel's machinery, K-quant super-blocks
     kRouteQ4KStreamFused, // ... with the Q8_1 quantize in the prologue
+    kRouteQ4KMma,         // Q4_K: the Q4_0 tensor-core kernel's machinery (m16n8k32 int8), larger M
+    kRouteQ4KMmaFused,    // ... with the Q8_1 quantize in the prologue
     kRouteCount
 };
 
@@ -81,9 +83,10 @@ struct Q4Group {
 cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t K, Q4Plan *plan, bool q4k = false);
 // The tensor-core kernel's plan (route kRouteQ4_0Mma), or route kRouteQ4_0Generic
 // when it does not apply.
-cudaError_t plan_q4_0_mma(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t K, Q4Plan *plan);
+cudaError_t plan_q4_0_mma(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t K, Q4Plan *plan,
+                          bool q4k = false);
 cudaError_t launch_q4_0_mma(const Q4Plan &plan, const Q4Group &grp, int32_t *dots, int M, int64_t K, bool fused,
-                            cudaStream_t s);
+                            cudaStream_t s, bool q4k = false);
 cudaError_t launch_q4_0(const Q4Plan &plan, const Q4Group &grp, int32_t *dots, int M, int64_t K, bool fused,
                         cudaStream_t s, bool q4k = false);
 

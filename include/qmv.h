@@ -147,8 +147,9 @@ QMV_API qmv_status qmv_q4_0_q8_1_group(int count, const void *const *w, const vo
  *   y   fp32 [M][N]: y[m][n] = sum_b d8[m][b] * (d sc_j S - dmin mn_j T) over
  *       the Q8_1 blocks b (= sub-blocks), with the exact integer sums
  *       S = sum q * q8 and T = sum q8, accumulated in fp32.
- *   K a multiple of 256. One streaming kernel (dp4a) serves every M; it stages
- *   the activations in shared memory, so very large K returns QMV_ERR_SHAPE.
+ *   K a multiple of 256. The dp4a streaming kernel serves M = 1..4, the int8
+ *   tensor cores (m16n8k32 on the unsigned nibbles, D = S exactly) M = 5..8; both
+ *   stage the activations in shared memory, so very large K returns QMV_ERR_SHAPE.
  */
 QMV_API qmv_status qmv_q4_k_q8_1(const void *w, const void *xq, float *y, int M, int64_t N, int64_t K,
                                  qmv_stream_t stream);

@@ -1,4 +1,5 @@
-"""GPU parity: Q4_K x Q8_1 MMVQ through the C ABI vs the CPU oracle.
+"""GPU parity: Q4_K x Q8_1 MMVQ through the C ABI vs the CPU oracle (the dp4a
+streaming kernel up to M = 4, the int8 tensor-core kernel from M = 5).
 
 - Integer sub-block sums S = sum q * q8 identical (qmv_debug_q4_k_block_dots runs
   the product kernel's device code with the product kernel choice).
@@ -61,9 +62,27 @@ def test_block_dots_exact(q, M):
 
 @pytest.mark.parametrize("M", range(1, 9))
 def test_multi_span_ragged(q, M):
+    """dp4a streaming kernel up to M = 4, int8 tensor cores (m16n8k32) from M = 5."""
     q.route_reset()
     _case(q, M, 16 * 152 + 37, 2048, seed=100 + M)
-    assert q.route_counts()["q4_k_stream_dp4a"] == 1
+    assert q.route_counts()["q4_k_stream_dp4a" if M <= 4 else "q4_k_mma_m16n8k32"] == 1
+
+
+@pytest.mark.parametrize("M", [1, 5, 8])
+def test_both_kernels_at_every_m(q, monkeypatch, M):
+    """The kernel the planner does not pick for this M, forced: within the bound too."""
+    synth = _synth()
+    N, K = 16 * 40 + 9, 4096
+    w = synth.q4_k_weights(N, K, seed=150 + M, device=DEV)
+    xq = q.qmv_quantize_q8_1(synth.activations_f32(M, K, seed=160 + M, device=DEV))
+    monkeypatch.setenv("QMV_Q4K_MMA_MIN_M", "1" if M < 5 else "9")
+    q.route_reset()
+    y = q.qmv_q4_k_q8_1(w, xq, K)
+    dots = q.qmv_debug_q4_k_block_dots(w, xq, K)
+    assert q.route_counts()["q4_k_mma_m16n8k32" if M < 5 else "q4_k_stream_dp4a"] == 2
+    assert np.array_equal(dots.cpu().numpy(), oracle.q4_k_block_dots(w.cpu().numpy(), xq.cpu().numpy(), K))
+    y_ref, bound = oracle.q4_k_q8_1(w.cpu().numpy(), xq.cpu().numpy(), K)
+    assert_close(f"forced kernel M={M}", y.cpu().numpy(), y_ref, bound)
 
 
 @pytest.mark.parametrize("M,N,K", [(1, 1, 256), (2, 7, 512), (5, 33, 4096), (8, 100, 12288), (3, 1, 14336)])
@@ -71,12 +90,12 @@ def test_shapes(q, M, N, K):
     _case(q, M, N, K, seed=N + K)
 
 
-@pytest.mark.parametrize("M", [1, 4, 8])
+@pytest.mark.parametrize("M", [1, 4, 6, 8])
 def test_fused_bit_identical(q, M):
     w, x, xq, y = _case(q, M, 1000, 4096, seed=200 + M)
     q.route_reset()
     yf = q.qmv_q4_k_q8_1_fused(w, x)
-    assert q.route_counts()["q4_k_stream_fused_quantize"] == 1
+    assert q.route_counts()["q4_k_stream_fused_quantize" if M <= 4 else "q4_k_mma_fused_quantize"] == 1
     assert torch.equal(yf, y)
 
 
