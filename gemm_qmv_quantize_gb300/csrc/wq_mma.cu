@@ -502,8 +502,10 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const 
         // the busiest CTA holds waves * grid / tiles times the mean. Within 15 % of the mean
         // a candidate scores 1, else its imbalance; fewer than 16 resident warps per SM
         // add 0.5 (too few to hide the decode latency), each pass over K beyond the first
-        // adds 1 (a pass repeats the per-round reduction); ties keep the earlier (deeper
-        // ring) candidate. Activations stay in shared memory whenever they fit (re-read
+        // adds 1 (a pass repeats the per-round reduction), every 8 resident warps take
+        // 0.05 off (the kernel is bound by latency, and more warps hide more of it: at
+        // M = 1 three 8-warp CTAs with 2 slots beat two with 4 on balanced shapes); ties
+        // keep the earlier candidate. Activations stay in shared memory whenever they fit (re-read
         // through L1 they thrash it at M = 8); 16 warps share one staged copy where 8-warp
         // CTAs would fit only one per SM. At M <= 2, where the activations fit in L1, an
         // unstaged candidate may win on balance.
@@ -512,7 +514,7 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const 
         const int s_env = env_int("QMV_WQ_SLOTS", 0);
         const int w_env = env_int("QMV_WQ_WARPS", 0);
         struct Cand { int W, S; bool xs; };
-        const Cand cands[] = {{8, 4, true}, {8, 3, true}, {8, 2, true}, {16, 3, true}, {16, 2, true},
+        const Cand cands[] = {{8, 3, true}, {8, 4, true}, {8, 2, true}, {16, 3, true}, {16, 2, true},
                               {8, 4, false}, {8, 3, false}, {8, 2, false}};
         constexpr int kCands = static_cast<int>(sizeof(cands) / sizeof(cands[0]));
         int best = -1, best_occ = 0, best_B = 0, best_P = 1;
@@ -556,7 +558,8 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const 
             if (occ < 1) continue;
             const int64_t g = std::min<int64_t>(ntiles, static_cast<int64_t>(dev.sm_count) * occ);
             const double imb = static_cast<double>((ntiles + g - 1) / g * g) / static_cast<double>(ntiles);
-            const double score = (imb <= 1.15 ? 1.0 : imb) + (occ * Wc < 16 ? 0.5 : 0.0) + (Pc - 1);
+            const double score = (imb <= 1.15 ? 1.0 : imb) + (occ * Wc < 16 ? 0.5 : 0.0) + (Pc - 1) -
+                                 0.05 * (occ * Wc / 8);
             if (score < best_score) {
                 best_score = score;
                 best = c;
