@@ -384,7 +384,10 @@ __global__ void __launch_bounds__(kThreads, 1) q4_0_mma_kernel(const __grid_cons
             }
             }
             __syncwarp();   // every lane is done with the box: refill the slot
-            if (lane == 0 && pending()) issue(slot);
+            if (lane == 0 && pending()) {
+                fence_proxy_async_shared();   // the warp's reads of the box before the copy's writes
+                issue(slot);
+            }
             if (++slot == S) {
                 slot = 0;
                 phase ^= 1u;

@@ -429,7 +429,10 @@ __global__ void __launch_bounds__(stream_threads(M)) q4_0_stream_kernel(
                 q4_unit<M, kDots>(wu, act0 + uin * kActUnitStride, L.act_m_stride, v, du, Nm * nb);
         }
         __syncwarp();   // every lane is done with the slot
-        if (lane == 0 && c + S < nchunks) issue(c + S, slot);
+        if (lane == 0 && c + S < nchunks) {
+            fence_proxy_async_shared();   // the warp's reads of the slot before the copy's writes
+            issue(c + S, slot);
+        }
         if (!kDots) {
             // Inclusive scan within the row: the lanes of one row are consecutive,
             // min(uin, lane) of them precede this lane in the chunk.

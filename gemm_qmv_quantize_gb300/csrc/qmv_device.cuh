@@ -116,6 +116,15 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const void *tmap, int x, 
         : "memory");
 }
 
+// Order this thread's earlier generic-proxy shared-memory accesses (and, after a
+// warp or CTA barrier, those of the threads it synchronized with) before its later
+// async-proxy (bulk copy / TMA) accesses: a slot the warp has just read is refilled
+// by a copy only after the reads are performed.
+__device__ __forceinline__ void fence_proxy_async_shared()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 16-byte asynchronous copy global -> shared (both 16-byte aligned), bypassing L1;
 // cp_async_wait_all waits for all of this thread's outstanding copies.
 __device__ __forceinline__ void cp_async_16(void *dst, const void *src)

@@ -313,7 +313,10 @@ __global__ void __launch_bounds__(32 * kW, kW == 16 ? 1 : (kMT == 1 ? 3 : 2))
                     sb = *reinterpret_cast<const uint32_t *>(sbx + (gid + 8) * 16 + 4 * t);
                 }
                 __syncwarp();   // the slot is in registers: refill it
-                if (lane == 0 && pending()) issue(slot);
+                if (lane == 0 && pending()) {
+                    fence_proxy_async_shared();   // the warp's reads of the slot before the copy's writes
+                    issue(slot);
+                }
 
                 // B fragments: activation rows gid + 8 mt. Columns of D past M are never
                 // stored, so their lanes need only finite values: from shared memory they
