@@ -325,3 +325,17 @@ def test_chunked_group_and_generic(q, M):
     _nvfp4(q, M, 33, 1040, seed=1900 + M)
     _fp8(q, M, 21, 1000, seed=1950 + M)
     assert q.route_counts()["nvfp4_generic"] == (M + 7) // 8 and q.route_counts()["fp8_generic"] == (M + 7) // 8
+
+
+# ------------------------------------------------ largest K and M
+
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_nvfp4_large_k(q, M):
+    """K = 65536 (a 2 MB fp16 activation matrix at M = 16): staged in passes or read
+    through L1, within the bound."""
+    _nvfp4(q, M, 16 * 7 + 3, 65536, seed=2300 + M, outliers=2)
+
+
+def test_fp8_largest_m_large_k(q):
+    """M = 96 (six 16-row chunks) with K = 16384."""
+    _fp8(q, 96, 16 * 5 + 1, 16384, seed=2400)

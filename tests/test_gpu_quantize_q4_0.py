@@ -397,3 +397,25 @@ def test_q4_0_group_on_q8_1_matches_single_calls(q, q4_kernel, M):
         assert torch.equal(o, q.qmv_q4_0_q8_1(w, x, K))
     y_ref, bound = oracle.q4_0_q8_1(ws[1].cpu().numpy(), xqs[1].cpu().numpy(), K)
     assert_close("group[1]", outs[1].cpu().numpy(), y_ref, bound)
+
+
+# ---------------------------------------------------------------- largest K
+
+def test_large_k_routes_and_parity(q):
+    """K = 65536: the streaming kernel at M = 1; at M = 8 the staged activations of
+    the streaming and tensor-core kernels exceed shared memory, so the single call
+    takes the generic kernel and the fused call refuses with QMV_ERR_SHAPE."""
+    synth = _synth()
+    K, N = 65536, 40
+    w = synth.q4_0_weights(N, K, seed=77, device=DEV)
+    for M, route in ((1, "q4_0_stream_dp4a"), (8, "q4_0_generic")):
+        x = synth.activations_f32(M, K, seed=78 + M, device=DEV)
+        xq = q.qmv_quantize_q8_1(x)
+        q.route_reset()
+        y = q.qmv_q4_0_q8_1(w, xq, K)
+        assert q.route_counts()[route] == 1
+        y_ref, bound = oracle.q4_0_q8_1(w.cpu().numpy(), xq.cpu().numpy(), K)
+        assert_close(f"K=65536 M={M}", y.cpu().numpy(), y_ref, bound)
+    from gemm_qmv_quantize_gb300 import QmvError
+    with pytest.raises(QmvError, match="QMV_ERR_SHAPE"):
+        q.qmv_q4_0_q8_1_fused(w, synth.activations_f32(8, K, seed=90, device=DEV))
