@@ -43,6 +43,7 @@ constexpr int kStreamThreadsWide = 256;  // streaming kernel, larger M: up to 8 
 #endif
 constexpr int kWideFromM = QMV_Q4_WIDE_FROM_M;   // first M whose registers allow only 8 warps
 __host__ __device__ constexpr int stream_threads(int M) { return M < kWideFromM ? kStreamThreads : kStreamThreadsWide; }
+constexpr int kActRegsThreads = 512;     // streaming kernel with register-resident activations
 // Staged activations, per activation row, one record per unit (8 blocks):
 // q8[256] (bytes 0..255), d8[8] as fp32 (256..287), 8*sum(q8)[8] (288..319),
 // padded to 336 bytes (21 x 16, odd) so 16-byte reads of consecutive records by
@@ -232,6 +233,101 @@ __device__ __forceinline__ void q4k_unit(const uint8_t *wu, const uint8_t *act, 
     }
 }
 
+// One activation row's record of one unit held in registers (M = 1, a lane that
+// handles the same unit of every row it visits): q8 of the unit's 8 blocks, d8, 8 T.
+struct ActRegs {
+    uint4 q[16];
+    float d8[8];
+    int t8[8];
+};
+
+__device__ __forceinline__ void load_act_regs(const uint8_t *rec, ActRegs &r)
+{
+    const uint4 *a = reinterpret_cast<const uint4 *>(rec);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) r.q[i] = a[i];
+    const float4 d8a = *reinterpret_cast<const float4 *>(rec + kActD8Off);
+    const float4 d8b = *reinterpret_cast<const float4 *>(rec + kActD8Off + 16);
+    const int4 t8a = *reinterpret_cast<const int4 *>(rec + kActT8Off);
+    const int4 t8b = *reinterpret_cast<const int4 *>(rec + kActT8Off + 16);
+    r.d8[0] = d8a.x; r.d8[1] = d8a.y; r.d8[2] = d8a.z; r.d8[3] = d8a.w;
+    r.d8[4] = d8b.x; r.d8[5] = d8b.y; r.d8[6] = d8b.z; r.d8[7] = d8b.w;
+    r.t8[0] = t8a.x; r.t8[1] = t8a.y; r.t8[2] = t8a.z; r.t8[3] = t8a.w;
+    r.t8[4] = t8b.x; r.t8[5] = t8b.y; r.t8[6] = t8b.z; r.t8[7] = t8b.w;
+}
+
+// q4_unit / q4k_unit for M = 1 against a register-resident activation record.
+__device__ __forceinline__ float q4_unit_regs(const uint8_t *wu, const ActRegs &r)
+{
+    const uint4 *wp = reinterpret_cast<const uint4 *>(wu);
+    uint32_t w[36];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+        const uint4 v = wp[i];
+        w[4 * i] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+    }
+    float part = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+        const int wa = (18 * j) / 4;
+        uint32_t qa[4], qb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            qa[i] = __byte_perm(w[wa + i], w[wa + i + 1], 0x5432);
+            qb[i] = w[wa + 5 + i];
+        }
+        const int sa = q4_block_dot(qa, r.q[2 * j], r.q[2 * j + 1], r.t8[j]);
+        const int sb = q4_block_dot(qb, r.q[2 * j + 2], r.q[2 * j + 3], r.t8[j + 1]);
+        part = fmaf(f16_bits_to_float(w[wa] & 0xffffu) * r.d8[j], static_cast<float>(sa), part);
+        part = fmaf(f16_bits_to_float(w[wa + 4] >> 16) * r.d8[j + 1], static_cast<float>(sb), part);
+    }
+    return part;
+}
+
+__device__ __forceinline__ float q4k_unit_regs(const uint8_t *wu, const ActRegs &r)
+{
+    const uint4 *wp = reinterpret_cast<const uint4 *>(wu);
+    uint32_t w[36];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+        const uint4 v = wp[i];
+        w[4 * i] = v.x;
+        w[4 * i + 1] = v.y;
+        w[4 * i + 2] = v.z;
+        w[4 * i + 3] = v.w;
+    }
+    const float d = f16_bits_to_float(w[0] & 0xffffu), dmin = f16_bits_to_float(w[0] >> 16);
+    const uint32_t sc[2] = {w[1] & 0x3f3f3f3fu, (w[3] & 0x0f0f0f0fu) | ((w[1] >> 2) & 0x30303030u)};
+    const uint32_t mn[2] = {w[2] & 0x3f3f3f3fu, ((w[3] >> 4) & 0x0f0f0f0fu) | ((w[2] >> 2) & 0x30303030u)};
+    float part = 0.0f;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint4 x0 = r.q[4 * c], x1 = r.q[4 * c + 1], x2 = r.q[4 * c + 2], x3 = r.q[4 * c + 3];
+        const uint32_t lo_x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+        const uint32_t hi_x[8] = {x2.x, x2.y, x2.z, x2.w, x3.x, x3.y, x3.z, x3.w};
+        int lo = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t qw = w[4 + 8 * c + i];
+            lo = dp4a_us(qw & 0x0f0f0f0fu, lo_x[i], lo);
+            hi = dp4a_us(qw & 0xf0f0f0f0u, hi_x[i], hi);
+        }
+        const int sd[2] = {lo, hi >> 4};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int j = 2 * c + h;
+            const float dsc = d * static_cast<float>((sc[j >> 2] >> (8 * (j & 3))) & 0xffu);
+            const float dmn = dmin * static_cast<float>((mn[j >> 2] >> (8 * (j & 3))) & 0xffu);
+            part = fmaf(dsc * r.d8[j], static_cast<float>(sd[h]), part);
+            part = fmaf(-(dmn * r.d8[j]), 0.125f * static_cast<float>(r.t8[j]), part);
+        }
+    }
+    return part;
+}
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
@@ -336,8 +432,11 @@ __device__ __forceinline__ void stage_q8_1(const Q4Group &grp, int nb, uint8_t *
 // prologue; else they are Q8_1 [M][K/32]. kDots: write the integer block dots of
 // matrix 0 instead of y (a single-matrix group). kQ4K: the weights are Q4_K
 // super-blocks (a row is K/256 of 144 bytes, the same units as Q4_0).
-template <int M, bool kDots, bool kFused, bool kQ4K>
-__global__ void __launch_bounds__(stream_threads(M)) q4_0_stream_kernel(
+// kActRegs (M = 1, rows of U units with 32 % U == 0): a lane handles unit lane % U of
+// every row it visits, so its activation record is loaded into registers once
+// instead of read from shared memory for every unit.
+template <int M, bool kDots, bool kFused, bool kQ4K, bool kActRegs = false>
+__global__ void __launch_bounds__(kActRegs ? kActRegsThreads : stream_threads(M)) q4_0_stream_kernel(
     const __grid_constant__ Q4Group grp, int32_t *__restrict__ dots, int64_t K, int S, int P)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -404,6 +503,8 @@ __global__ void __launch_bounds__(stream_threads(M)) q4_0_stream_kernel(
     float carry[M];   // partial sum of the row left open by the previous chunk
 #pragma unroll
     for (int m = 0; m < M; ++m) carry[m] = 0.0f;
+    ActRegs ar;
+    if (kActRegs) load_act_regs(act0 + uin * kActUnitStride, ar);   // uin never changes (du == 0)
     int slot = 0;
     uint32_t phase = 0;
     for (int c = 0; c < nchunks; ++c) {
@@ -423,7 +524,9 @@ __global__ void __launch_bounds__(stream_threads(M)) q4_0_stream_kernel(
         if (live) {
             const uint8_t *wu = ring + slot * L.slotbytes + lane * kUnitBytes;
             int32_t *du = kDots ? dots + (r0 + rr) * nb + 8 * uin : nullptr;
-            if (kQ4K)
+            if (kActRegs)
+                v[0] = kQ4K ? q4k_unit_regs(wu, ar) : q4_unit_regs(wu, ar);
+            else if (kQ4K)
                 q4k_unit<M, kDots>(wu, act0 + uin * kActUnitStride, L.act_m_stride, v, du, Nm * nb);
             else
                 q4_unit<M, kDots>(wu, act0 + uin * kActUnitStride, L.act_m_stride, v, du, Nm * nb);
@@ -546,6 +649,8 @@ cudaError_t launch_m(const Q4Plan &p, const Q4Group &grp, int32_t *dots, int64_t
     cfg.numAttrs = set_launch_overlap_attr(attr);
     if (p.route == kRouteQ4_0Stream) {
         auto kern = q4_0_stream_kernel<M, kDots, kFused, kQ4K>;
+        if constexpr (M == 1 && !kDots)
+            if (p.act_regs) kern = q4_0_stream_kernel<M, kDots, kFused, kQ4K, true>;
         cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), p.smem_bytes);
         if (e != cudaSuccess) return e;
         cfg.blockDim = dim3(static_cast<unsigned>(p.warps * 32));   // consumers + the producer
@@ -590,6 +695,7 @@ cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t 
     plan->prefetch = 0;
     plan->round = 0;
     plan->smem_bytes = 0;
+    plan->act_regs = false;
     plan->grid = static_cast<int>((N + kWarps - 1) / kWarps);
     if (!aligned || K % 256 != 0) return cudaSuccess;
     // from a few activation rows on, the tensor cores
@@ -602,15 +708,32 @@ cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t 
     const int act_rows = M * grp.nx;
     const int cap = stream_threads(M) / 32;
     int warps = std::max(1, std::min(cap, env_int("QMV_Q4_WARPS", cap)));
-    const int S = std::max(1, std::min(8, env_int("QMV_Q4_SLOTS", 2)));
+    int S = std::max(1, std::min(8, env_int("QMV_Q4_SLOTS", 2)));
     const int budget = env_int("QMV_Q4_PAIR_SMEM", 0) ? dev.smem_per_sm / 2 - 2048 : dev.smem_optin;
     while (warps > 1 && q4_layout(act_rows, K, warps, S).total > static_cast<uint32_t>(budget)) --warps;
     if (q4_layout(act_rows, K, warps, S).total > static_cast<uint32_t>(dev.smem_optin)) return cudaSuccess;
+    // M = 1 with rows of U units, U dividing 32 (K = 4096: U = 16): every lane keeps
+    // one unit of every row it visits, so its activation record lives in registers
+    // (119 of them: 16 warps still fit) and the 20 shared-memory reads of the record
+    // per 144-byte unit are gone (Llama-2-7B stack 3839 -> 3972 GB/s)
+    bool act_regs = false;
+    const int U = static_cast<int>(K / 256);
+    if (M == 1 && U <= 32 && 32 % U == 0 && env_int("QMV_Q4_ACT_REGS", 1) != 0) {
+        int w2 = std::min(warps, std::max(1, std::min(kActRegsThreads / 32, env_int("QMV_Q4_ACT_REGS_WARPS", 16))));
+        const int S2 = std::max(1, std::min(8, env_int("QMV_Q4_ACT_REGS_SLOTS", S)));
+        while (w2 > 1 && q4_layout(act_rows, K, w2, S2).total > static_cast<uint32_t>(dev.smem_optin)) --w2;
+        if (q4_layout(act_rows, K, w2, S2).total <= static_cast<uint32_t>(dev.smem_optin)) {
+            act_regs = true;
+            warps = w2;
+            S = S2;
+        }
+    }
     const int per_sm = std::max(1, std::min(4, env_int("QMV_Q4_CTAS_PER_SM", 1)));
     const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>((N + warps - 1) / warps,
                                                                  static_cast<int64_t>(dev.sm_count) * per_sm));
     if ((N / (ctas * warps) + 1) * (K / 256) >= (int64_t(1) << 31)) return cudaSuccess;   // 32-bit unit counters
     plan->route = kRouteQ4_0Stream;
+    plan->act_regs = act_regs;
     plan->warps = warps;
     plan->stages = S;
     plan->prefetch = std::max(0, std::min(S * warps, env_int("QMV_Q4_PREFETCH", 4)));

@@ -53,6 +53,7 @@ struct Q4Plan {
     int round;         // tensor-core kernel: tiles per reduction round
     int grid;
     int smem_bytes;
+    bool act_regs;     // streaming kernel, M = 1: activation record in registers (rows of U | 32 units)
 };
 
 // Programmatic dependent launch (opt-in, qmv_set_launch_overlap): fills attr[0]
