@@ -287,6 +287,44 @@ __device__ __forceinline__ float q4_unit_regs(const uint8_t *wu, const ActRegs &
     return part;
 }
 
+// q4_unit for M = 2 against two register-resident activation records (the weight
+// unit decoded once for both rows).
+__device__ __forceinline__ void q4_unit_regs2(const uint8_t *wu, const ActRegs (&r)[2], float (&v)[2])
+{
+    const uint4 *wp = reinterpret_cast<const uint4 *>(wu);
+    uint32_t w[36];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+        const uint4 x = wp[i];
+        w[4 * i] = x.x;
+        w[4 * i + 1] = x.y;
+        w[4 * i + 2] = x.z;
+        w[4 * i + 3] = x.w;
+    }
+    float p0 = 0.0f, p1 = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+        const int wa = (18 * j) / 4;
+        uint32_t qa[4], qb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            qa[i] = __byte_perm(w[wa + i], w[wa + i + 1], 0x5432);
+            qb[i] = w[wa + 5 + i];
+        }
+        const float da = f16_bits_to_float(w[wa] & 0xffffu), db = f16_bits_to_float(w[wa + 4] >> 16);
+        const int a0 = q4_block_dot(qa, r[0].q[2 * j], r[0].q[2 * j + 1], r[0].t8[j]);
+        const int b0 = q4_block_dot(qb, r[0].q[2 * j + 2], r[0].q[2 * j + 3], r[0].t8[j + 1]);
+        const int a1 = q4_block_dot(qa, r[1].q[2 * j], r[1].q[2 * j + 1], r[1].t8[j]);
+        const int b1 = q4_block_dot(qb, r[1].q[2 * j + 2], r[1].q[2 * j + 3], r[1].t8[j + 1]);
+        p0 = fmaf(da * r[0].d8[j], static_cast<float>(a0), p0);
+        p0 = fmaf(db * r[0].d8[j + 1], static_cast<float>(b0), p0);
+        p1 = fmaf(da * r[1].d8[j], static_cast<float>(a1), p1);
+        p1 = fmaf(db * r[1].d8[j + 1], static_cast<float>(b1), p1);
+    }
+    v[0] = p0;
+    v[1] = p1;
+}
+
 __device__ __forceinline__ float q4k_unit_regs(const uint8_t *wu, const ActRegs &r)
 {
     const uint4 *wp = reinterpret_cast<const uint4 *>(wu);
@@ -432,11 +470,12 @@ __device__ __forceinline__ void stage_q8_1(const Q4Group &grp, int nb, uint8_t *
 // prologue; else they are Q8_1 [M][K/32]. kDots: write the integer block dots of
 // matrix 0 instead of y (a single-matrix group). kQ4K: the weights are Q4_K
 // super-blocks (a row is K/256 of 144 bytes, the same units as Q4_0).
-// kActRegs (M = 1, rows of U units with 32 % U == 0): a lane handles unit lane % U of
-// every row it visits, so its activation record is loaded into registers once
-// instead of read from shared memory for every unit.
+// kActRegs (M = 1, or Q4_0 at M = 2; rows of U units with 32 % U == 0): a lane
+// handles unit lane % U of every row it visits, so its activation records are loaded
+// into registers once instead of read from shared memory for every unit.
 template <int M, bool kDots, bool kFused, bool kQ4K, bool kActRegs = false>
-__global__ void __launch_bounds__(kActRegs ? kActRegsThreads : stream_threads(M)) q4_0_stream_kernel(
+__global__ void __launch_bounds__(kActRegs ? (M == 1 ? kActRegsThreads : kStreamThreadsWide) : stream_threads(M))
+    q4_0_stream_kernel(
     const __grid_constant__ Q4Group grp, int32_t *__restrict__ dots, int64_t K, int S, int P)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -503,8 +542,11 @@ __global__ void __launch_bounds__(kActRegs ? kActRegsThreads : stream_threads(M)
     float carry[M];   // partial sum of the row left open by the previous chunk
 #pragma unroll
     for (int m = 0; m < M; ++m) carry[m] = 0.0f;
-    ActRegs ar;
-    if (kActRegs) load_act_regs(act0 + uin * kActUnitStride, ar);   // uin never changes (du == 0)
+    ActRegs ar[kActRegs ? M : 1];
+    if (kActRegs) {   // uin never changes (du == 0)
+#pragma unroll
+        for (int m = 0; m < (kActRegs ? M : 1); ++m) load_act_regs(act0 + m * L.act_m_stride + uin * kActUnitStride, ar[m]);
+    }
     int slot = 0;
     uint32_t phase = 0;
     for (int c = 0; c < nchunks; ++c) {
@@ -524,8 +566,10 @@ __global__ void __launch_bounds__(kActRegs ? kActRegsThreads : stream_threads(M)
         if (live) {
             const uint8_t *wu = ring + slot * L.slotbytes + lane * kUnitBytes;
             int32_t *du = kDots ? dots + (r0 + rr) * nb + 8 * uin : nullptr;
-            if (kActRegs)
-                v[0] = kQ4K ? q4k_unit_regs(wu, ar) : q4_unit_regs(wu, ar);
+            if constexpr (kActRegs && M == 2)
+                q4_unit_regs2(wu, ar, v);
+            else if (kActRegs)
+                v[0] = kQ4K ? q4k_unit_regs(wu, ar[0]) : q4_unit_regs(wu, ar[0]);
             else if (kQ4K)
                 q4k_unit<M, kDots>(wu, act0 + uin * kActUnitStride, L.act_m_stride, v, du, Nm * nb);
             else
@@ -649,7 +693,7 @@ cudaError_t launch_m(const Q4Plan &p, const Q4Group &grp, int32_t *dots, int64_t
     cfg.numAttrs = set_launch_overlap_attr(attr);
     if (p.route == kRouteQ4_0Stream) {
         auto kern = q4_0_stream_kernel<M, kDots, kFused, kQ4K>;
-        if constexpr (M == 1 && !kDots)
+        if constexpr ((M == 1 || (M == 2 && !kQ4K)) && !kDots)
             if (p.act_regs) kern = q4_0_stream_kernel<M, kDots, kFused, kQ4K, true>;
         cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), p.smem_bytes);
         if (e != cudaSuccess) return e;
@@ -718,9 +762,13 @@ cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t 
     // per 144-byte unit are gone (Llama-2-7B stack 3839 -> 3972 GB/s)
     bool act_regs = false;
     const int U = static_cast<int>(K / 256);
-    if (M == 1 && U <= 32 && 32 % U == 0 && env_int("QMV_Q4_ACT_REGS", 1) != 0) {
-        int w2 = std::min(warps, std::max(1, std::min(kActRegsThreads / 32, env_int("QMV_Q4_ACT_REGS_WARPS", 16))));
-        const int S2 = std::max(1, std::min(8, env_int("QMV_Q4_ACT_REGS_SLOTS", S)));
+    // M = 2 (Q4_0): two records, 215 registers, 8 warps with 4-slot rings (Llama-3-8B
+    // MLP 3218 -> 3264 GB/s)
+    const bool m2 = M == 2 && !q4k && env_int("QMV_Q4_ACT_REGS_M2", 1) != 0;
+    if ((M == 1 || m2) && U <= 32 && 32 % U == 0 && env_int("QMV_Q4_ACT_REGS", 1) != 0) {
+        const int wcap = M == 1 ? kActRegsThreads / 32 : kStreamThreadsWide / 32;
+        int w2 = std::min(warps, std::max(1, std::min(wcap, env_int("QMV_Q4_ACT_REGS_WARPS", 16))));
+        const int S2 = std::max(1, std::min(8, env_int("QMV_Q4_ACT_REGS_SLOTS", M == 1 ? S : 4)));
         while (w2 > 1 && q4_layout(act_rows, K, w2, S2).total > static_cast<uint32_t>(dev.smem_optin)) --w2;
         if (q4_layout(act_rows, K, w2, S2).total <= static_cast<uint32_t>(dev.smem_optin)) {
             act_regs = true;
