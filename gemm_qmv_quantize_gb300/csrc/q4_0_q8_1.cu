@@ -473,7 +473,11 @@ __device__ __forceinline__ void stage_q8_1(const Q4Group &grp, int nb, uint8_t *
 // kActRegs (M = 1, or Q4_0 at M = 2; rows of U units with 32 % U == 0): a lane
 // handles unit lane % U of every row it visits, so its activation records are loaded
 // into registers once instead of read from shared memory for every unit.
-template <int M, bool kDots, bool kFused, bool kQ4K, bool kActRegs = false>
+// kPair (Q4_0, M = 2..4, rows of 16 units): in a chunk of two whole rows, lanes l and
+// l + 16 hold the same unit of the two rows; each computes both rows' unit against
+// half of the M activation rows and they swap halves with one shuffle per output
+// pair, so a lane reads ceil(M / 2) activation records from shared memory, not M.
+template <int M, bool kDots, bool kFused, bool kQ4K, bool kActRegs = false, bool kPair = false>
 __global__ void __launch_bounds__(kActRegs ? (M == 1 ? kActRegsThreads : kStreamThreadsWide) : stream_threads(M))
     q4_0_stream_kernel(
     const __grid_constant__ Q4Group grp, int32_t *__restrict__ dots, int64_t K, int S, int P)
@@ -563,7 +567,35 @@ __global__ void __launch_bounds__(kActRegs ? (M == 1 ? kActRegsThreads : kStream
         float v[M];
 #pragma unroll
         for (int m = 0; m < M; ++m) v[m] = 0.0f;
-        if (live) {
+        // (kPair) a chunk of 32 live units: two whole rows
+        const bool paired = kPair && c * kChunkUnits + kChunkUnits <= TU;
+        if (paired) {
+            constexpr int MA = (M + 1) / 2, MB = M - MA;
+            const int h = lane >> 4;
+            const uint8_t *w0 = ring + slot * L.slotbytes + (lane & 15) * kUnitBytes;   // the chunk's first row
+            const uint8_t *w1 = w0 + 16 * kUnitBytes;                                   // its second row
+            const uint8_t *ab = act0 + (h ? MA : 0) * L.act_m_stride + uin * kActUnitStride;
+            // half 1 holds MB <= MA rows: its missing row re-reads its last one (discarded)
+            const uint32_t ast = (h && MB < MA) ? 0u : L.act_m_stride;
+            float p0[MA], p1[MA];
+#pragma unroll
+            for (int k = 0; k < MA; ++k) p0[k] = p1[k] = 0.0f;
+            q4_unit<MA, false>(w0, ab, ast, p0, nullptr, 0);
+            q4_unit<MA, false>(w1, ab, ast, p1, nullptr, 0);
+            // half 0 keeps the first row's activation rows 0..MA-1 and receives MA..M-1;
+            // half 1 keeps the second row's MA..M-1 and receives 0..MA-1
+#pragma unroll
+            for (int k = 0; k < MA; ++k) {
+                const float got = __shfl_xor_sync(0xffffffffu, h ? p0[k] : p1[k], 16);
+                if (h) {
+                    v[k] = got;
+                    if (k < MB) v[MA + k] = p1[k];
+                } else {
+                    v[k] = p0[k];
+                    if (k < MB) v[MA + k] = got;
+                }
+            }
+        } else if (live) {
             const uint8_t *wu = ring + slot * L.slotbytes + lane * kUnitBytes;
             int32_t *du = kDots ? dots + (r0 + rr) * nb + 8 * uin : nullptr;
             if constexpr (kActRegs && M == 2)
@@ -695,6 +727,8 @@ cudaError_t launch_m(const Q4Plan &p, const Q4Group &grp, int32_t *dots, int64_t
         auto kern = q4_0_stream_kernel<M, kDots, kFused, kQ4K>;
         if constexpr ((M == 1 || (M == 2 && !kQ4K)) && !kDots)
             if (p.act_regs) kern = q4_0_stream_kernel<M, kDots, kFused, kQ4K, true>;
+        if constexpr (M >= 2 && M <= 4 && !kQ4K && !kDots)
+            if (p.pair) kern = q4_0_stream_kernel<M, kDots, kFused, kQ4K, false, true>;
         cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kern), p.smem_bytes);
         if (e != cudaSuccess) return e;
         cfg.blockDim = dim3(static_cast<unsigned>(p.warps * 32));   // consumers + the producer
@@ -740,6 +774,7 @@ cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t 
     plan->round = 0;
     plan->smem_bytes = 0;
     plan->act_regs = false;
+    plan->pair = false;
     plan->grid = static_cast<int>((N + kWarps - 1) / kWarps);
     if (!aligned || K % 256 != 0) return cudaSuccess;
     // from a few activation rows on, the tensor cores
@@ -776,12 +811,20 @@ cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t 
             S = S2;
         }
     }
+    // Q4_0 at M = 4 with rows of 16 units (K = 4096): lane pairs share activation
+    // records, half the shared-memory reads of them (Llama-3-8B MLP 2116 -> 2401 GB/s).
+    // At M = 3 the odd split adds a third more dot work and gains nothing; at M = 2 the
+    // records fit in registers. QMV_Q4_PAIR=1 forces it at M = 2..3, 0 disables it.
+    const int pair_env = env_int("QMV_Q4_PAIR", -1);
+    const bool pair = !act_regs && !q4k && M >= 2 && M <= 4 && U == 16 &&
+                      (pair_env < 0 ? M == 4 : pair_env != 0);
     const int per_sm = std::max(1, std::min(4, env_int("QMV_Q4_CTAS_PER_SM", 1)));
     const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>((N + warps - 1) / warps,
                                                                  static_cast<int64_t>(dev.sm_count) * per_sm));
     if ((N / (ctas * warps) + 1) * (K / 256) >= (int64_t(1) << 31)) return cudaSuccess;   // 32-bit unit counters
     plan->route = kRouteQ4_0Stream;
     plan->act_regs = act_regs;
+    plan->pair = pair;
     plan->warps = warps;
     plan->stages = S;
     plan->prefetch = std::max(0, std::min(S * warps, env_int("QMV_Q4_PREFETCH", 4)));

@@ -53,7 +53,8 @@ struct Q4Plan {
     int round;         // tensor-core kernel: tiles per reduction round
     int grid;
     int smem_bytes;
-    bool act_regs;     // streaming kernel, M = 1: activation record in registers (rows of U | 32 units)
+    bool act_regs;     // streaming kernel, M <= 2: activation records in registers (rows of U | 32 units)
+    bool pair;         // streaming kernel, Q4_0 M = 2..4, rows of 16 units: lane pairs share records
 };
 
 // Programmatic dependent launch (opt-in, qmv_set_launch_overlap): fills attr[0]

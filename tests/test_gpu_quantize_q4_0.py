@@ -419,3 +419,29 @@ def test_large_k_routes_and_parity(q):
     from gemm_qmv_quantize_gb300 import QmvError
     with pytest.raises(QmvError, match="QMV_ERR_SHAPE"):
         q.qmv_q4_0_q8_1_fused(w, synth.activations_f32(8, K, seed=90, device=DEV))
+
+
+# ---------------------------------------------------------------- lane pairs sharing activation records
+
+@pytest.mark.parametrize("M", [2, 3, 4])
+@pytest.mark.parametrize("fused", [False, True])
+def test_q4_0_lane_pairs_bit_identical(q, monkeypatch, M, fused):
+    """K = 4096, enough rows that warps see whole two-row chunks (and an odd last row):
+    the lane-pair path gives every output bit-identical to the path that reads all M
+    records per lane (the same per-unit arithmetic), and within the bound."""
+    synth = _synth()
+    N, K = 16 * 1216 + 37, 4096
+    w = synth.q4_0_weights(N, K, seed=500 + M, device=DEV)
+    x = synth.activations_f32(M, K, seed=510 + M, device=DEV)
+    xq = q.qmv_quantize_q8_1(x)
+    run = (lambda: q.qmv_q4_0_q8_1_fused(w, x)) if fused else (lambda: q.qmv_q4_0_q8_1(w, xq, K))
+    monkeypatch.setenv("QMV_Q4_ACT_REGS_M2", "0")   # M = 2 through the pairs too
+    monkeypatch.setenv("QMV_Q4_MMA_MIN_M", "9")
+    ys = []
+    for pair in ("1", "0"):   # forced on at M = 2..3 too
+        monkeypatch.setenv("QMV_Q4_PAIR", pair)
+        ys.append(run())
+    assert torch.equal(ys[0], ys[1])
+    rows = synth.sample_rows(N, 48, seed=M).numpy()
+    y_ref, bound = oracle.q4_0_q8_1(np.ascontiguousarray(w.cpu().numpy()[rows]), xq.cpu().numpy(), K)
+    assert_close(f"lane pairs M={M}", ys[0].cpu().numpy()[:, rows], y_ref, bound)
