@@ -546,10 +546,12 @@ __global__ void __launch_bounds__(kActRegs ? (M == 1 ? kActRegsThreads : kStream
     float carry[M];   // partial sum of the row left open by the previous chunk
 #pragma unroll
     for (int m = 0; m < M; ++m) carry[m] = 0.0f;
-    ActRegs ar[kActRegs ? M : 1];
+    // register-resident records: rows 0 .. kRegRows-1 (M = 3: rows 0, 1; row 2 from shared memory)
+    constexpr int kRegRows = kActRegs ? (M < 3 ? M : 2) : 1;
+    ActRegs ar[kRegRows];
     if (kActRegs) {   // uin never changes (du == 0)
 #pragma unroll
-        for (int m = 0; m < (kActRegs ? M : 1); ++m) load_act_regs(act0 + m * L.act_m_stride + uin * kActUnitStride, ar[m]);
+        for (int m = 0; m < kRegRows; ++m) load_act_regs(act0 + m * L.act_m_stride + uin * kActUnitStride, ar[m]);
     }
     int slot = 0;
     uint32_t phase = 0;
@@ -598,7 +600,15 @@ __global__ void __launch_bounds__(kActRegs ? (M == 1 ? kActRegsThreads : kStream
         } else if (live) {
             const uint8_t *wu = ring + slot * L.slotbytes + lane * kUnitBytes;
             int32_t *du = kDots ? dots + (r0 + rr) * nb + 8 * uin : nullptr;
-            if constexpr (kActRegs && M == 2)
+            if constexpr (kActRegs && M == 3) {
+                float v2[2];
+                q4_unit_regs2(wu, ar, v2);
+                v[0] = v2[0];
+                v[1] = v2[1];
+                float v3[1] = {0.0f};
+                q4_unit<1, false>(wu, act0 + 2 * L.act_m_stride + uin * kActUnitStride, 0u, v3, nullptr, 0);
+                v[2] = v3[0];
+            } else if constexpr (kActRegs && M == 2)
                 q4_unit_regs2(wu, ar, v);
             else if (kActRegs)
                 v[0] = kQ4K ? q4k_unit_regs(wu, ar[0]) : q4_unit_regs(wu, ar[0]);
@@ -725,7 +735,7 @@ cudaError_t launch_m(const Q4Plan &p, const Q4Group &grp, int32_t *dots, int64_t
     cfg.numAttrs = set_launch_overlap_attr(attr);
     if (p.route == kRouteQ4_0Stream) {
         auto kern = q4_0_stream_kernel<M, kDots, kFused, kQ4K>;
-        if constexpr ((M == 1 || (M == 2 && !kQ4K)) && !kDots)
+        if constexpr ((M == 1 || ((M == 2 || M == 3) && !kQ4K)) && !kDots)
             if (p.act_regs) kern = q4_0_stream_kernel<M, kDots, kFused, kQ4K, true>;
         if constexpr (M >= 2 && M <= 4 && !kQ4K && !kDots)
             if (p.pair) kern = q4_0_stream_kernel<M, kDots, kFused, kQ4K, false, true>;
@@ -798,8 +808,10 @@ cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t 
     bool act_regs = false;
     const int U = static_cast<int>(K / 256);
     // M = 2 (Q4_0): two records, 215 registers, 8 warps with 4-slot rings (Llama-3-8B
-    // MLP 3218 -> 3264 GB/s)
-    const bool m2 = M == 2 && !q4k && env_int("QMV_Q4_ACT_REGS_M2", 1) != 0;
+    // MLP 3218 -> 3264 GB/s). M = 3 (Q4_0): rows 0 and 1 in registers, row 2 read from
+    // shared memory, 231 registers (Llama-3-8B MLP 2556 -> 2840 GB/s)
+    const bool m2 = (M == 2 && !q4k && env_int("QMV_Q4_ACT_REGS_M2", 1) != 0) ||
+                    (M == 3 && !q4k && env_int("QMV_Q4_ACT_REGS_M3", 1) != 0);
     if ((M == 1 || m2) && U <= 32 && 32 % U == 0 && env_int("QMV_Q4_ACT_REGS", 1) != 0) {
         const int wcap = M == 1 ? kActRegsThreads / 32 : kStreamThreadsWide / 32;
         int w2 = std::min(warps, std::max(1, std::min(wcap, env_int("QMV_Q4_ACT_REGS_WARPS", 16))));

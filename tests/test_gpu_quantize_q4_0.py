@@ -445,3 +445,23 @@ def test_q4_0_lane_pairs_bit_identical(q, monkeypatch, M, fused):
     rows = synth.sample_rows(N, 48, seed=M).numpy()
     y_ref, bound = oracle.q4_0_q8_1(np.ascontiguousarray(w.cpu().numpy()[rows]), xq.cpu().numpy(), K)
     assert_close(f"lane pairs M={M}", ys[0].cpu().numpy()[:, rows], y_ref, bound)
+
+
+@pytest.mark.parametrize("fused", [False, True])
+def test_q4_0_m3_register_records_bit_identical(q, monkeypatch, fused):
+    """M = 3, K = 4096 with two of the three activation records in registers: every
+    output bit-identical to the all-shared-memory path, and within the bound."""
+    synth = _synth()
+    M, N, K = 3, 16 * 1216 + 37, 4096
+    w = synth.q4_0_weights(N, K, seed=530, device=DEV)
+    x = synth.activations_f32(M, K, seed=531, device=DEV)
+    xq = q.qmv_quantize_q8_1(x)
+    run = (lambda: q.qmv_q4_0_q8_1_fused(w, x)) if fused else (lambda: q.qmv_q4_0_q8_1(w, xq, K))
+    ys = []
+    for on in ("1", "0"):
+        monkeypatch.setenv("QMV_Q4_ACT_REGS_M3", on)
+        ys.append(run())
+    assert torch.equal(ys[0], ys[1])
+    rows = synth.sample_rows(N, 48, seed=3).numpy()
+    y_ref, bound = oracle.q4_0_q8_1(np.ascontiguousarray(w.cpu().numpy()[rows]), xq.cpu().numpy(), K)
+    assert_close("M = 3 register records", ys[0].cpu().numpy()[:, rows], y_ref, bound)
