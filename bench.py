@@ -130,6 +130,8 @@ WORKLOADS["q4_0_4096sq_m1"] = dict(M=1, mats=lambda: [("q4_0", 4096, 4096)] * 48
                                    desc="Q4_0 GEMV M=1, N=K=4096, 48 rotated copies")
 WORKLOADS["q4_0_11008x4096_m1"] = dict(M=1, mats=lambda: [("q4_0", 11008, 4096)] * 16,
                                        desc="Q4_0 GEMV M=1, 11008x4096, 16 rotated copies")
+WORKLOADS["q4_0_4096x11008_m1"] = dict(M=1, mats=lambda: [("q4_0", 4096, 11008)] * 16,
+                                       desc="Q4_0 GEMV M=1, 4096x11008 (Llama-2-7B down), 16 rotated copies")
 WORKLOADS["q4_0_14336x4096_m8"] = dict(M=8, mats=lambda: [("q4_0", 14336, 4096)] * 8,
                                        desc="Q4_0 M=8, 14336x4096 (Llama-3-8B gate), 8 rotated copies")
 WORKLOADS["q4_k_12288x4096_m1"] = dict(M=1, mats=lambda: [("q4_k", 12288, 4096)] * 16,
