@@ -64,6 +64,26 @@ def test_workload_tables():
     dense = bench.dense_27b_stack(False)
     assert sum(bench.weight_bytes(*m) for m in dense) == 11_890_851_840
     assert sum(1 for f, _, _ in mixed if f == "fp8") == 32
+    qwen = bench.qwen3_8b_stack()   # 36 x {q, o 4096^2; k, v 1024x4096; gate/up/down 12288x4096} + lm_head
+    weights = 36 * (2 * 4096 ** 2 + 2 * 1024 * 4096 + 3 * 12288 * 4096) + 151936 * 4096
+    assert sum(bench.weight_bytes(*m) for m in qwen) == weights * 144 // 256 == 4_257_054_720
+    st = bench.qwen3_8b_stages()
+    assert len(st) == 145 and sorted(i for s in st for i in s) == list(range(len(qwen)))
+    mlp = bench.llama3_8b_mlp()     # one copy: 99,090,432 bytes
+    assert sum(bench.weight_bytes(*m) for m in mlp) == 99_090_432 * bench.MLP_COPIES
+    st = bench.llama3_8b_mlp_stages()
+    assert sorted(i for s in st for i in s) == list(range(len(mlp)))
+
+
+def test_every_workload_outgrows_l2():
+    """Timing hygiene: no workload's weights fit in the 129 MB L2, so repeated steps
+    stream from HBM (the single shapes and the MLP rotate copies, three L2s' worth)."""
+    for name, w in bench.WORKLOADS.items():
+        nbytes = sum(bench.weight_bytes(*m) for m in w["mats"]())
+        assert nbytes > 2 * bench.L2_BYTES, name
+        assert "129 MB" in bench.l2_note(nbytes)
+    with pytest.raises(ValueError):
+        bench.l2_note(99_090_432)
 
 
 @pytest.mark.timeout(600)
