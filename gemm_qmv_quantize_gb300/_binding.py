@@ -55,6 +55,7 @@ SIGNATURES = {
     "qmv_route_launches": (_i64, [_i32]),
     "qmv_route_reset": (None, []),
     "qmv_error_flags": (_i32, [ctypes.POINTER(ctypes.c_uint32), _i32]),
+    "qmv_debug_wait_bound": (_i32, [_vp, _vp]),
 }
 
 
@@ -273,6 +274,17 @@ def qmv_q4_k_q8_1_group(ws, xqs, K: int, outs=None, stream=None):
 def qmv_q4_k_q8_1_fused_group(ws, xs, outs=None, stream=None):
     """Several independent fused Q4_K calls (same M, K) in one launch."""
     return _q4_k_group("qmv_q4_k_q8_1_fused_group", ws, xs, xs[0].shape[1], True, outs, stream)
+
+
+def qmv_debug_wait_bound(out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """int64 [2] on the current device: [1 if the bounded wait completed else 0,
+    nanoseconds waited]; the wait is on an mbarrier nothing completes, so it gives up
+    and sets the timeout bit of error_flags()."""
+    if out is None:
+        out = torch.full((2,), -1, dtype=torch.int64, device="cuda")
+    _need(out, "out", torch.int64, (2,))
+    _check("qmv_debug_wait_bound", lib().qmv_debug_wait_bound(out.data_ptr(), _stream(stream)))
+    return out
 
 
 def qmv_debug_q4_k_block_dots(w: torch.Tensor, xq: torch.Tensor, K: int, out: torch.Tensor | None = None,

@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "qmv.h"
+#include "qmv_device.cuh"
 #include "qmv_internal.h"
 
 namespace qmv {
@@ -38,6 +39,33 @@ qmv_status check_shape(int M, int64_t N, int64_t K, int64_t kblock, int max_m = 
     if (M < 0 || M > max_m || N < 0 || K < 0 || N > kMaxDim || K > kMaxDim) return QMV_ERR_SHAPE;
     if (kblock > 1 && K % kblock != 0) return QMV_ERR_SHAPE;
     return QMV_OK;
+}
+
+// Error word of the wait-bound self-check below (OR-ed into qmv_error_flags).
+__device__ uint32_t g_abi_error;
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// One thread waits, with the bounded wait of the streaming kernels, on an mbarrier
+// that expects one arrival nobody makes: the wait must give up, flag the error word
+// and return. out[0] = 1 if the wait completed (never expected), else 0; out[1] =
+// nanoseconds spent in the wait.
+__global__ void wait_bound_kernel(int64_t *out)
+{
+    __shared__ __align__(8) uint64_t bar;
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+    const uint64_t t0 = globaltimer_ns();
+    const bool done = mbar_wait_sleep(&bar, 0);
+    const uint64_t t1 = globaltimer_ns();
+    out[0] = done ? 1 : 0;
+    out[1] = static_cast<int64_t>(t1 - t0);
+    if (!done) atomicOr(&g_abi_error, kErrWaitTimeout);
 }
 
 qmv_status zero_fill(float *y, int M, int64_t N, cudaStream_t s)
@@ -439,12 +467,25 @@ qmv_status qmv_error_flags(uint32_t *flags, int clear)
 {
     if (!flags) return QMV_ERR_NULL;
     if (cudaDeviceSynchronize() != cudaSuccess) return QMV_ERR_CUDA;
-    uint32_t w = 0, w2 = 0, w3 = 0;
+    uint32_t w = 0, w2 = 0, w3 = 0, w4 = 0;
     if (read_error_word_q4_0(&w, clear != 0) != cudaSuccess) return QMV_ERR_CUDA;
     if (read_error_word_wq(&w2, clear != 0) != cudaSuccess) return QMV_ERR_CUDA;
     if (read_error_word_q4_0_mma(&w3, clear != 0) != cudaSuccess) return QMV_ERR_CUDA;
-    *flags = w | w2 | w3;
+    if (cudaMemcpyFromSymbol(&w4, g_abi_error, sizeof(uint32_t)) != cudaSuccess) return QMV_ERR_CUDA;
+    if (clear) {
+        const uint32_t zero = 0;
+        if (cudaMemcpyToSymbol(g_abi_error, &zero, sizeof(uint32_t)) != cudaSuccess) return QMV_ERR_CUDA;
+    }
+    *flags = w | w2 | w3 | w4;
     return QMV_OK;
+}
+
+qmv_status qmv_debug_wait_bound(int64_t *out, qmv_stream_t stream)
+{
+    if (!out) return QMV_ERR_NULL;
+    if (misaligned(out, alignof(int64_t))) return QMV_ERR_ALIGN;
+    wait_bound_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(out);
+    return from_cuda(cudaGetLastError());
 }
 
 }  // extern "C"

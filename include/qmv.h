@@ -283,6 +283,21 @@ QMV_API void qmv_route_reset(void);
  */
 QMV_API qmv_status qmv_error_flags(uint32_t *flags, int clear);
 
+/*
+ * Self-check of the bounded device-side wait that every streaming kernel uses on
+ * its mbarriers: one thread waits on an mbarrier that nothing completes, so the
+ * wait must give up after its bound, set the timeout bit (1) of the error word and
+ * return, leaving the context usable. The bound is 2000 suspending try-waits with
+ * a 1 ms hint each: at most about 2 s; on a GB300 each returns after about 3.8 us,
+ * so the wait gives up after about 7.6 ms of waiting.
+ *   out  DEVICE int64 [2], 8-byte aligned, owned by the caller: out[0] = 1 if the
+ *        wait completed (never expected), 0 if it gave up; out[1] = nanoseconds
+ *        spent waiting (%globaltimer).
+ * Asynchronous on `stream`. Returns QMV_ERR_NULL / QMV_ERR_ALIGN for a bad `out`,
+ * QMV_ERR_CUDA if the launch fails.
+ */
+QMV_API qmv_status qmv_debug_wait_bound(int64_t *out, qmv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -211,6 +211,11 @@ def test_error_flags_null(lib):
     assert lib.qmv_error_flags(None, 0) == NULL
 
 
+def test_wait_bound_validation(lib):
+    assert lib.qmv_debug_wait_bound(None, None) == NULL
+    assert lib.qmv_debug_wait_bound(P + 4, None) == ALIGN
+
+
 def test_binding_raises_loudly_when_library_missing(monkeypatch, tmp_path):
     from gemm_qmv_quantize_gb300 import _binding
     monkeypatch.setattr(_binding, "_LIB_PATH", str(tmp_path / "missing.so"))
