@@ -1,7 +1,7 @@
 """Planted mistakes: each mutant is a copy of the oracle source with one
 plausible error (a swapped nibble half, a dropped offset, a wrong scale group,
 a transposed operand, ties to even instead of away from zero, an off-by-one
-exponent bias). The oracle's pin tests must fail on every one of them.
+exponent bias, a signed maximum, a dropped global scale, a 5-bit mask). The oracle's pin tests must fail on every one of them.
 
 The mistakes are planted in a temporary copy of the oracle on the CPU; the
 oracle itself is never modified.
@@ -50,6 +50,16 @@ MUTANTS = {
                                   "(r % 2 == 0) ? (qs[32 * c + r / 2] & 0x0f) : (qs[32 * c + r / 2] >> 4)"),
     "q4k_sub_block_of_next": ("oracle_q4_k_scale_min(blk + 4, i / 32, &sc, &mn);",
                               "oracle_q4_k_scale_min(blk + 4, (i / 32 + 1) % 8, &sc, &mn);"),
+    "q8_amax_signed": ("float a = fabsf(xb[i]);", "float a = xb[i];"),
+    "q8_scale_over_128": ("float d = amax / 127.0f;", "float d = amax / 128.0f;"),
+    "q4_block_sum_t_drops_last": ("for (int j = 0; j < 32; ++j) t += q8[j];",
+                                  "for (int j = 0; j < 31; ++j) t += q8[j];"),
+    "nvfp4_global_scale_dropped": ("* (double)g;", "* 1.0;"),
+    "fp8_row_scale_of_next_row": ("(double)rs[n]", "(double)rs[(n + 1) % N]"),
+    "e4m3_subnormal_unit": ("if (e == 0) v = ldexp((double)m, -9);", "if (e == 0) v = ldexp((double)m, -10);"),
+    "q4k_min_high_bits_from_wrong_byte": ("*mn = (p[j + 4] >> 4) | ((p[j] >> 6) << 4);",
+                                          "*mn = (p[j + 4] >> 4) | ((p[j - 4] >> 6) << 4);"),
+    "q4k_scale_five_bits": ("*sc = p[j] & 63;", "*sc = p[j] & 31;"),
     "fp8_x_transposed": ("double xv = oracle_fp16_to_double(x[m * K + k]);\n                acc += wv * xv;\n                mag += fabs(wv * xv);\n            }\n            y[m * N + n] = acc;\n            bound[m * N + n] = mag;\n        }\n    }\n}\n",
                          "double xv = oracle_fp16_to_double(x[(k * M + m) % (M * K)]);\n                acc += wv * xv;\n                mag += fabs(wv * xv);\n            }\n            y[m * N + n] = acc;\n            bound[m * N + n] = mag;\n        }\n    }\n}\n"),
 }
