@@ -548,7 +548,8 @@ def _run_ours_on_stream(args, rank, world, local_rank, stack, stream, barrier, m
     line = {
         "metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(stack), "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": dtype_of(stack)[0],
+        "dtype_detail": dtype_of(stack)[1], "data": "synthetic",
         "hbm_frac": round(gbs / world / peak, 4), "hbm_peak_gbs": peak, "hbm_peak_kind": peak_kind,
         "tok_per_s": round(stack.M * world / step_s, 1),
         "config": {"workload": stack.name, "desc": WORKLOADS[stack.name]["desc"], "M": stack.M,
@@ -571,10 +572,11 @@ def _run_ours_on_stream(args, rank, world, local_rank, stack, stream, barrier, m
 
 
 def dtype_of(stack):
+    """(arithmetic type of the products, what the path computes in detail)."""
     fmts = {f for f, _, _ in stack.mats}
     if fmts <= {"q4_0", "q4_k"}:
-        return "int8 dp4a (int32 block sums) + fp32 scale/accumulate"
-    return "fp16 x fp16 tensor-core MMA, fp32 accumulate (exact fp16 decode of e2m1/e4m3)"
+        return "int8", "int8 x int8 block dots in int32 (dp4a / m16n8k32), fp32 scale and accumulate"
+    return "fp16", "fp16 x fp16 tensor-core MMA (m16n8k16), fp32 accumulate; e2m1/e4m3 decode to fp16 is exact"
 
 
 def kernel_roofline(args, stack, stream, barrier, step_s=None):
@@ -786,7 +788,7 @@ def run_reference(args, rank, world):
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "tok_per_s": round(w["M"] / step_s, 4),
         "config": {"workload": args.workload, "desc": w["desc"], "M": w["M"]},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
