@@ -1,0 +1,116 @@
+"""Integer identities behind the MMVQ kernels, checked on the CPU with a plain
+emulation of the instructions (PTX ISA semantics) against the oracle's exact block
+sums S = sum q4u * q8 and T = sum q8.
+
+- "Machine Learning on NVIDIA CMP", section "The DP2A patch": one 4-way int8 dot
+  equals a 2-way dot over bytes 0..1 plus one over bytes 2..3 of B, once A's four
+  bytes are widened to int16 by two sign-replicating byte permutes.
+- The dp4a streaming kernel: unsigned low nibbles (mask 0x0f) and high nibbles kept
+  in place (mask 0xf0, i.e. 16 q) against signed Q8_1 bytes, so S = lo + hi / 16
+  exactly, and a block's dot is S - 8 T.
+- The int8 tensor-core kernel: the weight bytes 16 (q - 8) as int8, formed as
+  (nibble << 4) ^ 0x80, so a block's product is 16 (S - 8 T) exactly in int32.
+"""
+import numpy as np
+import pytest
+
+import oracle
+
+
+def _u8(w):
+    w = np.asarray(w, dtype=np.uint32)
+    return [((w >> (8 * i)) & 0xFF).astype(np.int64) for i in range(4)]
+
+
+def _s8(w):
+    return [np.where(b >= 128, b - 256, b) for b in _u8(w)]
+
+
+def dp4a(a, b, c, a_signed=True):
+    """dp4a.{s32|u32}.s32: c + sum_i a.byte[i] * b.byte[i], b signed."""
+    av = _s8(a) if a_signed else _u8(a)
+    bv = _s8(b)
+    return c + sum(x * y for x, y in zip(av, bv))
+
+
+def prmt(a, b, sel):
+    """prmt.b32 default mode: result byte i = byte (sel nibble i & 7) of {b, a}
+    (a = bytes 0..3, b = bytes 4..7), or that byte's sign bit replicated when the
+    nibble's bit 3 is set."""
+    src = _u8(a) + _u8(b)
+    out = np.zeros_like(np.asarray(a, dtype=np.int64))
+    for i in range(4):
+        nib = (sel >> (4 * i)) & 0xF
+        byte = src[nib & 7]
+        if nib & 8:
+            byte = np.where(byte & 0x80, 0xFF, 0x00)
+        out |= byte << (8 * i)
+    return out
+
+
+def dp2a(a, b, c, hi):
+    """dp2a.{lo|hi}.s32.s32: c + a.half[0] * b.byte[o] + a.half[1] * b.byte[o + 1],
+    o = 2 for .hi, 0 for .lo; a as two int16, b as four int8."""
+    a = np.asarray(a, dtype=np.int64)
+    h0, h1 = a & 0xFFFF, (a >> 16) & 0xFFFF
+    h0, h1 = np.where(h0 >= 1 << 15, h0 - (1 << 16), h0), np.where(h1 >= 1 << 15, h1 - (1 << 16), h1)
+    bv = _s8(b)
+    o = 2 if hi else 0
+    return c + h0 * bv[o] + h1 * bv[o + 1]
+
+
+def test_dp4a_equals_two_permutes_and_two_dp2a():
+    rng = np.random.default_rng(11)
+    edges = np.array([0, 0x7F7F7F7F, 0x80808080, 0xFFFFFFFF, 0x017F80FF, 0x80FF017F], dtype=np.uint64)
+    a = np.concatenate([rng.integers(0, 1 << 32, 200_000, dtype=np.uint64), np.repeat(edges, len(edges))])
+    b = np.concatenate([rng.integers(0, 1 << 32, 200_000, dtype=np.uint64), np.tile(edges, len(edges))])
+    c = rng.integers(-(1 << 20), 1 << 20, len(a))
+    ref = dp4a(a, b, c)
+    a_lo = prmt(a, 0, 0x9180)   # {(int16) a.byte0, (int16) a.byte1}
+    a_hi = prmt(a, 0, 0xB3A2)   # {(int16) a.byte2, (int16) a.byte3}
+    assert np.array_equal(dp2a(a_hi, b, dp2a(a_lo, b, c, hi=False), hi=True), ref)
+
+
+def test_prmt_widening_is_sign_extension():
+    for byte in range(256):
+        s = byte - 256 if byte >= 128 else byte
+        got = int(prmt(np.array([byte | (byte << 8)]), 0, 0x9180)[0])
+        assert got == ((s & 0xFFFF) | ((s & 0xFFFF) << 16))
+
+
+def _blocks(seed, N=37, M=3, K=1024):
+    from gemm_qmv_quantize_gb300 import synth
+    w = synth.q4_0_weights(N, K, seed=seed).numpy()
+    xq = oracle.quantize_q8_1(synth.activations_f32(M, K, seed=seed + 1).numpy())
+    # extreme activation blocks: all +127 and all -127 quants
+    xq[0, 4:36] = 127
+    xq[1, 40:72] = np.uint8(129)   # -127
+    S, T = oracle.q4_0_block_dots(w, xq, K)
+    nb = K // 32
+    qs = w.reshape(N, nb, 18)[:, :, 2:].copy().view("<u4")     # [N][nb][4] words of nibbles
+    q8 = xq.reshape(M, nb, 36)[:, :, 4:].copy().view("<u4")    # [M][nb][8] words of int8
+    return qs.astype(np.uint64), q8.astype(np.uint64), S.astype(np.int64), T.astype(np.int64)
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_stream_kernel_block_dot(seed):
+    qs, q8, S, T = _blocks(seed)
+    lo = sum(dp4a(qs[None, :, :, i] & 0x0F0F0F0F, q8[:, None, :, i], 0, a_signed=False) for i in range(4))
+    hi = sum(dp4a(qs[None, :, :, i] & 0xF0F0F0F0, q8[:, None, :, 4 + i], 0, a_signed=False) for i in range(4))
+    assert np.all(hi % 16 == 0)                       # the kept-in-place high nibbles are 16 q
+    assert np.array_equal(lo + (hi >> 4), S)          # arithmetic shift: exact on multiples of 16
+    assert np.array_equal(lo + (hi >> 4) - 8 * T[:, None, :], S - 8 * T[:, None, :])
+
+
+@pytest.mark.parametrize("seed", [4, 5])
+def test_tensor_core_kernel_bytes(seed):
+    qs, q8, S, T = _blocks(seed)
+    f_lo = ((qs << 4) & 0xF0F0F0F0) ^ 0x80808080      # int8 bytes 16 (q_lo - 8)
+    f_hi = (qs & 0xF0F0F0F0) ^ 0x80808080             # int8 bytes 16 (q_hi - 8)
+    for i in range(4):                                # byte 0 of each word: its low nibble q
+        q = (qs[..., i] & 0xF).astype(np.int64)
+        assert np.array_equal(_s8(f_lo[..., i])[0], 16 * (q - 8))
+    D = sum(dp4a(f_lo[None, :, :, i], q8[:, None, :, i], 0) + dp4a(f_hi[None, :, :, i], q8[:, None, :, 4 + i], 0)
+            for i in range(4))
+    assert np.array_equal(D, 16 * (S - 8 * T[:, None, :]))
+    assert np.abs(D).max() < 1 << 31                  # fits the int32 accumulator
