@@ -1,5 +1,6 @@
 """GB300 (sm_103a) weight-only-quantized skinny matmul: Q8_1 activation quantizer,
-Q4_0 and Q4_K x Q8_1 MMVQ at M = 1..8, NVFP4 W4A16 and FP8 W8A16 at M = 1..16.
+Q4_0 and Q4_K x Q8_1 MMVQ at M = 1..8, NVFP4 W4A16 and FP8 W8A16 at M = 1..96 (one
+weight pass per chunk of at most 16 rows).
 
 The compute lives in the C-ABI CUDA library ``_build/libqmv.so`` (declared in
 ``include/qmv.h``); this package is its thin Python binding. Seeded synthetic

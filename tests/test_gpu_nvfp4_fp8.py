@@ -2,7 +2,7 @@
 
 fp32 outputs within |y - y_ref| <= 1e-3 * sum|w*x| + 1e-6 on: several tiles with
 a ragged tail at M = 1..16 (rows 9..16 as a second activation tile of the same
-weight pass); the full-size matrices of the 27B-class dense stack
+weight pass) and chunked M up to 96; the full-size matrices of the 27B-class dense stack
 and its 151936-row lm_head (sampled rows); fp16 activation outliers up to
 6e4 (the overflow case of "v100-skinny README", section "How QPN works");
 zero scales; K that is not a multiple of the streaming step (generic kernel).
