@@ -56,6 +56,7 @@ SIGNATURES = {
     "qmv_route_reset": (None, []),
     "qmv_error_flags": (_i32, [ctypes.POINTER(ctypes.c_uint32), _i32]),
     "qmv_debug_wait_bound": (_i32, [_vp, _vp]),
+    "qmv_debug_plan_q4": (_i32, [_i32, _i32, _i64, _i64, _i32, _i32, _i32, _i32, _i32, _vp]),
 }
 
 
@@ -285,6 +286,24 @@ def qmv_debug_wait_bound(out: torch.Tensor | None = None, stream=None) -> torch.
     _need(out, "out", torch.int64, (2,))
     _check("qmv_debug_wait_bound", lib().qmv_debug_wait_bound(out.data_ptr(), _stream(stream)))
     return out
+
+
+PLAN_FIELDS = ("route", "warps", "slots", "grid", "smem_bytes", "act_regs", "pair", "chunk_units")
+GB300_DEVICE = dict(sm_count=152, smem_optin=232448, smem_per_sm=233472)
+
+
+def qmv_debug_plan_q4(M: int, N: int, K: int, q4k: bool = False, n_inputs: int = 1, w_align16: bool = True,
+                      sm_count: int = GB300_DEVICE["sm_count"], smem_optin: int = GB300_DEVICE["smem_optin"],
+                      smem_per_sm: int = GB300_DEVICE["smem_per_sm"]) -> dict:
+    """The Q4_0 / Q4_K launch plan for one call on the given device (GB300 by
+    default), as a dict of PLAN_FIELDS with the route as its name. No GPU needed for
+    the streaming-kernel plans."""
+    out = (ctypes.c_int64 * 8)()
+    _check("qmv_debug_plan_q4", lib().qmv_debug_plan_q4(int(bool(q4k)), M, N, K, n_inputs, int(bool(w_align16)),
+                                                        sm_count, smem_optin, smem_per_sm, out))
+    plan = dict(zip(PLAN_FIELDS, (int(v) for v in out)))
+    plan["route"] = lib().qmv_route_name(plan["route"]).decode()
+    return plan
 
 
 def qmv_debug_q4_k_block_dots(w: torch.Tensor, xq: torch.Tensor, K: int, out: torch.Tensor | None = None,

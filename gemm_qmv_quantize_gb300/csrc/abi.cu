@@ -480,6 +480,38 @@ qmv_status qmv_error_flags(uint32_t *flags, int clear)
     return QMV_OK;
 }
 
+qmv_status qmv_debug_plan_q4(int q4k, int M, int64_t N, int64_t K, int n_inputs, int w_align16, int sm_count,
+                             int smem_optin, int smem_per_sm, int64_t *out)
+{
+    if (!out) return QMV_ERR_NULL;
+    qmv_status st = check_shape(M, N, K, q4k ? 256 : 32);
+    if (st != QMV_OK) return st;
+    if (M < 1 || N < 1 || K < 1 || n_inputs < 1 || n_inputs > kMaxGroup || N < n_inputs || sm_count < 1 ||
+        smem_optin < 1 || smem_per_sm < 1)
+        return QMV_ERR_SHAPE;
+    const DeviceInfo dev{0, sm_count, smem_optin, smem_per_sm};
+    // n_inputs matrices of N / n_inputs rows, each reading its own activation; the
+    // plan looks only at the weights' alignment, the rows and the distinct inputs
+    Q4Group g{};
+    g.count = n_inputs;
+    g.nx = n_inputs;
+    const uintptr_t base = w_align16 ? 0x10000u : 0x10002u;
+    for (int i = 0; i <= n_inputs; ++i) g.row_start[i] = N * i / n_inputs;
+    for (int i = 0; i < n_inputs; ++i) {
+        g.xslot[i] = i;
+        g.w[i] = reinterpret_cast<const uint8_t *>(base);
+    }
+    Q4Plan plan{};
+    if (plan_q4_0(dev, g, M, K, &plan, q4k != 0) != cudaSuccess) return QMV_ERR_CUDA;
+    int route = plan.route;
+    if (q4k && route == kRouteQ4_0Stream) route = kRouteQ4KStream;
+    if (q4k && route == kRouteQ4_0Mma) route = kRouteQ4KMma;
+    const int64_t v[8] = {route, plan.warps, plan.stages, plan.grid, plan.smem_bytes, plan.act_regs ? 1 : 0,
+                          plan.pair ? 1 : 0, plan.chunk_units};
+    for (int i = 0; i < 8; ++i) out[i] = v[i];
+    return QMV_OK;
+}
+
 qmv_status qmv_debug_wait_bound(int64_t *out, qmv_stream_t stream)
 {
     if (!out) return QMV_ERR_NULL;

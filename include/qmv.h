@@ -265,6 +265,27 @@ QMV_API qmv_status qmv_debug_q4_k_block_dots(const void *w, const void *xq, int3
                                              int64_t K, qmv_stream_t stream);
 
 /*
+ * The launch plan the Q4_0 / Q4_K heuristic picks for one call on a device given
+ * by its SM count and shared-memory limits. The streaming-kernel plans need no
+ * CUDA call (usable without a GPU); the tensor-core kernel's plan (M >= 5 unless
+ * QMV_Q4_MMA_MIN_M / QMV_Q4K_MMA_MIN_M move the threshold) queries the current
+ * device's occupancy and returns QMV_ERR_CUDA without one.
+ *   q4k          0 = Q4_0 (K % 32 == 0), 1 = Q4_K (K % 256 == 0).
+ *   M, N, K      as in qmv_q4_0_q8_1 (M 1..8, N >= n_inputs, K > 0); N rows in all.
+ *   n_inputs     1..8 matrices of N / n_inputs rows, each with its own activation.
+ *   w_align16    1 if the weights start on 16-byte boundaries, else 0.
+ *   sm_count, smem_optin, smem_per_sm  the device (GB300: 152, 232448, 233472).
+ *   out          HOST int64 [8]: route (a qmv_route_name index), warps per CTA,
+ *                ring slots per warp, grid (CTAs), dynamic shared memory bytes,
+ *                activation records in registers (0/1), lane pairs (0/1), and
+ *                144-byte units per ring slot. For Q4_K a q4_0_generic route means that
+ *                no kernel takes the shape (the call returns QMV_ERR_SHAPE).
+ * Returns QMV_ERR_NULL for out == NULL, QMV_ERR_SHAPE for values out of range.
+ */
+QMV_API qmv_status qmv_debug_plan_q4(int q4k, int M, int64_t N, int64_t K, int n_inputs, int w_align16,
+                                     int sm_count, int smem_optin, int smem_per_sm, int64_t *out);
+
+/*
  * Kernel-choice census: a counter per kernel route, bumped on every launch, so a
  * caller can check which kernel served each region and that no fallback ran
  * (the census of "v100-skinny README", "Native mixed-precision checkpoint path").
