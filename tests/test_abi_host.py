@@ -44,6 +44,36 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    """A C99 program (no CUDA headers) that includes include/qmv.h, takes the address
+    of every declared entry point, links against libqmv.so and runs calls that answer
+    before any CUDA call."""
+    import subprocess
+    names = sorted(_declared_symbols())
+    src = tmp_path / "abi_check.c"
+    src.write_text("\n".join([
+        "#include <stdio.h>",
+        '#include "qmv.h"',
+        "typedef void (*fn)(void);",
+        "static const fn every[] = {" + ", ".join(f"(fn){n}" for n in names) + "};",
+        "int main(void) {",
+        "    int bad = 0;",
+        "    if (sizeof every / sizeof every[0] != %d) bad |= 1;" % len(names),
+        "    if (qmv_quantize_q8_1(0, 0, 1, 64, 0) != QMV_ERR_NULL) bad |= 2;",
+        "    if (qmv_q4_0_q8_1((const void *)0x10000, (const void *)0x10000, (float *)0x10000, 9, 64, 4096, 0)"
+        " != QMV_ERR_SHAPE) bad |= 4;",
+        "    if (qmv_route_count() < 1 || !qmv_status_string(QMV_ERR_ALIGN)) bad |= 8;",
+        '    printf("%d\\n", bad);',
+        "    return bad;",
+        "}", ""]))
+    build_dir = os.path.dirname(lib._name)
+    exe = tmp_path / "abi_check"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), str(src),
+                    "-o", str(exe), "-L", build_dir, "-lqmv", f"-Wl,-rpath,{build_dir}"], check=True)
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "0", (r.stdout, r.stderr)
+
+
 def test_binding_table_matches_header():
     from gemm_qmv_quantize_gb300 import _binding
     assert set(_binding.SIGNATURES) == _declared_symbols()
