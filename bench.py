@@ -485,6 +485,24 @@ def timed(replay, steps, barrier, sync):
     return start.elapsed_time(end) * 1e-3
 
 
+def step_spread(replay, n):
+    """Per-step device times of n more replays after the timed region (an event pair
+    around each): median, p10 and p90 in ms. Reported beside the line's value, which
+    comes from the timed region alone."""
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in ev:
+        a.record()
+        replay()
+        b.record()
+    torch.cuda.synchronize()
+    ts = sorted(a.elapsed_time(b) for a, b in ev)
+
+    def pick(f):
+        return round(ts[min(n - 1, int(f * (n - 1) + 0.5))], 4)
+    return {"n": n, "median_ms": pick(0.5), "p10_ms": pick(0.1), "p90_ms": pick(0.9)}
+
+
 def q4_fused(args) -> bool:
     """Q4_0 path: the quantize fused into the MMVQ prologue at M = 1 (every CTA
     quantizes the row: cheaper than a launch); at M >= 2 the two-call path (one
@@ -536,6 +554,10 @@ def _run_ours_on_stream(args, rank, world, local_rank, stack, stream, barrier, m
     step_s = t / args.steps
     gbs = replica_rate(stack.bytes_per_step, step_s, world) / 1e9
     kernels = launches_per_step * args.steps if not args.eager else sum(q.route_counts().values()) - launches0
+    try:
+        spread = step_spread(replay, max(1, min(args.steps, 200)))
+    except RuntimeError as exc:   # a CUDA error here is reported in the line, not fatal to it
+        spread = {"error": str(exc)[:200]}
 
     # dominant kernel: the GEMV of every call, timed per launch with event nodes in the graph
     roof = kernel_roofline(args, stack, stream, barrier, step_s=None if args.eager else step_s)
@@ -563,7 +585,7 @@ def _run_ours_on_stream(args, rank, world, local_rank, stack, stream, barrier, m
                    "schedule": ("one launch per matrix, each after the previous" if len(stack.stages) == len(stack.mats)
                                 else "decode dependency structure: matrices reading the same input share a launch"),
                    "parallelism": f"replicas{world}"},
-        "roofline": roof, "e2e": e2e, "gpu_launches": int(kernels), "clocks": clocks.summary(),
+        "roofline": roof, "e2e": e2e, "step_ms": spread, "gpu_launches": int(kernels), "clocks": clocks.summary(),
         "device_error_flags": err,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -100,3 +100,30 @@ def test_reference_arm_under_torchrun_prints_once():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_step_spread_percentiles(monkeypatch):
+    """The per-step spread reported beside the value: median, p10 and p90 of the
+    event-pair times, here with a stand-in event clock (steps of 1..10 units)."""
+    import torch
+    clock = {"t": 0.0, "k": 0}
+
+    class Ev:
+        def __init__(self, enable_timing=True):
+            self.v = None
+
+        def record(self):
+            clock["t"] += 1.0
+            self.v = clock["t"]
+
+        def elapsed_time(self, other):
+            return other.v - self.v
+
+    def replay():
+        clock["k"] += 1
+        clock["t"] += clock["k"] % 10
+
+    monkeypatch.setattr(torch.cuda, "Event", Ev)
+    monkeypatch.setattr(torch.cuda, "synchronize", lambda: None)
+    assert bench.step_spread(replay, 100) == {"n": 100, "median_ms": 6.0, "p10_ms": 2.0, "p90_ms": 9.0}
+    assert bench.step_spread(replay, 1)["median_ms"] >= 1.0
