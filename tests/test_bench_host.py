@@ -134,3 +134,20 @@ def test_step_spread_percentiles(monkeypatch):
     monkeypatch.setattr(torch.cuda, "synchronize", lambda: None)
     assert bench.step_spread(replay, 100) == {"n": 100, "median_ms": 6.0, "p10_ms": 2.0, "p90_ms": 9.0}
     assert bench.step_spread(replay, 1)["median_ms"] >= 1.0
+
+
+def test_algorithmic_bytes_match_the_closed_forms():
+    """The numerator of every GB/s figure: packed weights + scales + activations +
+    outputs, per format, against the per-weight closed forms and the 4096 x 4096
+    single-matrix and Llama-2-7B stack figures."""
+    K = N = 4096
+    assert bench.weight_bytes("q4_0", N, K) == N * K * 18 // 32 == 9_437_184
+    assert bench.weight_bytes("q4_k", N, K) == N * K * 144 // 256
+    assert bench.weight_bytes("nvfp4", N, K) == N * K // 2 + N * K // 16      # 0.5625 B per weight
+    assert bench.weight_bytes("fp8", N, K) == N * K + 4 * N                    # + fp32 row scale
+    assert bench.call_bytes("q4_0", 1, N, K) == 9_437_184 + 4_608 + 16_384     # Q8_1 in, fp32 out
+    assert bench.call_bytes("q4_0", 1, N, K, fused=True) == 9_437_184 + 16_384 + 16_384   # fp32 in
+    assert bench.call_bytes("nvfp4", 8, N, K) == bench.weight_bytes("nvfp4", N, K) + 8 * K * 2 + 8 * N * 4
+    mats = bench.llama2_7b_stack()
+    assert sum(4 * n for _, n, _ in mats) == 5_567_488                         # outputs of one token
+    assert sum((k // 32) * 36 for _, _, k in mats) == 1_285_632                # one Q8_1 row per matmul
