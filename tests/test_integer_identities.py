@@ -114,3 +114,48 @@ def test_tensor_core_kernel_bytes(seed):
             for i in range(4))
     assert np.array_equal(D, 16 * (S - 8 * T[:, None, :]))
     assert np.abs(D).max() < 1 << 31                  # fits the int32 accumulator
+
+
+def test_q4_k_word_wide_scale_unpack():
+    """The Q4_K streaming kernel unpacks the 12 packed bytes with four word-wide
+    mask/shift pairs (w1 = bytes 0..3, w2 = 4..7, w3 = 8..11): byte j of
+    w1 & 0x3f3f3f3f / w2 & 0x3f3f3f3f are scale / minimum of sub-block j < 4, byte j of
+    (w3 & 0x0f0f0f0f) | ((w1 >> 2) & 0x30303030) and
+    ((w3 >> 4) & 0x0f0f0f0f) | ((w2 >> 2) & 0x30303030) those of sub-block 4 + j."""
+    rng = np.random.default_rng(21)
+    packs = np.concatenate([rng.integers(0, 256, (3000, 12), dtype=np.uint8),
+                            np.full((1, 12), 0xFF, np.uint8), np.zeros((1, 12), np.uint8)])
+    for p in packs:
+        w1, w2, w3 = (int(v) for v in p.view("<u4"))
+        words = {"sc_lo": w1 & 0x3F3F3F3F, "mn_lo": w2 & 0x3F3F3F3F,
+                 "sc_hi": (w3 & 0x0F0F0F0F) | ((w1 >> 2) & 0x30303030),
+                 "mn_hi": ((w3 >> 4) & 0x0F0F0F0F) | ((w2 >> 2) & 0x30303030)}
+        for j in range(4):
+            assert oracle.q4_k_scale_min(p, j) == ((words["sc_lo"] >> 8 * j) & 0xFF, (words["mn_lo"] >> 8 * j) & 0xFF)
+            assert oracle.q4_k_scale_min(p, 4 + j) == ((words["sc_hi"] >> 8 * j) & 0xFF,
+                                                       (words["mn_hi"] >> 8 * j) & 0xFF)
+
+
+@pytest.mark.parametrize("seed", [6, 7])
+def test_q4_k_stream_sub_block_dots(seed):
+    """Data words 8c .. 8c + 7 of a super-block hold sub-block 2c in their low nibbles
+    and 2c + 1 in their high nibbles: low nibbles (mask 0x0f) against activation block
+    2c, high nibbles in place (mask 0xf0, 16 q) against block 2c + 1, exactly S."""
+    from gemm_qmv_quantize_gb300 import synth
+    N, M, K = 29, 2, 1024
+    w = synth.q4_k_weights(N, K, seed=seed).numpy()
+    xq = oracle.quantize_q8_1(synth.activations_f32(M, K, seed=seed + 1).numpy())
+    xq[1, 4:36] = np.uint8(129)   # a block of -127 quants
+    S = oracle.q4_k_block_dots(w, xq, K).astype(np.int64)
+    nsb, nb = K // 256, K // 32
+    data = w.reshape(N, nsb, 144)[:, :, 16:].copy().view("<u4").astype(np.uint64)   # [N][nsb][32] words
+    q8 = xq.reshape(M, nb, 36)[:, :, 4:].copy().view("<u4").astype(np.uint64)       # [M][nb][8] words
+    for s in range(nsb):
+        for c in range(4):
+            b_lo, b_hi = 8 * s + 2 * c, 8 * s + 2 * c + 1
+            lo = sum(dp4a(data[None, :, s, 8 * c + i] & 0x0F0F0F0F, q8[:, None, b_lo, i], 0, a_signed=False)
+                     for i in range(8))
+            hi = sum(dp4a(data[None, :, s, 8 * c + i] & 0xF0F0F0F0, q8[:, None, b_hi, i], 0, a_signed=False)
+                     for i in range(8))
+            assert np.all(hi % 16 == 0)
+            assert np.array_equal(lo, S[:, :, b_lo]) and np.array_equal(hi >> 4, S[:, :, b_hi])
