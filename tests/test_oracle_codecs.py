@@ -113,3 +113,20 @@ def test_e2m1_round_trip():
                                     (3.5, 0x6), (5.0, 0x6), (7.0, 0x7), (-2.6, 0xD)])
 def test_e2m1_encode_ties_to_even(v, code):
     assert oracle.e2m1_encode(v) == code
+
+
+def test_e2m1_times_e4m3_is_exact_in_fp16():
+    """The NVFP4 kernel folds the group scale into the fp16 weight (one fp16 multiply
+    per pair): every E2M1 value times every non-NaN E4M3 scale has at most 6
+    significant bits and a magnitude within [2^-10, 2688], so fp16 holds it exactly
+    and the only rounding left is the fp32 accumulation."""
+    vals = [oracle.e2m1_to_double(c) for c in range(16)]
+    scales = [oracle.e4m3_to_double(b) for b in range(256) if b & 0x7F != 0x7F]
+    nonzero = []
+    for v in vals:
+        for s in scales:
+            p = v * s
+            assert float(np.float16(p)) == p, (v, s)
+            if p:
+                nonzero.append(abs(p))
+    assert min(nonzero) == 2.0 ** -10 and max(nonzero) == 6 * 448 == 2688
