@@ -1,6 +1,7 @@
-"""Integer identities behind the MMVQ kernels, checked on the CPU with a plain
-emulation of the instructions (PTX ISA semantics) against the oracle's exact block
-sums S = sum q4u * q8 and T = sum q8.
+"""Arithmetic identities behind the kernels, checked on the CPU with a plain
+emulation of the instructions (PTX ISA semantics, IEEE fp32) against the oracle:
+the exact block sums S = sum q4u * q8 and T = sum q8, the Q4_K scale decode, and
+the Q8_1 bytes.
 
 - "Machine Learning on NVIDIA CMP", section "The DP2A patch": one 4-way int8 dot
   equals a 2-way dot over bytes 0..1 plus one over bytes 2..3 of B, once A's four
@@ -10,6 +11,9 @@ sums S = sum q4u * q8 and T = sum q8.
   exactly, and a block's dot is S - 8 T.
 - The int8 tensor-core kernel: the weight bytes 16 (q - 8) as int8, formed as
   (nibble << 4) ^ 0x80, so a block's product is 16 (S - 8 T) exactly in int32.
+- The Q8_1 quantizer: x * fl(1 / d) rounded to nearest, redone with the IEEE
+  quotient and ties away from zero only near a half-integer, gives the oracle's
+  bytes (random, wide-range, subnormal-scale and one-ulp-from-a-tie blocks).
 """
 import numpy as np
 import pytest
@@ -159,3 +163,45 @@ def test_q4_k_stream_sub_block_dots(seed):
                      for i in range(8))
             assert np.all(hi % 16 == 0)
             assert np.array_equal(lo, S[:, :, b_lo]) and np.array_equal(hi >> 4, S[:, :, b_hi])
+
+
+def _q8_fast_path(x):
+    """The device quantizer's per-block arithmetic in IEEE fp32 (numpy rounds like
+    the device's non-fast-math ops): d = amax / 127; t = x * fl(1 / d) rounded to
+    nearest even; where t lies within 2^-13 of a half-integer, or 1 / d overflows, the
+    value is redone as roundf(x / d) (ties away from zero) with the IEEE quotient."""
+    x = x.astype(np.float32)
+    amax = np.abs(x).max(axis=1)
+    d = (amax / np.float32(127)).astype(np.float32)
+    with np.errstate(divide="ignore", over="ignore"):
+        inv = (np.float32(1) / d).astype(np.float32)
+    rcp = np.where(d == 0, np.float32(0), inv).astype(np.float32)
+    t = (x * rcp[:, None]).astype(np.float32)
+    n = np.rint(t)
+    with np.errstate(invalid="ignore"):   # t = inf where 1 / d overflowed: redone below
+        slow = np.abs(t - n) > np.float32(0.5 - 2.0 ** -13)
+    slow |= (~np.isfinite(inv) & (d != 0))[:, None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        qd = (x / d[:, None]).astype(np.float32)
+    away = np.sign(qd) * np.floor(np.abs(qd.astype(np.float64)) + 0.5)
+    q = np.where(slow, np.clip(away, -127, 127), n)
+    return np.where(d[:, None] == 0, 0, q).astype(np.int64)
+
+
+def test_quantizer_fast_path_matches_the_oracle():
+    rng = np.random.default_rng(31)
+    blocks = [rng.standard_normal((20000, 32)),
+              rng.standard_normal((2000, 32)) * 1e-40,                      # subnormal amax: 1 / d overflows
+              np.exp(rng.uniform(-80, 80, (2000, 32))) * rng.choice([-1, 1], (2000, 32))]
+    # adversarial: every value near a tie of x / d, for random scales
+    d = np.exp(rng.uniform(-20, 20, 4000)).astype(np.float32)
+    k = rng.integers(-126, 127, (4000, 31)) + 0.5
+    near = (k * d[:, None]).astype(np.float32)
+    step = rng.choice([-1, 0, 1], near.shape)          # one ulp below, on, or above the tie
+    near = np.nextafter(near, np.where(step > 0, np.float32(np.inf), np.where(step < 0, np.float32(-np.inf), near)))
+    blocks.append(np.concatenate([near, (127 * d)[:, None]], axis=1))   # amax pins d
+    for b in blocks:
+        b = b.astype(np.float32)
+        xq = oracle.quantize_q8_1(b.reshape(1, -1)).reshape(len(b), 36)
+        q_oracle = xq[:, 4:].view(np.int8).astype(np.int64)
+        assert np.array_equal(_q8_fast_path(b), q_oracle)
