@@ -62,3 +62,24 @@ def test_without_the_swizzle_the_reads_conflict():
         assert conflicts(8, 5120, True)
     finally:
         chunk_slot = saved
+
+
+def _constant(name):
+    import os
+    import re
+    from conftest import ROOT
+    src = open(os.path.join(ROOT, "gemm_qmv_quantize_gb300", "csrc", "q4_0_q8_1.cu")).read()
+    return int(re.search(rf"constexpr int {name} = (\d+);", src).group(1))
+
+
+@pytest.mark.parametrize("name,words", [("kActUnitStride", 21), ("kUnitBytes", 9)])
+def test_q4_stream_records_and_units_are_conflict_free(name, words):
+    """The Q4 streaming kernel: consecutive lanes read consecutive 144-byte weight
+    units of a ring slot and consecutive 336-byte activation records of a row, 16 bytes
+    at a time. Both strides are odd multiples of 16 bytes, so every 16-byte offset of
+    eight consecutive units or records falls in eight different bank groups."""
+    stride = _constant(name)
+    assert stride == 16 * words and words % 2 == 1
+    for j in range(words):
+        for first in range(64):
+            assert len({((first + l) * stride + 16 * j) // 16 % 8 for l in range(8)}) == 8
