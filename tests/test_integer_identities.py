@@ -11,6 +11,8 @@ the Q8_1 bytes.
   exactly, and a block's dot is S - 8 T.
 - The int8 tensor-core kernel: the weight bytes 16 (q - 8) as int8, formed as
   (nibble << 4) ^ 0x80, so a block's product is 16 (S - 8 T) exactly in int32.
+- The Q4_0 unit layout: the 36 aligned words of a 144-byte unit give each block's
+  scale and nibble words (even blocks realigned by one byte permute).
 - The Q8_1 quantizer: x * fl(1 / d) rounded to nearest, redone with the IEEE
   quotient and ties away from zero only near a half-integer, gives the oracle's
   bytes (random, wide-range, subnormal-scale and one-ulp-from-a-tie blocks).
@@ -205,3 +207,24 @@ def test_quantizer_fast_path_matches_the_oracle():
         xq = oracle.quantize_q8_1(b.reshape(1, -1)).reshape(len(b), 36)
         q_oracle = xq[:, 4:].view(np.int8).astype(np.int64)
         assert np.array_equal(_q8_fast_path(b), q_oracle)
+
+
+def test_q4_0_unit_words_to_blocks():
+    """The streaming kernel reads a 144-byte unit (eight 18-byte Q4_0 blocks) as 36
+    aligned words w: block j (even) starts at word wa = 18 j / 4 with its scale in the
+    low half of w[wa] and its nibbles two bytes into the next words, realigned by
+    prmt(w[wa + i], w[wa + i + 1], 0x5432); block j + 1 has its scale in the high half
+    of w[wa + 4] and its nibbles in w[wa + 5 .. wa + 8]."""
+    rng = np.random.default_rng(41)
+    for _ in range(200):
+        unit = rng.integers(0, 256, 144, dtype=np.uint8)
+        w = [int(v) for v in unit.view("<u4")]
+        for j in range(0, 8, 2):
+            wa = 18 * j // 4
+            blk, nxt = unit[18 * j:18 * j + 18], unit[18 * j + 18:18 * j + 36]
+            assert w[wa] & 0xFFFF == int(blk[:2].view("<u2")[0])
+            assert w[wa + 4] >> 16 == int(nxt[:2].view("<u2")[0])
+            for i in range(4):
+                assert int(prmt(np.array([w[wa + i]]), np.array([w[wa + i + 1]]), 0x5432)[0]) == \
+                    int(blk[2 + 4 * i:6 + 4 * i].view("<u4")[0])
+                assert w[wa + 5 + i] == int(nxt[2 + 4 * i:6 + 4 * i].view("<u4")[0])
