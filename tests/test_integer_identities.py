@@ -11,6 +11,8 @@ the Q8_1 bytes.
   exactly, and a block's dot is S - 8 T.
 - The int8 tensor-core kernel: the weight bytes 16 (q - 8) as int8, formed as
   (nibble << 4) ^ 0x80, so a block's product is 16 (S - 8 T) exactly in int32.
+- The tensor-core kernel's m16n8k32 fragments: rebuilt into A and B by the PTX
+  layout, their product lands 16 (S - 8T) in the lanes the epilogue reads.
 - The Q4_0 unit layout: the 36 aligned words of a 144-byte unit give each block's
   scale and nibble words (even blocks realigned by one byte permute).
 - The Q8_1 quantizer: x * fl(1 / d) rounded to nearest, redone with the IEEE
@@ -228,3 +230,34 @@ def test_q4_0_unit_words_to_blocks():
                 assert int(prmt(np.array([w[wa + i]]), np.array([w[wa + i + 1]]), 0x5432)[0]) == \
                     int(blk[2 + 4 * i:6 + 4 * i].view("<u4")[0])
                 assert w[wa + 5 + i] == int(nxt[2 + 4 * i:6 + 4 * i].view("<u4")[0])
+
+
+def test_q4_0_tensor_core_fragment_mapping():
+    """mma.sync.m16n8k32.s8 fragments of the Q4_0 tensor-core kernel, lane (g, t) =
+    (lane / 4, lane % 4): A registers {lo of row g, lo of row g + 8, hi of row g, hi of
+    row g + 8} built from nibble word t of each row's block (k = 4t.. and 16 + 4t..),
+    B registers Q8_1 words t and 4 + t of activation row g. Rebuilt into A (16 x 32)
+    and B (32 x 8) by the PTX fragment layout, D = A B gives, in lane (g, t)'s d0..d3,
+    16 (S - 8T) of weight rows g, g + 8 against activation rows 2t, 2t + 1."""
+    qs, q8, S, T = _blocks(8, N=16, M=8, K=256)
+    for b in range(qs.shape[1]):
+        A = np.zeros((16, 32), np.int64)
+        B = np.zeros((32, 8), np.int64)
+        for lane in range(32):
+            g, t = lane // 4, lane % 4
+            lo = lambda r: ((qs[r, b, t] << 4) & 0xF0F0F0F0) ^ 0x80808080   # noqa: E731
+            hi = lambda r: (qs[r, b, t] & 0xF0F0F0F0) ^ 0x80808080         # noqa: E731
+            a = [lo(g), lo(g + 8), hi(g), hi(g + 8)]
+            for j in range(4):
+                A[g, 4 * t + j] = _s8(a[0])[j]
+                A[g + 8, 4 * t + j] = _s8(a[1])[j]
+                A[g, 16 + 4 * t + j] = _s8(a[2])[j]
+                A[g + 8, 16 + 4 * t + j] = _s8(a[3])[j]
+                B[4 * t + j, g] = _s8(q8[g, b, t])[j]
+                B[16 + 4 * t + j, g] = _s8(q8[g, b, 4 + t])[j]
+        D = A @ B
+        want = 16 * (S[:, :, b] - 8 * T[:, None, b])    # [act][row]
+        for lane in range(32):
+            g, t = lane // 4, lane % 4
+            d = [D[g, 2 * t], D[g, 2 * t + 1], D[g + 8, 2 * t], D[g + 8, 2 * t + 1]]
+            assert d == [want[2 * t, g], want[2 * t + 1, g], want[2 * t, g + 8], want[2 * t + 1, g + 8]]
