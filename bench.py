@@ -56,11 +56,12 @@ def llama2_7b_stages():
     return st + [[224]]
 
 
-def dense_27b_stack(mixed: bool):
+def dense_27b_stack(mixed: bool, layers: int = 64):
     """64 layers of {qkv 7168x5120, o 5120x5120, gate/up 17408x5120, down 5120x17408};
-    mixed: attention projections of layers 3, 7, ..., 63 in FP8, plus an NVFP4 lm_head."""
+    mixed: attention projections of layers 3, 7, ..., 63 in FP8, plus an NVFP4 lm_head.
+    `layers` < 64 gives the first layers of the same stack (and its lm_head)."""
     mats = []
-    for layer in range(64):
+    for layer in range(layers):
         attn = "fp8" if (mixed and layer % 4 == 3) else "nvfp4"
         mats += [(attn, 7168, 5120), (attn, 5120, 5120), ("nvfp4", 17408, 5120), ("nvfp4", 17408, 5120),
                  ("nvfp4", 5120, 17408)]
@@ -69,13 +70,13 @@ def dense_27b_stack(mixed: bool):
     return mats
 
 
-def dense_27b_stages(mixed: bool):
+def dense_27b_stages(mixed: bool, layers: int = 64):
     """Per layer {qkv}, {o}, {gate, up} (the same input), {down}; then the lm_head."""
     st = []
-    for layer in range(64):
+    for layer in range(layers):
         b = 5 * layer
         st += [[b], [b + 1], [b + 2, b + 3], [b + 4]]
-    return st + ([[320]] if mixed else [])
+    return st + ([[5 * layers]] if mixed else [])
 
 
 def qwen3_8b_stack():
@@ -335,10 +336,13 @@ def profiled_traffic(kernel: str, workload: str):
 class Stack:
     """Resident weights and per-call activation/output buffers of one workload."""
 
-    def __init__(self, name: str, device, seed: int = 1234, fused: bool = True, grouped: bool = True):
+    def __init__(self, name: str, device, seed: int = 1234, fused: bool = True, grouped: bool = True, spec=None):
+        """spec: dict(M, mats, stages) of a workload not in WORKLOADS (tests build
+        reduced stacks of the same shapes through the same dispatch)."""
         import torch
         from gemm_qmv_quantize_gb300 import synth
-        w = WORKLOADS[name]
+        w = WORKLOADS[name] if spec is None else dict(M=spec["M"], mats=lambda: list(spec["mats"]),
+                                                       stages=lambda: [list(st) for st in spec["stages"]])
         self.name, self.M, self.mats, self.device = name, w["M"], w["mats"](), device
         self.fused = fused
         # Dependent stages: matrices of a stage read the same input tensor and are
@@ -526,11 +530,37 @@ def run_ours(args, rank, world, local_rank):
     q.set_launch_overlap(not args.no_overlap)
     with torch.cuda.stream(stream):
         line = _run_ours_on_stream(args, rank, world, local_rank, stack, stream, barrier, max_over_ranks)
+    # secondary records: other workloads timed in the same run, each with its own roofline
+    second = secondary_workloads(args)
+    if second:
+        del stack
+        torch.cuda.empty_cache()
+        line["secondary"] = []
+        for wl in second:
+            sargs = argparse.Namespace(**{**vars(args), "workload": wl, "steps": min(args.steps, 300)})
+            st2 = Stack(wl, dev, seed=1234 + rank, fused=q4_fused(sargs), grouped=not args.serial)
+            with torch.cuda.stream(stream):
+                rec = _run_ours_on_stream(sargs, rank, world, local_rank, st2, stream, barrier, max_over_ranks,
+                                          secondary=True)
+            line["secondary"].append(rec)
+            del st2
+            torch.cuda.empty_cache()
     dist.close()
     return line if rank == 0 else None
 
 
-def _run_ours_on_stream(args, rank, world, local_rank, stack, stream, barrier, max_over_ranks):
+def secondary_workloads(args):
+    """Workloads timed after the main one in the same run: by default the 27B-class
+    NVFP4 stack at M = 1 beside the default Q4_0 stack (the two M = 1 paths whose
+    HBM fraction is the target), none beside any other workload."""
+    if args.secondary == "auto":
+        return ["nvfp4_27b_m1"] if args.workload == DEFAULT_WORKLOAD else []
+    return [w for w in args.secondary.split(",") if w and w != "none"]
+
+
+def _run_ours_on_stream(args, rank, world, local_rank, stack, stream, barrier, max_over_ranks, secondary=False):
+    """The measured line of one workload: its timed region, roofline, clocks and, for
+    the main record, e2e, parity and the CPU baseline (secondary records: parity only)."""
     import torch
     import gemm_qmv_quantize_gb300 as q
     q.route_reset()   # launches of one step, by the route census of an eager step
@@ -563,7 +593,7 @@ def _run_ours_on_stream(args, rank, world, local_rank, stack, stream, barrier, m
     roof = kernel_roofline(args, stack, stream, barrier, step_s=None if args.eager else step_s)
 
     # end to end through the public API with host buffers: pinned x in, y out, every step
-    e2e = end_to_end(args, stack, replay, stream, barrier, max_over_ranks, world)
+    e2e = None if secondary else end_to_end(args, stack, replay, stream, barrier, max_over_ranks, world)
 
     err = q.error_flags(clear=True)
     peak, peak_kind = measured_peak()
@@ -588,8 +618,14 @@ def _run_ours_on_stream(args, rank, world, local_rank, stack, stream, barrier, m
         "roofline": roof, "e2e": e2e, "step_ms": spread, "gpu_launches": int(kernels), "clocks": clocks.summary(),
         "device_error_flags": err,
     }
+    if secondary:
+        for key in ("metric", "unit", "n_gpus", "higher_is_better", "scaling", "vs_baseline", "data", "e2e",
+                    "hbm_peak_gbs", "hbm_peak_kind", "warmup"):
+            line.pop(key, None)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
+        line["parity"] = sampled_parity(stack)
+        if not secondary:
+            line["cpu_baseline"] = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
     return line
 
 
@@ -699,12 +735,24 @@ def end_to_end(args, stack, replay, stream, barrier, max_over_ranks, world):
 # ----------------------------------------------------------------------------- the oracle (CPU) arm
 
 
+def host_threads() -> int:
+    """Host cores this process may run on (the oracle's C calls release the GIL, so
+    a thread per core runs the plain oracle in parallel over row blocks)."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except (AttributeError, OSError):
+        return max(1, os.cpu_count() or 1)
+
+
 class OracleSampler:
     """Times the CPU oracle on a bounded sample of a workload: for each distinct
-    matrix shape, the first rows of one seeded matrix with the same per-call work
-    (Q8_1 quantize of the activation + the dot products), the time budget split
-    across shapes in proportion to the stack's bytes. Inputs are generated once
-    (untimed) and reused by every sample."""
+    matrix shape, row blocks of one seeded matrix with the same per-call work (Q8_1
+    quantize of the activation + the dot products), the time budget split across
+    shapes in proportion to the stack's bytes, on `threads` host threads that take
+    row blocks in turn. Inputs are generated once (untimed) and reused by every
+    sample; the oracle itself is the plain, single-threaded C code."""
+
+    BLOCK_ROWS = 64
 
     def __init__(self, workload: str, seed: int = 99):
         w = WORKLOADS[workload]
@@ -739,81 +787,154 @@ class OracleSampler:
             self.cache[shape] = have = (r, w, x)
         return have
 
-    def sample(self, budget_s: float):
+    def prepare(self):
+        """Generate every shape's seeded inputs (untimed)."""
+        for shape in self.shapes:
+            self._inputs(shape, min(shape[1], 8192))
+
+    def sample(self, budget_s: float, threads: int = 1):
+        """(GB/s, info) of one bounded sample: `budget_s` seconds of wall time."""
+        import itertools
+        from concurrent.futures import ThreadPoolExecutor
+
         import numpy as np
 
         import oracle
-        done_bytes, done_time, rows_done = 0, 0.0, {}
+        done_bytes, wall, rows_done = 0, 0.0, {}
+        act = {sh: (self.M * (sh[2] // 32) * Q8_1_BLOCK if sh[0] in ("q4_0", "q4_k") else self.M * sh[2] * 2)
+               for sh in self.shapes}
         for shape in self.shapes:
             fmt, n, k = shape
-            rows, t_shape, key = 16, 0.0, f"{fmt} {n}x{k}"
-            rows_done[key] = 0
+            key = f"{fmt} {n}x{k}"
             cap = min(n, 8192)   # rows of the seeded matrix, cycled through until the time share is used
             _, w, x = self._inputs(shape, cap)
-            while t_shape < budget_s * self.share[shape]:
-                off = rows_done[key] % cap
-                r = min(rows, cap - off)
+            blocks = itertools.count()
+
+            def one_call(off, r):
                 if fmt == "q4_0":
-                    t0 = time.perf_counter()
                     oracle.q4_0_q8_1(np.ascontiguousarray(w[0][off:off + r]), oracle.quantize_q8_1(x), k)
                 elif fmt == "q4_k":
-                    t0 = time.perf_counter()
                     oracle.q4_k_q8_1(np.ascontiguousarray(w[0][off:off + r]), oracle.quantize_q8_1(x), k)
                 elif fmt == "nvfp4":
-                    t0 = time.perf_counter()
-                    oracle.nvfp4_w4a16(np.ascontiguousarray(w[0][off:off + r]), np.ascontiguousarray(w[1][off:off + r]),
-                                       w[2], x)
+                    oracle.nvfp4_w4a16(np.ascontiguousarray(w[0][off:off + r]),
+                                       np.ascontiguousarray(w[1][off:off + r]), w[2], x)
                 else:
-                    t0 = time.perf_counter()
-                    oracle.fp8_w8a16(np.ascontiguousarray(w[0][off:off + r]), np.ascontiguousarray(w[1][off:off + r]), x)
-                dt = time.perf_counter() - t0
-                # the sampled rows' weights and outputs, plus the activation once per call
-                act = self.M * (k // 32) * Q8_1_BLOCK if fmt in ("q4_0", "q4_k") else self.M * k * 2
-                done_bytes += weight_bytes(fmt, r, k) + self.M * r * 4 + act
-                done_time += dt
-                t_shape += dt
-                rows_done[key] += r
-                rows = min(rows * 2, 2048)
-        sample = ("oracle (plain C, fp64, one thread) on the rows of one seeded matrix per distinct shape (at most "
-                  "8192 rows, cycled), time split by the stack's bytes per shape; rows processed per shape: "
-                  f"{rows_done}")
-        return done_bytes / done_time / 1e9, {"bytes": done_bytes, "seconds": round(done_time, 3), "sample": sample}
+                    oracle.fp8_w8a16(np.ascontiguousarray(w[0][off:off + r]),
+                                     np.ascontiguousarray(w[1][off:off + r]), x)
+
+            def worker(deadline):
+                b = r_done = 0
+                while True:
+                    off = (next(blocks) * self.BLOCK_ROWS) % cap
+                    r = min(self.BLOCK_ROWS, cap - off)
+                    one_call(off, r)
+                    # the rows' weights and outputs, plus the activation once per call
+                    b += weight_bytes(fmt, r, k) + self.M * r * 4 + act[shape]
+                    r_done += r
+                    if time.perf_counter() >= deadline:
+                        return b, r_done
+
+            t0 = time.perf_counter()
+            deadline = t0 + budget_s * self.share[shape]
+            with ThreadPoolExecutor(max_workers=threads) as ex:
+                parts = list(ex.map(worker, [deadline] * threads))
+            wall += time.perf_counter() - t0
+            done_bytes += sum(p[0] for p in parts)
+            rows_done[key] = sum(p[1] for p in parts)
+        sample = (f"oracle (plain C, fp64) on {threads} host threads taking blocks of {self.BLOCK_ROWS} rows of one "
+                  "seeded matrix per distinct shape (at most 8192 rows, cycled), wall time split by the stack's "
+                  f"bytes per shape; rows processed per shape: {rows_done}")
+        return done_bytes / wall / 1e9, {"bytes": done_bytes, "seconds": round(wall, 3), "sample": sample}
 
 
-def cpu_sample(workload: str, budget_s: float):
-    return OracleSampler(workload).sample(budget_s)
-
-
-def cpu_baseline(workload: str, budget_s: float):
-    gbs, info = cpu_sample(workload, budget_s)
-    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": info["sample"],
+def cpu_baseline(workload: str, budget_s: float, threads: int | None = None):
+    threads = threads or host_threads()
+    sampler = OracleSampler(workload)
+    sampler.prepare()
+    gbs, info = sampler.sample(budget_s, threads)
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": info["sample"],
             "seconds": info["seconds"]}
+
+
+def sampled_parity(stack, rows: int = 8, seed: int = 7, threads: int | None = None):
+    """Parity of the program that was timed, checked after the timed region (the
+    cpu_baseline leg): for every matrix of the stack, `rows` sampled output rows (the
+    first, the last and random ones) of the last step's y against the oracle on the
+    same weights and activations, |y - y_ref| <= 1e-3 * sum_k |w x| + 1e-6."""
+    from concurrent.futures import ThreadPoolExecutor
+
+    import numpy as np
+    import torch
+
+    import oracle
+    from gemm_qmv_quantize_gb300 import synth
+    torch.cuda.synchronize()
+    xs_host, jobs = {}, []
+    for i, (fmt, n, k) in enumerate(stack.mats):
+        ridx = synth.sample_rows(n, rows, seed + i).to(stack.device)
+        j = stack.input_of[i]
+        if j not in xs_host:
+            xs_host[j] = stack.xs[i].cpu().numpy()
+        w = tuple(t.index_select(0, ridx).cpu().numpy() if isinstance(t, torch.Tensor) else t
+                  for t in stack.weights[i])
+        jobs.append((fmt, k, w, j, stack.ys[i].index_select(1, ridx).cpu().numpy()))
+
+    def check(job):
+        fmt, k, w, j, y = job
+        x = xs_host[j]
+        if fmt == "q4_0":
+            y_ref, bound = oracle.q4_0_q8_1(w[0], oracle.quantize_q8_1(x), k)
+        elif fmt == "q4_k":
+            y_ref, bound = oracle.q4_k_q8_1(w[0], oracle.quantize_q8_1(x), k)
+        elif fmt == "nvfp4":
+            y_ref, bound = oracle.nvfp4_w4a16(w[0], w[1], w[2], x)
+        else:
+            y_ref, bound = oracle.fp8_w8a16(w[0], w[1], x)
+        if not np.all(np.isfinite(y)):
+            return float("inf"), y.size
+        return float(np.max(np.abs(y.astype(np.float64) - y_ref) / (1e-3 * bound + 1e-6))), y.size
+
+    with ThreadPoolExecutor(max_workers=threads or host_threads()) as ex:
+        res = list(ex.map(check, jobs))
+    worst = max(r[0] for r in res)
+    return {"matrices": len(jobs), "checked": int(sum(r[1] for r in res)), "rows_per_matrix": rows,
+            "max_err_over_tol": round(worst, 4) if worst != float("inf") else "inf", "ok": bool(worst <= 1.0)}
 
 
 def run_reference(args, rank, world):
     """The oracle as it stands, timed on this host's cores: each step is a bounded
-    sample of the workload; --ref-seconds is the budget of the whole run."""
+    sample of the workload (--ref-seconds of wall time over the whole run); the line
+    reports what was run -- the sample's bytes over its wall time, and the wall time
+    of a sampled step -- and, under its own key, the time the whole stack would take
+    at that rate."""
     if rank != 0:
         return None
+    threads = host_threads()
     sampler = OracleSampler(args.workload)
+    sampler.prepare()
     budget = args.ref_seconds / max(1, args.steps + args.warmup)
     for _ in range(args.warmup):
-        sampler.sample(budget)
-    vals, info = [], None
+        sampler.sample(budget, threads)
+    info, total_bytes = None, 0
+    t0 = time.perf_counter()
     for _ in range(args.steps):
-        gbs, info = sampler.sample(budget)
-        vals.append(gbs)
-    value = statistics.mean(vals)
+        _, info = sampler.sample(budget, threads)
+        total_bytes += info["bytes"]
+    wall = time.perf_counter() - t0
+    value = total_bytes / wall / 1e9
     w = WORKLOADS[args.workload]
     stack_bytes = sum(call_bytes(*m[:1], w["M"], *m[1:]) for m in w["mats"]())
-    step_s = stack_bytes / (value * 1e9)
+    stack_s = stack_bytes / (value * 1e9)
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall / max(1, args.steps) * 1e3, 3),
+        "step": f"one bounded sample of the workload: {round(total_bytes / max(1, args.steps))} bytes of "
+                "weights, activations and outputs per step",
+        "extrapolated_stack_ms": round(stack_s * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "tok_per_s": round(w["M"] / step_s, 4),
+        "data": "synthetic", "tok_per_s": round(w["M"] / stack_s, 4),
         "config": {"workload": args.workload, "desc": w["desc"], "M": w["M"]},
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": info["sample"] if info else ""},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -834,10 +955,15 @@ def parse_args(argv=None):
                    help="one launch per matrix in stream order (no grouped launches of independent matrices)")
     p.add_argument("--no-overlap", action="store_true",
                    help="no programmatic dependent launch between consecutive calls")
-    p.add_argument("--cpu-seconds", type=float, default=12.0, help="time budget of the cpu_baseline sample")
+    p.add_argument("--cpu-seconds", type=float, default=2.0,
+                   help="wall-time budget of the cpu_baseline sample (on every host core)")
     p.add_argument("--ref-seconds", type=float, default=60.0,
                    help="oracle time budget of the whole --impl reference run")
-    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true",
+                   help="skip the cpu_baseline leg (the oracle's timing and the sampled parity check)")
+    p.add_argument("--secondary", default="auto",
+                   help="comma-separated workloads timed after the main one in the same run ('none': no "
+                        "secondary record; auto: the NVFP4 27B stack at M = 1 beside the default workload)")
     return p.parse_args(argv)
 
 
@@ -852,6 +978,10 @@ def main(argv=None):
         line = run_ours(args, rank, world, local_rank)
     if line is not None:
         print(json.dumps(line), flush=True)
+        bad = [r for r in [line] + line.get("secondary", []) if r.get("parity", {}).get("ok") is False]
+        if bad:   # the timed program disagrees with the oracle: the line does not stand
+            print("parity check failed: " + ", ".join(r["config"]["workload"] for r in bad), file=sys.stderr)
+            sys.exit(1)
 
 
 if __name__ == "__main__":

@@ -11,9 +11,10 @@ from ._binding import (QmvError, QmvLibraryMissing, error_flags, get_launch_over
                        qgemm_nvfp4_w4a16, qmv_debug_q4_0_block_dots, qmv_q4_0_q8_1,
                        qmv_q4_0_q8_1_fused, qmv_q4_0_q8_1_fused_group, qmv_q4_0_q8_1_group, qmv_quantize_q8_1,
                        qmv_debug_q4_k_block_dots, qmv_q4_k_q8_1, qmv_q4_k_q8_1_fused, qmv_q4_k_q8_1_fused_group,
-                       qmv_q4_k_q8_1_group, qmv_debug_wait_bound, qmv_debug_plan_q4, route_counts, route_reset)
+                       qmv_q4_k_q8_1_group, qmv_debug_wait_bound, qmv_debug_cta_abort, qmv_debug_plan_q4, qmv_debug_plan_wq,
+                       route_counts, route_reset)
 
 __all__ = ["QmvError", "QmvLibraryMissing", "error_flags", "get_launch_overlap", "set_launch_overlap", "lib", "library_path", "qgemm_fp8_w8a16", "qgemm_fp8_w8a16_group", "qgemm_nvfp4_w4a16_group",
            "qgemm_nvfp4_w4a16", "qmv_debug_q4_0_block_dots", "qmv_q4_0_q8_1", "qmv_q4_0_q8_1_fused", "qmv_q4_0_q8_1_fused_group", "qmv_q4_0_q8_1_group", "qmv_quantize_q8_1",
            "qmv_debug_q4_k_block_dots", "qmv_q4_k_q8_1", "qmv_q4_k_q8_1_fused", "qmv_q4_k_q8_1_fused_group",
-           "qmv_q4_k_q8_1_group", "qmv_debug_wait_bound", "qmv_debug_plan_q4", "route_counts", "route_reset"]
+           "qmv_q4_k_q8_1_group", "qmv_debug_wait_bound", "qmv_debug_cta_abort", "qmv_debug_plan_q4", "qmv_debug_plan_wq", "route_counts", "route_reset"]

@@ -56,6 +56,9 @@ SIGNATURES = {
     "qmv_route_reset": (None, []),
     "qmv_error_flags": (_i32, [ctypes.POINTER(ctypes.c_uint32), _i32]),
     "qmv_debug_wait_bound": (_i32, [_vp, _vp]),
+    "qmv_debug_cta_abort": (_i32, [_vp, _i32, _vp]),
+    "qmv_debug_plan_wq": (_i32, [_i32, _i32, _i64, _i32, ctypes.POINTER(_i64), _i32, _i32, _i32, _i32,
+                                 ctypes.POINTER(_i32), _vp]),
     "qmv_debug_plan_q4": (_i32, [_i32, _i32, _i64, _i64, _i32, _i32, _i32, _i32, _i32, _vp]),
 }
 
@@ -288,6 +291,18 @@ def qmv_debug_wait_bound(out: torch.Tensor | None = None, stream=None) -> torch.
     return out
 
 
+def qmv_debug_cta_abort(stuck_warp: int = 3, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """int64 [8][4] on the current device, per warp of the self-check CTA: [1 if its
+    bounded wait gave up, 1 if it passed the round's barrier and saw the CTA's abort
+    word, copies in flight when it left the round, nanoseconds from its first wait to
+    the barrier]. Warp `stuck_warp` waits on copies that were never issued."""
+    if out is None:
+        out = torch.full((8, 4), -1, dtype=torch.int64, device="cuda")
+    _need(out, "out", torch.int64, (8, 4))
+    _check("qmv_debug_cta_abort", lib().qmv_debug_cta_abort(out.data_ptr(), int(stuck_warp), _stream(stream)))
+    return out
+
+
 PLAN_FIELDS = ("route", "warps", "slots", "grid", "smem_bytes", "act_regs", "pair", "chunk_units")
 GB300_DEVICE = dict(sm_count=152, smem_optin=232448, smem_per_sm=233472)
 
@@ -302,6 +317,28 @@ def qmv_debug_plan_q4(M: int, N: int, K: int, q4k: bool = False, n_inputs: int =
     _check("qmv_debug_plan_q4", lib().qmv_debug_plan_q4(int(bool(q4k)), M, N, K, n_inputs, int(bool(w_align16)),
                                                         sm_count, smem_optin, smem_per_sm, out))
     plan = dict(zip(PLAN_FIELDS, (int(v) for v in out)))
+    plan["route"] = lib().qmv_route_name(plan["route"]).decode()
+    return plan
+
+
+WQ_PLAN_FIELDS = ("route", "chunks", "chunk_rows", "warps", "slots", "staged", "passes", "tiles_per_round",
+                  "ctas_per_sm", "grid", "smem_bytes")
+
+
+def qmv_debug_plan_wq(M: int, K: int, N, fp4: bool = True, aligned16: bool = True, ctas_by_regs=None,
+                      sm_count: int = GB300_DEVICE["sm_count"], smem_optin: int = GB300_DEVICE["smem_optin"],
+                      smem_per_sm: int = GB300_DEVICE["smem_per_sm"]) -> dict:
+    """The NVFP4 (fp4) / FP8 launch plan for one call (N an int) or one grouped launch
+    (N a list of row counts) on the given device (GB300 by default), with CTAs per SM
+    from the occupancy model of include/qmv.h; a dict of WQ_PLAN_FIELDS with the route
+    as its name. No GPU needed."""
+    Ns = [int(N)] if isinstance(N, int) else [int(n) for n in N]
+    n_arr = (ctypes.c_int64 * len(Ns))(*Ns)
+    regs = None if ctas_by_regs is None else (ctypes.c_int * 3)(*[int(v) for v in ctas_by_regs])
+    out = (ctypes.c_int64 * 11)()
+    _check("qmv_debug_plan_wq", lib().qmv_debug_plan_wq(int(bool(fp4)), M, K, len(Ns), n_arr, int(bool(aligned16)),
+                                                        sm_count, smem_optin, smem_per_sm, regs, out))
+    plan = dict(zip(WQ_PLAN_FIELDS, (int(v) for v in out)))
     plan["route"] = lib().qmv_route_name(plan["route"]).decode()
     return plan
 

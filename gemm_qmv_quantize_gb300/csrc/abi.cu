@@ -41,15 +41,8 @@ qmv_status check_shape(int M, int64_t N, int64_t K, int64_t kblock, int max_m = 
     return QMV_OK;
 }
 
-// Error word of the wait-bound self-check below (OR-ed into qmv_error_flags).
+// Error word of the wait-bound self-checks below (OR-ed into qmv_error_flags).
 __device__ uint32_t g_abi_error;
-
-__device__ __forceinline__ uint64_t globaltimer_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-    return t;
-}
 
 // One thread waits, with the bounded wait of the streaming kernels, on an mbarrier
 // that expects one arrival nobody makes: the wait must give up, flag the error word
@@ -61,11 +54,74 @@ __global__ void wait_bound_kernel(int64_t *out)
     mbar_init(&bar, 1);
     fence_barrier_init();
     const uint64_t t0 = globaltimer_ns();
-    const bool done = mbar_wait_sleep(&bar, 0);
+    const bool done = mbar_wait_bounded(&bar, 0);
     const uint64_t t1 = globaltimer_ns();
     out[0] = done ? 1 : 0;
     out[1] = static_cast<int64_t>(t1 - t0);
     if (!done) atomicOr(&g_abi_error, kErrWaitTimeout);
+}
+
+// Source of the self-check's real copies (its contents are never used).
+__device__ __align__(16) uint8_t g_probe_src[64];
+
+constexpr int kProbeWarps = 8, kProbeSlots = 2, kProbeBytes = 16;
+
+// The tensor-core kernels' way of giving up, in one CTA of 8 warps: every warp fills
+// a 2-slot ring, warp `stuck` arms its mbarriers but issues no copy, so its bounded
+// wait runs out while the other warps consume real copies and go on to the CTA-wide
+// barrier that ends the round. The stuck warp must flag the error word and the CTA's
+// abort word and reach that barrier too; after it every warp sees the abort, lets its
+// copies land and returns. out int64 [8][4], per warp: 1 if its wait gave up; 1 if
+// it passed the barrier and saw the abort; copies still outstanding when it left the
+// round; nanoseconds from the first wait to the barrier.
+__global__ void cta_abort_kernel(int64_t *out, int stuck)
+{
+    __shared__ __align__(128) uint8_t ring[kProbeWarps][kProbeSlots][kProbeBytes];
+    __shared__ __align__(8) uint64_t bars[kProbeWarps][kProbeSlots];
+    __shared__ uint32_t cta_abort;
+    const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+    if (threadIdx.x == 0) cta_abort = 0u;
+    int outstanding = 0;
+    if (lane == 0) {
+        for (int s = 0; s < kProbeSlots; ++s) mbar_init(&bars[warp][s], 1);
+        fence_barrier_init();
+        const uint64_t pol = policy_evict_first();
+        for (int s = 0; s < kProbeSlots; ++s) {
+            mbar_arrive_expect_tx(&bars[warp][s], kProbeBytes);
+            if (warp != stuck) bulk_copy_g2s(ring[warp][s], g_probe_src + kProbeBytes * s, kProbeBytes, &bars[warp][s], pol);
+            ++outstanding;
+        }
+    }
+    __syncthreads();   // the prologue's barrier
+    int slot = 0;
+    uint32_t phase = 0;
+    bool failed = false;
+    const uint64_t t0 = globaltimer_ns();
+    for (int i = 0; i < kProbeSlots; ++i) {
+        if (!mbar_wait_bounded(&bars[warp][slot], phase)) {
+            if (lane == 0) note_wait_timeout(&g_abi_error, &cta_abort);
+            failed = true;
+            break;
+        }
+        --outstanding;
+        if (++slot == kProbeSlots) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+    __syncthreads();   // the round's barrier
+    const uint64_t t1 = globaltimer_ns();
+    const bool abort = cta_abort != 0u;
+    if (lane == 0) {
+        out[4 * warp] = failed ? 1 : 0;
+        out[4 * warp + 1] = abort ? 1 : 0;
+        out[4 * warp + 2] = outstanding;
+        out[4 * warp + 3] = static_cast<int64_t>(t1 - t0);
+    }
+    if (abort) {
+        if (lane == 0) drain_ring(bars[warp], kProbeSlots, slot, phase, outstanding);
+        return;
+    }
 }
 
 qmv_status zero_fill(float *y, int M, int64_t N, cudaStream_t s)
@@ -512,11 +568,40 @@ qmv_status qmv_debug_plan_q4(int q4k, int M, int64_t N, int64_t K, int n_inputs,
     return QMV_OK;
 }
 
+qmv_status qmv_debug_plan_wq(int fp4, int M, int64_t K, int count, const int64_t *N, int aligned16, int sm_count,
+                             int smem_optin, int smem_per_sm, const int *ctas_by_regs, int64_t *out)
+{
+    if (!out || !N) return QMV_ERR_NULL;
+    if (count < 1 || count > kMaxGroup || M < 1 || M > kMaxRowsW || K < 1 || sm_count < 1 || smem_optin < 1 ||
+        smem_per_sm < 1)
+        return QMV_ERR_SHAPE;
+    for (int i = 0; i < count; ++i) {
+        qmv_status st = check_shape(M, N[i], K, count > 1 ? (fp4 ? 256 : 128) : (fp4 ? 16 : 1), kMaxRowsW);
+        if (st != QMV_OK) return st;
+    }
+    static const int kLaunchBoundsCtas[3] = {3, 2, 1};   // the kernels' minimum CTAs per SM
+    const int *regs = ctas_by_regs ? ctas_by_regs : kLaunchBoundsCtas;
+    for (int i = 0; i < 3; ++i)
+        if (regs[i] < 1) return QMV_ERR_SHAPE;
+    const DeviceInfo dev{0, sm_count, smem_optin, smem_per_sm};
+    const cudaError_t e = debug_plan_wq(fp4 != 0, dev, M, K, count, N, aligned16 != 0, regs, out);
+    return e == cudaSuccess ? QMV_OK : (e == cudaErrorInvalidValue ? QMV_ERR_SHAPE : QMV_ERR_CUDA);
+}
+
 qmv_status qmv_debug_wait_bound(int64_t *out, qmv_stream_t stream)
 {
     if (!out) return QMV_ERR_NULL;
     if (misaligned(out, alignof(int64_t))) return QMV_ERR_ALIGN;
     wait_bound_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(out);
+    return from_cuda(cudaGetLastError());
+}
+
+qmv_status qmv_debug_cta_abort(int64_t *out, int stuck_warp, qmv_stream_t stream)
+{
+    if (!out) return QMV_ERR_NULL;
+    if (misaligned(out, alignof(int64_t))) return QMV_ERR_ALIGN;
+    if (stuck_warp < 0 || stuck_warp >= kProbeWarps) return QMV_ERR_SHAPE;
+    cta_abort_kernel<<<1, 32 * kProbeWarps, 0, static_cast<cudaStream_t>(stream)>>>(out, stuck_warp);
     return from_cuda(cudaGetLastError());
 }
 

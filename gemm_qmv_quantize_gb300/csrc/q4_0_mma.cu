@@ -62,16 +62,17 @@ struct MmaParams {
 };
 
 struct MmaLayout {
-    uint32_t off_bar, off_act, off_red, total;
+    uint32_t off_bar, off_abort, off_act, off_red, total;
 };
 
-// Shared memory: per-warp rings of boxes, their mbarriers, the staged activations,
-// the round's partial sums [warp][B * 16 rows][9].
+// Shared memory: per-warp rings of boxes, their mbarriers, the CTA's abort word, the
+// staged activations, the round's partial sums [warp][B * 16 rows][9].
 __host__ __device__ inline MmaLayout mma_layout(int S, int B, int nx, int nb, int M, bool q4k)
 {
     MmaLayout L;
     L.off_bar = static_cast<uint32_t>(kWarps * S * kBox);
-    L.off_act = (L.off_bar + static_cast<uint32_t>(kWarps * S) * 8u + 15u) & ~15u;
+    L.off_abort = L.off_bar + static_cast<uint32_t>(kWarps * S) * 8u;
+    L.off_act = (L.off_abort + 4u + 15u) & ~15u;
     L.off_red = L.off_act + static_cast<uint32_t>(nx) * static_cast<uint32_t>(nb) * act_block_bytes(M, q4k);
     L.total = L.off_red + static_cast<uint32_t>(kWarps * B * kTile * kRedPitch) * 4u;
     return L;
@@ -230,9 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1) q4_0_mma_kernel(const __grid_cons
                    static_cast<int>(gridDim.x);
     const int tb0 = warp / nsteps, s0 = warp - tb0 * nsteps;
     int p_lt = tb0, p_step = s0, p_rend = min(B, nt);
+    int outstanding = 0;   // lane 0: copies issued and not yet consumed
     auto issue = [&](int slot) {
         int mi, row0;
         locate(static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) * p_lt, mi, row0);
+        ++outstanding;
         mbar_arrive_expect_tx(&bars[slot], kBox);
         tma_load_2d(ring + slot * kBox, &p.tm[mi], p_step * kUnitBytes, row0, &bars[slot], pol);
         p_step += kWarps;
@@ -247,6 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1) q4_0_mma_kernel(const __grid_cons
         }
     };
     auto pending = [&]() { return p_lt < p_rend; };
+    // set when a warp's bounded wait gave up; zeroed before the prologue's barrier
+    volatile uint32_t &cta_abort = *reinterpret_cast<volatile uint32_t *>(smem + L.off_abort);
+    if (tid == 0) cta_abort = 0u;
     if (lane == 0) {
         for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
         fence_barrier_init();
@@ -279,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4_0_mma_kernel(const __grid_cons
         };
         int mi = 0, row0 = 0, tile_of = -1;
         const uint8_t *xa = act;
+        bool failed = false;
         for (int tb = tb0, s = s0; tb < bt;) {
             if (tb != cur) {
                 flush(tb);
@@ -290,17 +297,12 @@ __global__ void __launch_bounds__(kThreads, 1) q4_0_mma_kernel(const __grid_cons
                 tile_of = tile;
                 xa = act + static_cast<int64_t>(p.xslot[mi]) * nb * rb;
             }
-            if (!mbar_wait_sleep(&bars[slot], phase)) {
-                if (lane == 0) {
-                    atomicOr(&g_q4m_error, kErrWaitTimeout);
-                    // let this warp's other copies land before the CTA can release its memory
-                    for (int i = 1; i < S; ++i) {
-                        const int sl = (slot + i) % S;
-                        (void)mbar_wait_sleep(&bars[sl], sl > slot ? phase : phase ^ 1u);
-                    }
-                }
-                return;
+            if (!mbar_wait_bounded(&bars[slot], phase)) {
+                if (lane == 0) note_wait_timeout(&g_q4m_error, &cta_abort);
+                failed = true;
+                break;   // skip the rest of the round, up to its barrier
             }
+            --outstanding;
             const uint8_t *box = ring + slot * kBox;
             const uint8_t *rg = box + gid * kUnitBytes, *rh = box + (gid + 8) * kUnitBytes;
             if constexpr (kQ4K) {
@@ -398,9 +400,19 @@ __global__ void __launch_bounds__(kThreads, 1) q4_0_mma_kernel(const __grid_cons
                 ++tb;
             }
         }
-        if (kDots) continue;   // no reduction: every block dot went out directly
+        if (kDots) {   // no reduction and no CTA-wide barrier: every block dot went out directly
+            if (failed) {
+                if (lane == 0) drain_ring(bars, S, slot, phase, outstanding);
+                return;
+            }
+            continue;
+        }
         flush(bt);
         __syncthreads();
+        if (cta_abort) {   // a warp gave up waiting: the whole CTA leaves here, its copies landed
+            if (lane == 0) drain_ring(bars, S, slot, phase, outstanding);
+            return;
+        }
         for (int e = tid; e < bt * kTile * 8; e += kThreads) {
             const int rr = e >> 3, m = e & 7, tb = rr / kTile, r = rr - tb * kTile;
             if (m >= p.M) continue;

@@ -556,12 +556,12 @@ __global__ void __launch_bounds__(kActRegs ? (M == 1 ? kActRegsThreads : kStream
     int slot = 0;
     uint32_t phase = 0;
     for (int c = 0; c < nchunks; ++c) {
-        if (!mbar_wait_sleep(&bars[slot], phase)) {
+        if (!mbar_wait_bounded(&bars[slot], phase)) {
+            // chunks c .. c + S - 1 are in flight; no CTA-wide barrier follows the
+            // prologue in this kernel, so the warp may leave once they have landed
             if (lane == 0) {
-                atomicOr(&g_q4_error, kErrWaitTimeout);
-                // let this warp's other copies land before the CTA can release its memory
-                for (int s = 1; s < S && c + s < nchunks; ++s)
-                    (void)mbar_wait_sleep(&bars[(c + s) % S], ((c + s) / S) & 1);
+                note_wait_timeout(&g_q4_error, nullptr);
+                drain_ring(bars, S, slot, phase, min(S, nchunks - c));
             }
             return;
         }

@@ -8,7 +8,6 @@
 namespace qmv {
 
 constexpr uint32_t kErrWaitTimeout = 1u;   // error-word bit: an mbarrier wait gave up
-constexpr uint32_t kMaxWaitIters = 1u << 24;
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p)
 {
@@ -67,22 +66,66 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t pari
     return ok != 0;
 }
 
-// Bounded wait: false if the phase did not complete within kMaxWaitIters polls.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+// %globaltimer in ns; the memory clobber keeps the read in place relative to the
+// barriers and waits around it.
+__device__ __forceinline__ uint64_t globaltimer_ns()
 {
-    for (uint32_t i = 0; i < kMaxWaitIters; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t)::"memory");
+    return t;
+}
+
+// Bounds of every mbarrier wait. A poll is one try_wait that may suspend the thread
+// (hint: 1 ms) until the phase completes; an incomplete phase returns it after a few
+// microseconds. The wait gives up once kWaitLimitNs of %globaltimer time AND
+// kMinWaitPolls polls have passed -- a context switched off the GPU polls nothing,
+// so elapsed time alone does not end a wait -- and after kMaxWaitPolls polls in any
+// case (a clock that stood still). A weight copy lands within microseconds, even on
+// a contended memory system, so the bound is far above any valid wait.
+constexpr uint64_t kWaitLimitNs = 500ull * 1000ull * 1000ull;   // 0.5 s
+constexpr uint32_t kMinWaitPolls = 1024u;
+constexpr uint32_t kMaxWaitPolls = 1u << 21;
+
+// Bounded wait on phase `parity` of `bar`: true when it completed, false when the
+// bound ran out. The first poll reads no clock (the common case: the copy landed).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs)
+{
+    if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1; i < kMaxWaitPolls; ++i) {
+        if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
+        if (i >= kMinWaitPolls && globaltimer_ns() - t0 >= limit_ns) return false;
+    }
     return false;
 }
 
-// Bounded sleeping wait: at most kMaxSleepWaits suspensions of up to 1 ms each
-// (about 2 s in all) before giving up.
-constexpr uint32_t kMaxSleepWaits = 2000u;
-__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity)
+// ---------------------------------------------------------------- giving up without a fault
+
+// A warp whose bounded wait gave up does not leave the CTA on its own: the other warps
+// may be on their way to a CTA-wide barrier, which would then wait for a thread that
+// has exited. Instead the warp's lane 0 flags the error word and the CTA's abort word
+// (shared memory, zeroed before the CTA's first barrier), the warp skips the rest of
+// its work up to the CTA's next barrier, and after that barrier every warp reads the
+// abort word, lets its own copies in flight land (drain_ring) and returns: all threads
+// leave together and no copy writes into the memory of a CTA that has exited.
+__device__ __forceinline__ void note_wait_timeout(uint32_t *err_word, volatile uint32_t *cta_abort)
 {
-    for (uint32_t i = 0; i < kMaxSleepWaits; ++i)
-        if (mbar_try_wait_sleep(bar, parity, 1000000u)) return true;
-    return false;
+    atomicOr(err_word, kErrWaitTimeout);
+    if (cta_abort) *cta_abort = 1u;
+}
+
+// Lane 0: wait (bounded) for the `outstanding` copies of a warp's ring of S slots that
+// were issued and not yet consumed, the first at ring position `slot`, phase `parity`
+// (a completed wait consumes its copy; the one whose wait gave up is still counted).
+__device__ __forceinline__ void drain_ring(uint64_t *bars, int S, int slot, uint32_t parity, int outstanding)
+{
+    for (int i = 0; i < outstanding; ++i) {
+        (void)mbar_wait_bounded(&bars[slot], parity);
+        if (++slot == S) {
+            slot = 0;
+            parity ^= 1u;
+        }
+    }
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first()

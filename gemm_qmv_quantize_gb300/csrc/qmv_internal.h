@@ -113,6 +113,14 @@ Route plan_fp8(const uint8_t *w, const uint16_t *x, int64_t K);
 cudaError_t launch_fp8(Route r, const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M, int64_t K,
                        cudaStream_t s);
 
+// The NVFP4 / FP8 plan of one call (count matrices of N[i] rows) on a device given by
+// its limits, with CTAs per SM from an occupancy model instead of the device (no CUDA
+// call): ctas_by_regs = what the registers of the (8 warps, 1 row tile), (8 warps, 2
+// row tiles) and 16-warp kernels allow. out: route, chunks, rows of the first chunk,
+// warps, slots, staged, passes, tiles per round, CTAs per SM, grid, shared memory.
+cudaError_t debug_plan_wq(bool fp4, const DeviceInfo &dev, int M, int64_t K, int count, const int64_t *N,
+                          bool aligned16, const int ctas_by_regs[3], int64_t out[11]);
+
 // Device error words of each translation unit (read synchronously; optionally cleared).
 cudaError_t read_error_word_q4_0(uint32_t *out, bool clear);
 cudaError_t read_error_word_wq(uint32_t *out, bool clear);

@@ -106,19 +106,20 @@ constexpr int kScalesBox = kRowsPerCta * 16;          // 256 bytes: 16 rows x 16
 __host__ __device__ constexpr int red_pitch(int mt) { return 8 * mt + 1; }
 
 struct WqLayout {
-    uint32_t off_codes, off_scales, off_bar, off_red, off_x, total;
+    uint32_t off_codes, off_scales, off_bar, off_abort, off_red, off_x, total;
 };
 
 // Shared memory of W warps: per-warp rings of codes boxes (1024-byte aligned for the
-// swizzle), of scale boxes, their mbarriers, the round's partial sums
-// [warp][B * 16 rows][8 mt + 1], then the staged activations.
+// swizzle), of scale boxes, their mbarriers, the CTA's abort word, the round's
+// partial sums [warp][B * 16 rows][8 mt + 1], then the staged activations.
 __host__ __device__ inline WqLayout wq_layout(int S, int B, uint32_t xbytes, int mt, int W)
 {
     WqLayout L;
     L.off_codes = 0;
     L.off_scales = static_cast<uint32_t>(W * S * kCodesBox);
     L.off_bar = L.off_scales + static_cast<uint32_t>(W * S * kScalesBox);
-    L.off_red = (L.off_bar + static_cast<uint32_t>(W * S) * 8u + 15u) & ~15u;
+    L.off_abort = L.off_bar + static_cast<uint32_t>(W * S) * 8u;
+    L.off_red = (L.off_abort + 4u + 15u) & ~15u;
     L.off_x = (L.off_red + static_cast<uint32_t>(W * B * kRowsPerCta * red_pitch(mt)) * 4u + 127u) & ~127u;
     L.total = L.off_x + xbytes;
     return L;
@@ -209,7 +210,9 @@ __global__ void __launch_bounds__(32 * kW, kW == 16 ? 1 : (kMT == 1 ? 3 : 2))
     settle();
     int64_t p_tile = -1, p_row0 = 0;   // the producer's last located tile
     int p_mi = 0;
+    int outstanding = 0;   // lane 0: copies issued and not yet consumed
     auto issue = [&](int slot) {
+        ++outstanding;
         const int64_t tile = blockIdx.x + static_cast<int64_t>(gridDim.x) * p_lt;
         if (tile != p_tile) {
             locate(tile, p_mi, p_row0);
@@ -230,6 +233,9 @@ __global__ void __launch_bounds__(32 * kW, kW == 16 ? 1 : (kMT == 1 ? 3 : 2))
     // rounds before the last hold a multiple of kW items, so a warp with an item in
     // one round has one in every round of the pass but perhaps the last
     auto pending = [&]() { return p_ps < P && p_lt < p_rend; };
+    // set when a warp's bounded wait gave up; zeroed before the prologue's barrier
+    volatile uint32_t &cta_abort = *reinterpret_cast<volatile uint32_t *>(smem + L.off_abort);
+    if (tid == 0) cta_abort = 0u;
     if (lane == 0) {
         for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
         fence_barrier_init();
@@ -296,10 +302,11 @@ __global__ void __launch_bounds__(32 * kW, kW == 16 ? 1 : (kMT == 1 ? 3 : 2))
                     flush(tb);
                     cur = tb;
                 }
-                if (!mbar_wait_sleep(&bars[slot], phase)) {
-                    if (lane == 0) atomicOr(&g_wq_error, kErrWaitTimeout);
-                    return;
+                if (!mbar_wait_bounded(&bars[slot], phase)) {
+                    if (lane == 0) note_wait_timeout(&g_wq_error, &cta_abort);
+                    break;   // skip the rest of the round, up to its barrier
                 }
+                --outstanding;
                 // codes of rows gid and gid+8: 16-byte chunks 2t, 2t+1 of the row (swizzled by row & 7)
                 const uint8_t *cb = codes_ring + slot * kCodesBox;
                 const uint4 a0 = *reinterpret_cast<const uint4 *>(cb + gid * 128 + 16 * ((2 * t) ^ gid));
@@ -399,6 +406,10 @@ __global__ void __launch_bounds__(32 * kW, kW == 16 ? 1 : (kMT == 1 ? 3 : 2))
             }
             flush(bt);
             __syncthreads();
+            if (cta_abort) {   // a warp gave up waiting: the whole CTA leaves here, its copies landed
+                if (lane == 0) drain_ring(bars, S, slot, phase, outstanding);
+                return;
+            }
             for (int e = tid; e < bt * kRowsPerCta * 8 * kMT; e += kT) {
                 const int rr = e / (8 * kMT), m = e - rr * (8 * kMT), tb = rr / kRowsPerCta, r = rr - tb * kRowsPerCta;
                 int mi;
@@ -461,6 +472,123 @@ __global__ void __launch_bounds__(kThreads) wq_generic_kernel(const uint8_t *__r
     }
 }
 
+// The tensor-core kernel's launch plan for one call (or one chunk of <= 16 rows).
+struct WqPlan {
+    int W = 0, S = 0, B = 0, P = 1, occ = 0;
+    bool xsmem = false;
+    int64_t grid = 0;
+    uint32_t smem = 0;   // dynamic shared memory, bytes
+};
+
+// Plan candidates (warps, ring slots, activations in shared memory), in order of preference.
+struct WqCand {
+    int W, S;
+    bool xs;
+};
+constexpr WqCand kWqCands[] = {{8, 3, true}, {8, 4, true}, {8, 2, true}, {16, 3, true}, {16, 2, true},
+                               {8, 4, false}, {8, 3, false}, {8, 2, false}};
+constexpr int kWqCandCount = static_cast<int>(sizeof(kWqCands) / sizeof(kWqCands[0]));
+
+// Chooses the plan of `ntiles` 16-row tiles at M <= 16 rows. occ_of(W, xs, dyn, &occ)
+// gives the CTAs per SM of a candidate with `dyn` bytes of dynamic shared memory (the
+// occupancy API on a device, a model in the introspection call). Returns
+// cudaErrorInvalidValue when no candidate fits.
+template <typename OccFn>
+cudaError_t choose_wq_plan(bool fp4, const DeviceInfo &dev, int64_t ntiles, int M, int64_t K, OccFn occ_of,
+                           WqPlan *out)
+{
+    const int mt = M > 8 ? 2 : 1;
+    const int step_k = fp4 ? 2 * kStepBytes : kStepBytes;   // k per step
+    const int64_t nsteps_all = K / step_k;
+    // tiles per round for `ns` steps per pass and W warps: a multiple of W / gcd(ns, W),
+    // so every warp gets the same number of steps, and enough for 8 steps per warp
+    // between the round's barriers
+    auto round_unit = [](int64_t ns, int W) {
+        int gcd = W;
+        while (ns % gcd) gcd >>= 1;   // gcd(ns, W): W is a power of two
+        return static_cast<int>(W / gcd);
+    };
+    auto round_tiles = [&](int64_t ns, int W) {
+        const int unit = round_unit(ns, W);
+        int b = unit;
+        while (b * ns < 8 * W && b + unit <= kMaxRound) b += unit;
+        return b;
+    };
+    // Candidates scored by the tail they leave: whole tiles over `grid` CTAs take
+    // ceil(tiles / grid) rounds, so the busiest CTA holds waves * grid / tiles times the
+    // mean. Within 15 % of the mean a candidate scores 1, else its imbalance; fewer than
+    // 16 resident warps per SM add 0.5 (too few to hide the decode latency), each pass
+    // over K beyond the first adds 1 (a pass repeats the per-round reduction), every 8
+    // resident warps take 0.05 off (the kernel is bound by latency, and more warps hide
+    // more of it: at M = 1 three 8-warp CTAs with 2 slots beat two with 4 on balanced
+    // shapes); ties keep the earlier candidate. Activations stay in shared memory
+    // whenever they fit (re-read through L1 they thrash it at M = 8); 16 warps share one
+    // staged copy where 8-warp CTAs would fit only one per SM. At M <= 2, where the
+    // activations fit in L1, an unstaged candidate may win on balance.
+    const uint32_t x_cap = static_cast<uint32_t>(env_int("QMV_WQ_XSMEM_MAX", 200 * 1024));
+    const int p_env = env_int("QMV_WQ_PASSES", 0);
+    const int s_env = env_int("QMV_WQ_SLOTS", 0);
+    const int w_env = env_int("QMV_WQ_WARPS", 0);
+    int best = -1;
+    double best_score = 1e30;
+    WqPlan bp;
+    for (int c = 0; c < kWqCandCount; ++c) {
+        const WqCand &cd = kWqCands[c];
+        if (!cd.xs && best >= 0 && kWqCands[best].xs && (M > 2 || best_score <= 1.15)) break;
+        if (w_env > 0 && cd.W != w_env) continue;
+        const int Wc = cd.W;
+        const int Sc = s_env > 0 ? std::min(8, s_env) : cd.S;
+        // staged: the fewest passes (dividing the steps) whose slice of x fits, with
+        // fewer tiles per round (a smaller reduction buffer) where that makes it fit
+        int Pc = 0, Bc = 0;
+        uint32_t dyn = 0;
+        for (int pp = 1; pp <= (cd.xs ? 8 : 1) && Pc == 0; ++pp) {
+            if (p_env > 0 && cd.xs && pp != p_env) continue;
+            if (nsteps_all % pp) continue;
+            const int64_t ns = nsteps_all / pp;
+            const uint64_t xb = cd.xs ? static_cast<uint64_t>(M) * xs_row_stride(ns * step_k) : 0;
+            if (xb > x_cap) continue;
+            const int unit = round_unit(ns, Wc);
+            if (unit > kMaxRound) continue;
+            int b = round_tiles(ns, Wc);
+            uint32_t d = wq_layout(Sc, b, static_cast<uint32_t>(xb), mt, Wc).total + 1024;
+            while (d > static_cast<uint32_t>(dev.smem_optin) && b > unit) {
+                b -= unit;
+                d = wq_layout(Sc, b, static_cast<uint32_t>(xb), mt, Wc).total + 1024;
+            }
+            if (d > static_cast<uint32_t>(dev.smem_optin)) continue;
+            Pc = pp;
+            Bc = b;
+            dyn = d;
+        }
+        if (Pc == 0) continue;
+        int occ = 0;
+        const cudaError_t e = occ_of(Wc, cd.xs, dyn, &occ);
+        if (e != cudaSuccess) return e;
+        occ = std::min(occ, 4);
+        if (occ < 1) continue;
+        const int64_t g = std::min<int64_t>(ntiles, static_cast<int64_t>(dev.sm_count) * occ);
+        const double imb = static_cast<double>((ntiles + g - 1) / g * g) / static_cast<double>(ntiles);
+        const double score =
+            (imb <= 1.15 ? 1.0 : imb) + (occ * Wc < 16 ? 0.5 : 0.0) + (Pc - 1) - 0.05 * (occ * Wc / 8);
+        if (score < best_score) {
+            best_score = score;
+            best = c;
+            bp.W = Wc;
+            bp.S = Sc;
+            bp.xsmem = cd.xs;
+            bp.B = Bc;
+            bp.P = Pc;
+            bp.occ = occ;
+            bp.grid = g;
+            bp.smem = dyn;
+        }
+    }
+    if (best < 0) return cudaErrorInvalidValue;
+    *out = bp;
+    return cudaSuccess;
+}
+
 template <bool kFp4>
 cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M, int64_t K,
                       cudaStream_t s)
@@ -484,104 +612,22 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const 
         int64_t ntiles = 0;
         for (int i = 0; i < grp.count; ++i) ntiles += (grp.N[i] + kRowsPerCta - 1) / kRowsPerCta;
         if (ntiles == 0) return cudaSuccess;
-        constexpr int kStepK = kFp4 ? 2 * kStepBytes : kStepBytes;   // k per step
-        const int64_t nsteps_all = K / kStepK;
-        // tiles per round for `ns` steps per pass and W warps: a multiple of W / gcd(ns, W),
-        // so every warp gets the same number of steps, and enough for 8 steps per warp
-        // between the round's barriers
-        auto round_unit = [](int64_t ns, int W) {
-            int gcd = W;
-            while (ns % gcd) gcd >>= 1;   // gcd(ns, W): W is a power of two
-            return static_cast<int>(W / gcd);
-        };
-        auto round_tiles = [&](int64_t ns, int W) {
-            const int unit = round_unit(ns, W);
-            int b = unit;
-            while (b * ns < 8 * W && b + unit <= kMaxRound) b += unit;
-            return b;
-        };
-        // Candidates (warps, ring slots, activations in shared memory), scored by the
-        // tail they leave: whole tiles over `grid` CTAs take ceil(tiles / grid) rounds, so
-        // the busiest CTA holds waves * grid / tiles times the mean. Within 15 % of the mean
-        // a candidate scores 1, else its imbalance; fewer than 16 resident warps per SM
-        // add 0.5 (too few to hide the decode latency), each pass over K beyond the first
-        // adds 1 (a pass repeats the per-round reduction), every 8 resident warps take
-        // 0.05 off (the kernel is bound by latency, and more warps hide more of it: at
-        // M = 1 three 8-warp CTAs with 2 slots beat two with 4 on balanced shapes); ties
-        // keep the earlier candidate. Activations stay in shared memory whenever they fit (re-read
-        // through L1 they thrash it at M = 8); 16 warps share one staged copy where 8-warp
-        // CTAs would fit only one per SM. At M <= 2, where the activations fit in L1, an
-        // unstaged candidate may win on balance.
-        const uint32_t x_cap = static_cast<uint32_t>(env_int("QMV_WQ_XSMEM_MAX", 200 * 1024));
-        const int p_env = env_int("QMV_WQ_PASSES", 0);
-        const int s_env = env_int("QMV_WQ_SLOTS", 0);
-        const int w_env = env_int("QMV_WQ_WARPS", 0);
-        struct Cand { int W, S; bool xs; };
-        const Cand cands[] = {{8, 3, true}, {8, 4, true}, {8, 2, true}, {16, 3, true}, {16, 2, true},
-                              {8, 4, false}, {8, 3, false}, {8, 2, false}};
-        constexpr int kCands = static_cast<int>(sizeof(cands) / sizeof(cands[0]));
-        int best = -1, best_occ = 0, best_B = 0, best_P = 1;
-        double best_score = 1e30;
-        for (int c = 0; c < kCands; ++c) {
-            if (!cands[c].xs && best >= 0 && cands[best].xs && (M > 2 || best_score <= 1.15)) break;
-            if (w_env > 0 && cands[c].W != w_env) continue;
-            const int Wc = cands[c].W;
-            const int Sc = s_env > 0 ? std::min(8, s_env) : cands[c].S;
-            // staged: the fewest passes (dividing the steps) whose slice of x fits, with
-            // fewer tiles per round (a smaller reduction buffer) where that makes it fit
-            int Pc = 0, Bc = 0;
-            uint32_t dyn = 0;
-            for (int pp = 1; pp <= (cands[c].xs ? 8 : 1) && Pc == 0; ++pp) {
-                if (p_env > 0 && cands[c].xs && pp != p_env) continue;
-                if (nsteps_all % pp) continue;
-                const int64_t ns = nsteps_all / pp;
-                const uint64_t xb = cands[c].xs ? static_cast<uint64_t>(M) * xs_row_stride(ns * kStepK) : 0;
-                if (xb > x_cap) continue;
-                const int unit = round_unit(ns, Wc);
-                if (unit > kMaxRound) continue;
-                int b = round_tiles(ns, Wc);
-                uint32_t d = wq_layout(Sc, b, static_cast<uint32_t>(xb), mt, Wc).total + 1024;
-                while (d > static_cast<uint32_t>(dev.smem_optin) && b > unit) {
-                    b -= unit;
-                    d = wq_layout(Sc, b, static_cast<uint32_t>(xb), mt, Wc).total + 1024;
-                }
-                if (d > static_cast<uint32_t>(dev.smem_optin)) continue;
-                Pc = pp;
-                Bc = b;
-                dyn = d;
-            }
-            if (Pc == 0) continue;
-            const Kern kc = kernel_of(cands[c].xs, Wc);
+        auto occ_of = [&](int W, bool xs, uint32_t dyn, int *occ) -> cudaError_t {
+            const Kern kc = kernel_of(xs, W);
             cudaError_t e = ensure_smem_attr(reinterpret_cast<const void *>(kc), dev.smem_optin,
-                                             cands[c].xs ? cudaSharedmemCarveoutMaxShared : -1);
+                                             xs ? cudaSharedmemCarveoutMaxShared : -1);
             if (e != cudaSuccess) return e;
-            int occ = 0;
-            if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kc, 32 * Wc, dyn)) != cudaSuccess) return e;
-            occ = std::min(occ, 4);
-            if (occ < 1) continue;
-            const int64_t g = std::min<int64_t>(ntiles, static_cast<int64_t>(dev.sm_count) * occ);
-            const double imb = static_cast<double>((ntiles + g - 1) / g * g) / static_cast<double>(ntiles);
-            const double score = (imb <= 1.15 ? 1.0 : imb) + (occ * Wc < 16 ? 0.5 : 0.0) + (Pc - 1) -
-                                 0.05 * (occ * Wc / 8);
-            if (score < best_score) {
-                best_score = score;
-                best = c;
-                best_occ = occ;
-                best_B = Bc;
-                best_P = Pc;
-            }
-        }
-        if (best < 0) return cudaErrorInvalidValue;
-        const int W = cands[best].W;
-        const int S = s_env > 0 ? std::min(8, s_env) : cands[best].S;
-        const bool xsmem = cands[best].xs;
-        const int B = best_B, P = best_P;
+            return cudaOccupancyMaxActiveBlocksPerMultiprocessor(occ, kc, 32 * W, dyn);
+        };
+        WqPlan plan;
+        cudaError_t pe = choose_wq_plan(kFp4, dev, ntiles, M, K, occ_of, &plan);
+        if (pe != cudaSuccess) return pe;
+        const int W = plan.W, S = plan.S, B = plan.B, P = plan.P;
+        const bool xsmem = plan.xsmem;
         const uint32_t xbytes = xsmem ? static_cast<uint32_t>(M) * xs_row_stride(K / P) : 0u;
         const WqLayout L = wq_layout(S, B, xbytes, mt, W);
         cfg.blockDim = dim3(static_cast<unsigned>(32 * W));
-        const int per_sm = std::min(4, best_occ);
-        cfg.gridDim =
-            dim3(static_cast<unsigned>(std::min<int64_t>(ntiles, static_cast<int64_t>(dev.sm_count) * per_sm)));
+        cfg.gridDim = dim3(static_cast<unsigned>(plan.grid));
         WqParams p{};
         p.count = grp.count;
         int64_t t = 0;
@@ -608,7 +654,7 @@ cudaError_t launch_wq(Route r, const DeviceInfo &dev, const WqGroup &grp, const 
         if (env_int("QMV_PLAN_LOG", 0))   // diagnostic: the chosen plan, one line per launch
             std::fprintf(stderr, "wq plan: fmt=%s M=%d K=%lld tiles=%lld W=%d S=%d xsmem=%d P=%d B=%d occ=%d grid=%u smem=%u\n",
                          kFp4 ? "nvfp4" : "fp8", M, static_cast<long long>(K), static_cast<long long>(ntiles), W, S,
-                         xsmem ? 1 : 0, P, B, best_occ, cfg.gridDim.x, static_cast<unsigned>(cfg.dynamicSmemBytes));
+                         xsmem ? 1 : 0, P, B, plan.occ, cfg.gridDim.x, static_cast<unsigned>(cfg.dynamicSmemBytes));
         return cudaLaunchKernelEx(&cfg, kern, p, x, M, K, S, B, P);
     }
     if (grp.count != 1) return cudaErrorInvalidValue;   // groups need the tensor-core kernel
@@ -679,6 +725,43 @@ cudaError_t launch_wq_chunked(Route r, const DeviceInfo &dev, const WqGroup &grp
 }
 
 }  // namespace
+
+cudaError_t debug_plan_wq(bool fp4, const DeviceInfo &dev, int M, int64_t K, int count, const int64_t *N,
+                          bool aligned16, const int ctas_by_regs[3], int64_t out[11])
+{
+    for (int i = 0; i < 11; ++i) out[i] = 0;
+    const bool mma = aligned16 && K % (fp4 ? 256 : 128) == 0;
+    if (!mma) {   // the generic kernel, 8 activation rows per launch
+        if (count != 1) return cudaErrorInvalidValue;
+        out[0] = fp4 ? kRouteNvfp4Generic : kRouteFp8Generic;
+        out[1] = (M + 7) / 8;
+        out[2] = std::min(8, M);
+        return cudaSuccess;
+    }
+    int64_t ntiles = 0;
+    for (int i = 0; i < count; ++i) ntiles += (N[i] + kRowsPerCta - 1) / kRowsPerCta;
+    const int nch = M > 16 ? (M + 15) / 16 : 1;
+    const int mc = (M + nch - 1) / nch;   // the first (largest) chunk
+    out[0] = fp4 ? kRouteNvfp4Mma : kRouteFp8Mma;
+    out[1] = nch;
+    out[2] = mc;
+    if (ntiles == 0) return cudaSuccess;
+    const int mt = mc > 8 ? 2 : 1;
+    // CTAs per SM: the registers' limit of the variant, the shared memory of the SM
+    // less 1 KB reserved per CTA, and 64 resident warps
+    auto occ_model = [&](int W, bool, uint32_t dyn, int *occ) -> cudaError_t {
+        const int by_regs = ctas_by_regs[W == 16 ? 2 : (mt == 2 ? 1 : 0)];
+        *occ = std::min({by_regs, dev.smem_per_sm / static_cast<int>(dyn + 1024), 64 / W});
+        return cudaSuccess;
+    };
+    WqPlan plan;
+    const cudaError_t e = choose_wq_plan(fp4, dev, ntiles, mc, K, occ_model, &plan);
+    if (e != cudaSuccess) return e;
+    const int64_t v[8] = {plan.W, plan.S, plan.xsmem ? 1 : 0, plan.P, plan.B, plan.occ, plan.grid,
+                          static_cast<int64_t>(plan.smem)};
+    for (int i = 0; i < 8; ++i) out[3 + i] = v[i];
+    return cudaSuccess;
+}
 
 cudaError_t launch_nvfp4(Route r, const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M, int64_t K,
                          cudaStream_t s)

@@ -286,6 +286,36 @@ QMV_API qmv_status qmv_debug_plan_q4(int q4k, int M, int64_t N, int64_t K, int n
                                      int sm_count, int smem_optin, int smem_per_sm, int64_t *out);
 
 /*
+ * The launch plan the NVFP4 / FP8 heuristic picks for one call (count = 1) or one
+ * grouped launch (count 1..8 matrices of N[i] rows, the same M and K) on a device
+ * given by its limits, with no CUDA call (usable without a GPU). The planner scores
+ * candidate plans (warps, ring slots, activations staged in shared memory or not,
+ * passes over K) by the whole-tile tail they leave on the device's CTAs; the CTAs
+ * per SM of a candidate come from a model here -- the least of ctas_by_regs, the SM's
+ * shared memory over the candidate's (plus 1 KB reserved per CTA), and 64 resident
+ * warps -- where a launch asks the device's occupancy calculator.
+ *   fp4           1 = NVFP4, 0 = FP8.
+ *   M, K, N       as in qgemm_nvfp4_w4a16 / qgemm_fp8_w8a16 (M 1..96); N HOST int64
+ *                 [count]. Above 16 rows the plan is that of the first (largest) of
+ *                 the balanced chunks of at most 16 rows.
+ *   aligned16     1 if codes / weights and x start on 16-byte boundaries.
+ *   sm_count, smem_optin, smem_per_sm   the device (GB300: 152, 232448, 233472).
+ *   ctas_by_regs  HOST int [3] or NULL: the CTAs per SM the registers of the kernel
+ *                 variants allow -- 8 warps with one 8-row activation tile, 8 warps
+ *                 with two, 16 warps. NULL takes the launch bounds' minimum {3, 2, 1}
+ *                 (the compiler keeps the registers within them).
+ *   out           HOST int64 [11]: route (a qmv_route_name index), chunks, rows of
+ *                 the first chunk, warps, ring slots, staged (0/1), passes over K,
+ *                 tiles per round, CTAs per SM, grid, dynamic shared memory bytes.
+ *                 The generic route fills only route, chunks (8-row launches) and rows.
+ * Returns QMV_ERR_NULL for out or N NULL, QMV_ERR_SHAPE for values out of range or
+ * a shape no plan fits.
+ */
+QMV_API qmv_status qmv_debug_plan_wq(int fp4, int M, int64_t K, int count, const int64_t *N, int aligned16,
+                                     int sm_count, int smem_optin, int smem_per_sm, const int *ctas_by_regs,
+                                     int64_t *out);
+
+/*
  * Kernel-choice census: a counter per kernel route, bumped on every launch, so a
  * caller can check which kernel served each region and that no fallback ran
  * (the census of "v100-skinny README", "Native mixed-precision checkpoint path").
@@ -308,9 +338,9 @@ QMV_API qmv_status qmv_error_flags(uint32_t *flags, int clear);
  * Self-check of the bounded device-side wait that every streaming kernel uses on
  * its mbarriers: one thread waits on an mbarrier that nothing completes, so the
  * wait must give up after its bound, set the timeout bit (1) of the error word and
- * return, leaving the context usable. The bound is 2000 suspending try-waits with
- * a 1 ms hint each: at most about 2 s; on a GB300 each returns after about 3.8 us,
- * so the wait gives up after about 7.6 ms of waiting.
+ * return, leaving the context usable. The bound: 0.5 s of %globaltimer time once at
+ * least 1024 polls have been made (a context switched off the GPU makes no polls),
+ * and at most 2^21 polls in any case.
  *   out  DEVICE int64 [2], 8-byte aligned, owned by the caller: out[0] = 1 if the
  *        wait completed (never expected), 0 if it gave up; out[1] = nanoseconds
  *        spent waiting (%globaltimer).
@@ -318,6 +348,26 @@ QMV_API qmv_status qmv_error_flags(uint32_t *flags, int clear);
  * QMV_ERR_CUDA if the launch fails.
  */
 QMV_API qmv_status qmv_debug_wait_bound(int64_t *out, qmv_stream_t stream);
+
+/*
+ * Self-check of how a multi-warp kernel gives up (the tensor-core kernels: their
+ * warps meet at a CTA-wide barrier after every round). One CTA of 8 warps; each warp
+ * fills a 2-slot ring with real bulk copies, except warp `stuck_warp`, which arms its
+ * mbarriers and issues nothing, so its bounded wait runs out while the others reach
+ * the round's barrier. The stuck warp flags the timeout bit (1) of the error word and
+ * the CTA's abort word and goes on to the barrier; after it every warp sees the
+ * abort, waits (bounded) for its own copies in flight and returns: no thread is left
+ * at a barrier, no copy lands in the memory of an exited CTA. Takes about two wait
+ * bounds (the give-up, then the stuck warp's drain).
+ *   out         DEVICE int64 [8][4], 8-byte aligned: per warp, 1 if its wait gave up;
+ *               1 if it passed the barrier and saw the abort; the copies still in
+ *               flight when it left the round; nanoseconds from its first wait to
+ *               the barrier.
+ *   stuck_warp  0..7.
+ * Asynchronous on `stream`. Returns QMV_ERR_NULL / QMV_ERR_ALIGN for a bad `out`,
+ * QMV_ERR_SHAPE for stuck_warp out of range, QMV_ERR_CUDA if the launch fails.
+ */
+QMV_API qmv_status qmv_debug_cta_abort(int64_t *out, int stuck_warp, qmv_stream_t stream);
 
 #ifdef __cplusplus
 }

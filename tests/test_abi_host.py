@@ -246,6 +246,13 @@ def test_wait_bound_validation(lib):
     assert lib.qmv_debug_wait_bound(P + 4, None) == ALIGN
 
 
+def test_cta_abort_validation(lib):
+    assert lib.qmv_debug_cta_abort(None, 3, None) == NULL
+    assert lib.qmv_debug_cta_abort(P + 4, 3, None) == ALIGN
+    assert lib.qmv_debug_cta_abort(P, -1, None) == SHAPE
+    assert lib.qmv_debug_cta_abort(P, 8, None) == SHAPE
+
+
 def test_binding_raises_loudly_when_library_missing(monkeypatch, tmp_path):
     from gemm_qmv_quantize_gb300 import _binding
     monkeypatch.setattr(_binding, "_LIB_PATH", str(tmp_path / "missing.so"))

@@ -93,7 +93,10 @@ def test_reference_arm_under_torchrun_prints_once():
            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
            "--impl", "reference", "--gpus", "2", "--steps", "2", "--warmup", "1", "--ref-seconds", "1.5",
            "--workload", "q4_0_4096sq_m1"]
+    import time
+    t0 = time.perf_counter()
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    wall = time.perf_counter() - t0
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
     assert len(lines) == 1
@@ -106,7 +109,10 @@ def test_reference_arm_under_torchrun_prints_once():
     assert d["n_gpus"] == 2 and d["steps"] == 2 and d["warmup"] == 1 and d["higher_is_better"] is True
     assert d["vs_baseline"] is None and d["dtype"] == "f64" and d["config"]["workload"] == "q4_0_4096sq_m1"
     assert d["e2e"]["value"] == d["value"] and d["e2e"]["d2h_bytes_per_step"] == 0
-    assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["cores"] >= 1
+    assert d["cpu_baseline"]["value"] == d["value"] and d["cpu_baseline"]["cores"] == bench.host_threads()
+    # the step time is one the run actually took (the extrapolation to the whole stack has its own key)
+    assert d["steps"] * d["ms_per_step"] / 1e3 <= wall
+    assert d["extrapolated_stack_ms"] > 0 and "bytes" in d["step"]
 
 
 def test_step_spread_percentiles(monkeypatch):

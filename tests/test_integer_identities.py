@@ -3,9 +3,11 @@ emulation of the instructions (PTX ISA semantics, IEEE fp32) against the oracle:
 the exact block sums S = sum q4u * q8 and T = sum q8, the Q4_K scale decode, and
 the Q8_1 bytes.
 
-- "Machine Learning on NVIDIA CMP", section "The DP2A patch": one 4-way int8 dot
-  equals a 2-way dot over bytes 0..1 plus one over bytes 2..3 of B, once A's four
-  bytes are widened to int16 by two sign-replicating byte permutes.
+- "Machine Learning on NVIDIA CMP", section "The DP2A patch", rests on splitting a
+  4-way int8 dot into two 2-way dots: with A's four bytes sign-extended to int16
+  pairs (bytes 0, 1 in one word, bytes 2, 3 in the other), the 2-way dot of the
+  first word with B's bytes 0..1 plus that of the second with B's bytes 2..3 is the
+  4-way dot, for every A and B (plain algebra: the sum over four products regrouped).
 - The dp4a streaming kernel: unsigned low nibbles (mask 0x0f) and high nibbles kept
   in place (mask 0xf0, i.e. 16 q) against signed Q8_1 bytes, so S = lo + hi / 16
   exactly, and a block's dot is S - 8 T.
@@ -67,23 +69,24 @@ def dp2a(a, b, c, hi):
     return c + h0 * bv[o] + h1 * bv[o + 1]
 
 
-def test_dp4a_equals_two_permutes_and_two_dp2a():
+def _int16_pair(lo, hi):
+    """Two signed values packed as int16 halves of a 32-bit word (lo in bits 0..15)."""
+    return (np.asarray(lo, dtype=np.int64) & 0xFFFF) | ((np.asarray(hi, dtype=np.int64) & 0xFFFF) << 16)
+
+
+def test_dp4a_equals_two_dp2a_over_sign_extended_halves():
     rng = np.random.default_rng(11)
     edges = np.array([0, 0x7F7F7F7F, 0x80808080, 0xFFFFFFFF, 0x017F80FF, 0x80FF017F], dtype=np.uint64)
     a = np.concatenate([rng.integers(0, 1 << 32, 200_000, dtype=np.uint64), np.repeat(edges, len(edges))])
     b = np.concatenate([rng.integers(0, 1 << 32, 200_000, dtype=np.uint64), np.tile(edges, len(edges))])
     c = rng.integers(-(1 << 20), 1 << 20, len(a))
+    a0, a1, a2, a3 = _s8(a)   # A's bytes as signed values, sign-extended by the arithmetic itself
     ref = dp4a(a, b, c)
-    a_lo = prmt(a, 0, 0x9180)   # {(int16) a.byte0, (int16) a.byte1}
-    a_hi = prmt(a, 0, 0xB3A2)   # {(int16) a.byte2, (int16) a.byte3}
-    assert np.array_equal(dp2a(a_hi, b, dp2a(a_lo, b, c, hi=False), hi=True), ref)
-
-
-def test_prmt_widening_is_sign_extension():
-    for byte in range(256):
-        s = byte - 256 if byte >= 128 else byte
-        got = int(prmt(np.array([byte | (byte << 8)]), 0, 0x9180)[0])
-        assert got == ((s & 0xFFFF) | ((s & 0xFFFF) << 16))
+    assert np.array_equal(dp2a(_int16_pair(a2, a3), b, dp2a(_int16_pair(a0, a1), b, c, hi=False), hi=True), ref)
+    # the split is exact only with sign extension: zero-extended halves miss 256 per negative byte
+    zext = dp2a(_int16_pair(a2 & 0xFF, a3 & 0xFF), b, dp2a(_int16_pair(a0 & 0xFF, a1 & 0xFF), b, c, hi=False),
+                hi=True)
+    assert not np.array_equal(zext, ref)
 
 
 def _blocks(seed, N=37, M=3, K=1024):
