@@ -315,9 +315,11 @@ def source_digest(paths):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel's source
-    has not changed since the capture (else None)."""
+def profiled_traffic(kernel: str, workload: str, bytes_per_launch: float):
+    """DRAM bytes per launch of the bench's average launch, from a committed ncu
+    capture of a few launches of the same kernel source (their DRAM bytes over their
+    algorithmic bytes, times this launch's algorithmic bytes), or None when the source
+    has changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -325,8 +327,8 @@ def profiled_traffic(kernel: str, workload: str):
         e = d[kernel]
         if e.get("workload") != workload or e.get("source_sha") != source_digest(e["sources"]):
             return None
-        return float(e["dram_bytes_per_launch"])
-    except (OSError, KeyError, ValueError, TypeError):
+        return round(float(e["dram_bytes"]) / float(e["algorithmic_bytes"]) * bytes_per_launch)
+    except (OSError, KeyError, ValueError, TypeError, ZeroDivisionError):
         return None
 
 
@@ -695,7 +697,7 @@ def kernel_roofline(args, stack, stream, barrier, step_s=None):
         dur, achieved, timing = dur_iso, achieved_iso, how
     return {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak,
             "peak_kind": f"{peak_kind} (HBM copy bandwidth)", "unit": "GB/s", "frac": round(achieved / peak, 4),
-            "traffic": profiled_traffic(kname, stack.name), "bytes_per_launch": round(bytes_per_launch),
+            "traffic": profiled_traffic(kname, stack.name, bytes_per_launch), "bytes_per_launch": round(bytes_per_launch),
             "avg_launch_us": round(dur * 1e6, 3), "launches_timed": len(sel) * steps,
             "achieved_isolated": round(achieved_iso, 1), "frac_isolated": round(achieved_iso / peak, 4),
             "avg_launch_us_isolated": round(dur_iso * 1e6, 3), "timing": timing}

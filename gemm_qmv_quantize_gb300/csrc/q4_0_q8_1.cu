@@ -34,6 +34,20 @@ namespace {
 
 __device__ uint32_t g_q4_error;
 
+// Stage trace (profiling builds only, compiled with -DQMV_STAGE_TRACE): every warp of
+// the streaming kernel records %globaltimer at its start, after the programmatic-
+// dependency wait, after the activation prologue's barrier, when its first chunk has
+// landed and at its end, with its SM, into a per-launch record the host assigns
+// (qmv_stage_trace_set). gemm_qmv_quantize_gb300/stage_trace.py reads the records.
+#ifdef QMV_STAGE_TRACE
+constexpr int kTraceWarps = 16, kTraceFields = 8;   // per warp: 5 times, SM, chunks, valid
+#define QMV_TRACE_PARAM , unsigned long long *trace
+#define QMV_TRACE_STAMP(var) var = globaltimer_ns()
+#else
+#define QMV_TRACE_PARAM
+#define QMV_TRACE_STAMP(var)
+#endif
+
 constexpr int kThreads = 256;        // generic kernel
 constexpr int kWarps = kThreads / 32;
 constexpr int kStreamThreads = 512;      // streaming kernel, M <= kWideFromM - 1: up to 16 warps
@@ -480,8 +494,11 @@ __device__ __forceinline__ void stage_q8_1(const Q4Group &grp, int nb, uint8_t *
 template <int M, bool kDots, bool kFused, bool kQ4K, bool kActRegs = false, bool kPair = false>
 __global__ void __launch_bounds__(kActRegs ? (M == 1 ? kActRegsThreads : kStreamThreadsWide) : stream_threads(M))
     q4_0_stream_kernel(
-    const __grid_constant__ Q4Group grp, int32_t *__restrict__ dots, int64_t K, int S, int P)
+    const __grid_constant__ Q4Group grp, int32_t *__restrict__ dots, int64_t K, int S, int P QMV_TRACE_PARAM)
 {
+#ifdef QMV_STAGE_TRACE
+    uint64_t t_start = globaltimer_ns(), t_rel = 0, t_sync = 0, t_first = 0;
+#endif
     extern __shared__ __align__(128) uint8_t smem[];
     const int warps = blockDim.x >> 5;
     const Q4Layout L = q4_layout(M * grp.nx, K, warps, S);
@@ -524,6 +541,7 @@ __global__ void __launch_bounds__(kActRegs ? (M == 1 ? kActRegsThreads : kStream
     __syncwarp();
     grid_launch_dependents();
     grid_dependency_wait();
+    QMV_TRACE_STAMP(t_rel);
 
     // the rest of the ring is requested once the activation loads are in flight,
     // so that they do not queue behind a full ring of weight copies
@@ -536,6 +554,7 @@ __global__ void __launch_bounds__(kActRegs ? (M == 1 ? kActRegsThreads : kStream
     else
         stage_q8_1<M>(grp, nb, smem, L, blockDim.x, fill_ring);
     __syncthreads();   // the only CTA-wide barrier
+    QMV_TRACE_STAMP(t_sync);
 
     const uint8_t *act0 = smem + L.off_act + (grp.xslot[mi] * M) * L.act_m_stride;
     float *ym = grp.y[mi] + r0;
@@ -565,6 +584,9 @@ __global__ void __launch_bounds__(kActRegs ? (M == 1 ? kActRegsThreads : kStream
             }
             return;
         }
+#ifdef QMV_STAGE_TRACE
+        if (c == 0) t_first = globaltimer_ns();
+#endif
         const bool live = c * kChunkUnits + lane < TU;
         float v[M];
 #pragma unroll
@@ -662,6 +684,15 @@ __global__ void __launch_bounds__(kActRegs ? (M == 1 ? kActRegsThreads : kStream
             phase ^= 1u;
         }
     }
+#ifdef QMV_STAGE_TRACE
+    if (trace && lane == 0 && warp < kTraceWarps) {
+        unsigned long long *tw = trace + (static_cast<size_t>(blockIdx.x) * kTraceWarps + warp) * kTraceFields;
+        uint32_t sm;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sm));
+        tw[0] = t_start; tw[1] = t_rel; tw[2] = t_sync; tw[3] = t_first; tw[4] = globaltimer_ns();
+        tw[5] = sm; tw[6] = static_cast<unsigned long long>(nchunks); tw[7] = 1;
+    }
+#endif
 }
 
 // Any K % 32 == 0 and 2-byte aligned rows: one warp per weight row, lanes over blocks.
@@ -724,6 +755,19 @@ __global__ void __launch_bounds__(kThreads) q4_0_generic_kernel(const uint8_t *_
 
 // ---------------------------------------------------------------- host side
 
+#ifdef QMV_STAGE_TRACE
+unsigned long long *g_trace_buf = nullptr;
+int g_trace_records = 0, g_trace_next = 0, g_trace_ctas = 0;
+
+// The record of the next streaming launch (records are used in launch order, cyclically).
+unsigned long long *next_trace_record(int grid)
+{
+    if (!g_trace_buf || g_trace_records == 0 || grid > g_trace_ctas) return nullptr;
+    const int r = g_trace_next++ % g_trace_records;
+    return g_trace_buf + static_cast<size_t>(r) * g_trace_ctas * kTraceWarps * kTraceFields;
+}
+#endif
+
 template <int M, bool kDots, bool kFused, bool kQ4K>
 cudaError_t launch_m(const Q4Plan &p, const Q4Group &grp, int32_t *dots, int64_t K, cudaStream_t s)
 {
@@ -743,7 +787,11 @@ cudaError_t launch_m(const Q4Plan &p, const Q4Group &grp, int32_t *dots, int64_t
         if (e != cudaSuccess) return e;
         cfg.blockDim = dim3(static_cast<unsigned>(p.warps * 32));   // consumers + the producer
         cfg.dynamicSmemBytes = static_cast<size_t>(p.smem_bytes);
+#ifdef QMV_STAGE_TRACE
+        return cudaLaunchKernelEx(&cfg, kern, grp, dots, K, p.stages, p.prefetch, next_trace_record(p.grid));
+#else
         return cudaLaunchKernelEx(&cfg, kern, grp, dots, K, p.stages, p.prefetch);
+#endif
     }
     if (kQ4K || kFused || grp.count != 1) return cudaErrorInvalidValue;   // these need the streaming kernel
     cfg.blockDim = dim3(kThreads);
@@ -830,9 +878,19 @@ cudaError_t plan_q4_0(const DeviceInfo &dev, const Q4Group &grp, int M, int64_t 
     const int pair_env = env_int("QMV_Q4_PAIR", -1);
     const bool pair = !act_regs && !q4k && M >= 2 && M <= 4 && U == 16 &&
                       (pair_env < 0 ? M == 4 : pair_env != 0);
+    // Spare SMs: the grid leaves about one SM in twelve without a CTA. In a chain of
+    // calls with launch overlap the next call's CTAs take the SMs in the order they
+    // free up, and its last CTA lands on the SM that finished the previous call last;
+    // that CTA then starts after the others' early weight copies have landed, finishes
+    // last, and hands the lateness on to the next call (globaltimer traces of the
+    // Llama-2-7B stack: one CTA about 1 us behind the rest in every stage). With spare
+    // SMs the previous call's stragglers get no CTA of the next call. Llama-2-7B stack:
+    // 3935 GB/s with no spare SM, 4086 with 1, 4149 with 4, 4245 with 12, 4195 with 16,
+    // 3894 with 32.
     const int per_sm = std::max(1, std::min(4, env_int("QMV_Q4_CTAS_PER_SM", 1)));
+    const int spare = std::max(0, std::min(dev.sm_count - 1, env_int("QMV_Q4_SPARE_SMS", dev.sm_count / 12)));
     const int64_t ctas = std::max<int64_t>(1, std::min<int64_t>((N + warps - 1) / warps,
-                                                                 static_cast<int64_t>(dev.sm_count) * per_sm));
+                                                                 static_cast<int64_t>(dev.sm_count - spare) * per_sm));
     if ((N / (ctas * warps) + 1) * (K / 256) >= (int64_t(1) << 31)) return cudaSuccess;   // 32-bit unit counters
     plan->route = kRouteQ4_0Stream;
     plan->act_regs = act_regs;
@@ -885,6 +943,19 @@ cudaError_t launch_q4_0(const Q4Plan &plan, const Q4Group &grp_in, int32_t *dots
     if (fused) return launch_dispatch<false, true, false>(plan, grp, dots, M, K, s);
     return launch_dispatch<false, false, false>(plan, grp, dots, M, K, s);
 }
+
+#ifdef QMV_STAGE_TRACE
+// Profiling builds: records[r][cta < ctas][warp < 16][8] of the streaming kernel's launches, in
+// launch order from the next launch on (NULL stops tracing). Not part of the product library.
+extern "C" __attribute__((visibility("default"))) void qmv_stage_trace_set(unsigned long long *records, int count,
+                                                                          int ctas)
+{
+    g_trace_buf = records;
+    g_trace_records = records ? count : 0;
+    g_trace_ctas = ctas;
+    g_trace_next = 0;
+}
+#endif
 
 cudaError_t read_error_word_q4_0(uint32_t *out, bool clear)
 {

@@ -567,7 +567,8 @@ cudaError_t choose_wq_plan(bool fp4, const DeviceInfo &dev, int64_t ntiles, int 
         if (e != cudaSuccess) return e;
         occ = std::min(occ, 4);
         if (occ < 1) continue;
-        const int64_t g = std::min<int64_t>(ntiles, static_cast<int64_t>(dev.sm_count) * occ);
+        const int64_t g = std::min<int64_t>(
+            ntiles, std::max<int64_t>(1, static_cast<int64_t>(dev.sm_count) * occ - env_int("QMV_WQ_SPARE_CTAS", 0)));
         const double imb = static_cast<double>((ntiles + g - 1) / g * g) / static_cast<double>(ntiles);
         const double score =
             (imb <= 1.15 ? 1.0 : imb) + (occ * Wc < 16 ? 0.5 : 0.0) + (Pc - 1) - 0.05 * (occ * Wc / 8);
