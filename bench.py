@@ -153,9 +153,10 @@ for _m in (32, 96):
 WORKLOADS["mixed_27b_m32"] = dict(M=32, mats=lambda: dense_27b_stack(True), stages=lambda: dense_27b_stages(True),
                                   desc="27B-class stack, FP8 attention every 4th layer + NVFP4 lm_head, M=32 "
                                        "(chunks of 16 rows)")
-for _m in (1, 8, 16):
+for _m in (1, 8, 16, 24, 32, 48, 64, 96):
     WORKLOADS[f"nvfp4_17408x5120_m{_m}"] = dict(M=_m, mats=lambda: [("nvfp4", 17408, 5120)] * 8,
                                                desc=f"NVFP4 W4A16 17408x5120, M={_m}, 8 rotated copies")
+for _m in (1, 8, 16, 24, 48, 64):
     WORKLOADS[f"fp8_7168x5120_m{_m}"] = dict(M=_m, mats=lambda: [("fp8", 7168, 5120)] * 12,
                                             desc=f"FP8 W8A16 7168x5120, M={_m}, 12 rotated copies")
 DEFAULT_WORKLOAD = "llama2_7b_q4_0_m1"

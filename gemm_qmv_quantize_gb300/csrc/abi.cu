@@ -19,6 +19,7 @@ constexpr const char *kRouteNames[kRouteCount] = {
     "nvfp4_generic",
     "fp8_mma_m16n8k16", "fp8_generic", "zero_fill", "q4_0_mma_m16n8k32", "q4_0_mma_fused_quantize",
     "q4_k_stream_dp4a", "q4_k_stream_fused_quantize", "q4_k_mma_m16n8k32", "q4_k_mma_fused_quantize",
+    "nvfp4_tcgen05", "fp8_tcgen05",
 };
 
 constexpr int kMaxDevices = 64;
@@ -523,8 +524,9 @@ qmv_status qmv_error_flags(uint32_t *flags, int clear)
 {
     if (!flags) return QMV_ERR_NULL;
     if (cudaDeviceSynchronize() != cudaSuccess) return QMV_ERR_CUDA;
-    uint32_t w = 0, w2 = 0, w3 = 0, w4 = 0;
+    uint32_t w = 0, w2 = 0, w3 = 0, w4 = 0, w5 = 0;
     if (read_error_word_q4_0(&w, clear != 0) != cudaSuccess) return QMV_ERR_CUDA;
+    if (read_error_word_umma(&w5, clear != 0) != cudaSuccess) return QMV_ERR_CUDA;
     if (read_error_word_wq(&w2, clear != 0) != cudaSuccess) return QMV_ERR_CUDA;
     if (read_error_word_q4_0_mma(&w3, clear != 0) != cudaSuccess) return QMV_ERR_CUDA;
     if (cudaMemcpyFromSymbol(&w4, g_abi_error, sizeof(uint32_t)) != cudaSuccess) return QMV_ERR_CUDA;
@@ -532,7 +534,7 @@ qmv_status qmv_error_flags(uint32_t *flags, int clear)
         const uint32_t zero = 0;
         if (cudaMemcpyToSymbol(g_abi_error, &zero, sizeof(uint32_t)) != cudaSuccess) return QMV_ERR_CUDA;
     }
-    *flags = w | w2 | w3 | w4;
+    *flags = w | w2 | w3 | w4 | w5;
     return QMV_OK;
 }
 

@@ -128,6 +128,13 @@ __device__ __forceinline__ void drain_ring(uint64_t *bars, int S, int slot, uint
     }
 }
 
+__device__ __forceinline__ uint64_t policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first()
 {
     uint64_t p;

@@ -25,6 +25,8 @@ enum Route : int {
     kRouteQ4KStreamFused, // ... with the Q8_1 quantize in the prologue
     kRouteQ4KMma,         // Q4_K: the Q4_0 tensor-core kernel's machinery (m16n8k32 int8), larger M
     kRouteQ4KMmaFused,    // ... with the Q8_1 quantize in the prologue
+    kRouteNvfp4Umma,      // NVFP4: tcgen05.mma (TMEM accumulators), M <= 96 in one weight pass
+    kRouteFp8Umma,        // FP8: the same kernel with a byte-wide decode
     kRouteCount
 };
 
@@ -130,5 +132,28 @@ cudaError_t read_error_word_q4_0_mma(uint32_t *out, bool clear);
 // tensor map with a box of box_cols bytes x box_rows rows; zero fill outside.
 cudaError_t encode_map_2d(CUtensorMap *map, const void *base, int64_t rows, int64_t cols, uint32_t box_cols,
                           uint32_t box_rows, CUtensorMapSwizzle swizzle);
+// Tensor map of `rank` dimensions (dims[0] innermost), strides in bytes of dims 1..rank-1,
+// zero fill outside.
+cudaError_t encode_map_nd(CUtensorMap *map, CUtensorMapDataType dtype, int rank, const void *base, const uint64_t *dims,
+                          const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle);
+
+// NVFP4 / FP8 on the 5th-generation tensor cores (tcgen05, TMEM accumulators): a group
+// with M <= 96 rows in one weight pass. K a multiple of 256 (NVFP4) / 128 (FP8), codes,
+// NVFP4 scales and x 16-byte aligned.
+struct UmmaPlan {
+    int n_pad = 0;        // activation rows padded to a multiple of 16 (the MMA's N)
+    int T = 0, S = 0, Q = 0, R = 0;   // issuing threads, weight stages, A buffers, activation slices
+    int grid = 0;
+    uint32_t smem = 0, tmem_cols = 0;
+};
+// The tcgen05 kernel's plan for `tiles` 128-row tiles (no CUDA call).
+cudaError_t plan_umma(bool fp4, const DeviceInfo &dev, int64_t tiles, int M, int64_t K, UmmaPlan *out);
+// First M the tcgen05 kernel takes by default (QMV_WQ_UMMA_MIN_M overrides; 0 = never).
+int umma_min_m(bool fp4);
+cudaError_t launch_nvfp4_umma(const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M, int64_t K,
+                              cudaStream_t s);
+cudaError_t launch_fp8_umma(const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M, int64_t K,
+                            cudaStream_t s);
+cudaError_t read_error_word_umma(uint32_t *out, bool clear);
 
 }  // namespace qmv

@@ -84,6 +84,25 @@ cudaError_t encode_map_2d(CUtensorMap *map, const void *base, int64_t rows, int6
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t encode_map_nd(CUtensorMap *map, CUtensorMapDataType dtype, int rank, const void *base, const uint64_t *dims,
+                          const uint64_t *strides_bytes, const uint32_t *box, CUtensorMapSwizzle swizzle)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc || rank < 1 || rank > 5) return cudaErrorNotSupported;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) st[i] = strides_bytes[i];
+    }
+    const CUresult r = enc(map, dtype, static_cast<cuuint32_t>(rank), const_cast<void *>(base), d, st, b, es,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 
 namespace {
 
@@ -707,10 +726,24 @@ namespace {
 // the tensor-core kernel (one or two 8-row tiles per weight pass). Chunk c + 1
 // reads the same weights right after chunk c, from L2 when the group's weights fit
 // there. The generic kernel takes any M in 8-row launches already.
+// The tcgen05 kernel takes a call from umma_min_m(fp4) activation rows on, when its
+// operands suit TMA: K a multiple of the step, codes, scales and x 16-byte aligned (the
+// tensor-core route already requires all but the scales).
+bool umma_applies(bool fp4, const WqGroup &grp, int M)
+{
+    const int min_m = umma_min_m(fp4);
+    if (min_m <= 0 || M < min_m || M > 96) return false;
+    for (int i = 0; i < grp.count; ++i)
+        if (fp4 && grp.N[i] > 0 && !aligned16(grp.scales[i])) return false;
+    return true;
+}
+
 template <bool kFp4>
 cudaError_t launch_wq_chunked(Route r, const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M,
                               int64_t K, cudaStream_t s)
 {
+    if ((r == kRouteNvfp4Mma || r == kRouteFp8Mma) && umma_applies(kFp4, grp, M))
+        return kFp4 ? launch_nvfp4_umma(dev, grp, x, M, K, s) : launch_fp8_umma(dev, grp, x, M, K, s);
     if (M <= 16 || (r != kRouteNvfp4Mma && r != kRouteFp8Mma)) return launch_wq<kFp4>(r, dev, grp, x, M, K, s);
     const int nch = (M + 15) / 16;
     int m0 = 0;
@@ -727,6 +760,12 @@ cudaError_t launch_wq_chunked(Route r, const DeviceInfo &dev, const WqGroup &grp
 
 }  // namespace
 
+// Where the chunked mma.sync path would take several passes over the weights, the
+// tcgen05 kernel's one pass wins (measured, GB/s, mma.sync / tcgen05: NVFP4 17408 x 5120
+// at M = 16: 1949 / 1364, 24: 1058 / 1373, 48: 695 / 1414, 96: 373 / 1499; FP8 7168 x
+// 5120 at M = 32: 1332 / 1028, 48: 903 / 1018, 96: 477 / 1039).
+int umma_min_m(bool fp4) { return env_int("QMV_WQ_UMMA_MIN_M", fp4 ? 17 : 33); }
+
 cudaError_t debug_plan_wq(bool fp4, const DeviceInfo &dev, int M, int64_t K, int count, const int64_t *N,
                           bool aligned16, const int ctas_by_regs[3], int64_t out[11])
 {
@@ -741,6 +780,18 @@ cudaError_t debug_plan_wq(bool fp4, const DeviceInfo &dev, int M, int64_t K, int
     }
     int64_t ntiles = 0;
     for (int i = 0; i < count; ++i) ntiles += (N[i] + kRowsPerCta - 1) / kRowsPerCta;
+    const int min_m = umma_min_m(fp4);
+    if (min_m > 0 && M >= min_m) {   // the tcgen05 kernel: 128-row tiles, one pass for all M rows
+        int64_t tiles = 0;
+        for (int i = 0; i < count; ++i) tiles += (N[i] + 127) / 128;
+        UmmaPlan pl;
+        const cudaError_t e = plan_umma(fp4, dev, std::max<int64_t>(tiles, 1), M, K, &pl);
+        if (e != cudaSuccess) return e;
+        const int64_t v[11] = {fp4 ? kRouteNvfp4Umma : kRouteFp8Umma, 1, M, pl.T, pl.S, 1, 1, 1, 1,
+                               tiles ? pl.grid : 0, static_cast<int64_t>(pl.smem)};
+        for (int i = 0; i < 11; ++i) out[i] = v[i];
+        return cudaSuccess;
+    }
     const int nch = M > 16 ? (M + 15) / 16 : 1;
     const int mc = (M + nch - 1) / nch;   // the first (largest) chunk
     out[0] = fp4 ? kRouteNvfp4Mma : kRouteFp8Mma;

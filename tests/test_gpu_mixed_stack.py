@@ -12,7 +12,8 @@ programmatic dependent launch on, as the benchmark runs it). Every matrix's samp
 rows (first, last, random) are compared with the oracle within
 |y - y_ref| <= 1e-3 * sum|w x| + 1e-6, and the census must show exactly one launch
 (per chunk of 16 rows) of the FP8 kernel per FP8 region and of the NVFP4 kernel per
-NVFP4 stage, and no generic kernel.
+NVFP4 stage, and no generic kernel (from 17 rows the NVFP4 regions take the tcgen05
+kernel, from 33 the FP8 ones: one launch per stage there).
 """
 import pytest
 import torch
@@ -34,7 +35,7 @@ def q():
     q.set_launch_overlap(before)
 
 
-@pytest.mark.parametrize("M", [1, 8, 16, 32])
+@pytest.mark.parametrize("M", [1, 8, 16, 32, 48])
 def test_mixed_stack_regions_dispatch_and_match_the_oracle(q, M):
     spec = dict(M=M, mats=bench.dense_27b_stack(True, LAYERS), stages=bench.dense_27b_stages(True, LAYERS))
     stack = bench.Stack(f"mixed_27b_{LAYERS}layers_m{M}", torch.device("cuda"), seed=77 + M, spec=spec)
@@ -48,7 +49,9 @@ def test_mixed_stack_regions_dispatch_and_match_the_oracle(q, M):
     fp8_stages = sum(1 for st in stack.stages if stack.mats[st[0]][0] == "fp8")
     nvfp4_stages = len(stack.stages) - fp8_stages
     assert (fp8_stages, nvfp4_stages) == (2, 4 * LAYERS + 1 - 2)
-    assert counts == {"fp8_mma_m16n8k16": fp8_stages * chunks, "nvfp4_mma_m16n8k16": nvfp4_stages * chunks}, counts
+    want = {"nvfp4_tcgen05": nvfp4_stages} if M >= 17 else {"nvfp4_mma_m16n8k16": nvfp4_stages}
+    want.update({"fp8_tcgen05": fp8_stages} if M >= 33 else {"fp8_mma_m16n8k16": fp8_stages * chunks})
+    assert counts == want, counts
     assert not any(k.endswith("generic") for k in counts)
     par = bench.sampled_parity(stack, rows=8)
     print(f"M={M}: {par}")

@@ -291,8 +291,14 @@ def test_sixteen_warps_passes_group(q, monkeypatch, passes):
 
 # ------------------------------------------------ 17..96 rows: balanced chunks of <= 16 rows
 
+@pytest.fixture
+def chunked(monkeypatch):
+    """The chunked mma.sync path above 16 rows (the tcgen05 kernel switched off)."""
+    monkeypatch.setenv("QMV_WQ_UMMA_MIN_M", "0")
+
+
 @pytest.mark.parametrize("M", [17, 24, 33, 64, 96])
-def test_chunked_rows(q, M):
+def test_chunked_rows(q, M, chunked):
     """ceil(M / 16) launches of <= 16 rows each; every output within the bound."""
     N = 16 * 21 + 11
     q.route_reset()
@@ -304,13 +310,13 @@ def test_chunked_rows(q, M):
 
 @pytest.mark.parametrize("M", [40, 96])
 @pytest.mark.parametrize("N,K", [(7168, 5120), (5120, 5120)])
-def test_fp8_chunked_27b_attention_sampled(q, M, N, K):
+def test_fp8_chunked_27b_attention_sampled(q, M, N, K, chunked):
     rows = _synth().sample_rows(N, 24, seed=N + K + M).numpy()
     _fp8(q, M, N, K, seed=N * 11 + K + M, rows=rows)
 
 
 @pytest.mark.parametrize("M", [17, 96])
-def test_chunked_group_and_generic(q, M):
+def test_chunked_group_and_generic(q, M, chunked):
     """A gate/up-like group chunked by rows, and the generic kernel (K % 256 != 0) at M > 16."""
     synth = _synth()
     K = 5120
@@ -325,6 +331,24 @@ def test_chunked_group_and_generic(q, M):
     _nvfp4(q, M, 33, 1040, seed=1900 + M)
     _fp8(q, M, 21, 1000, seed=1950 + M)
     assert q.route_counts()["nvfp4_generic"] == (M + 7) // 8 and q.route_counts()["fp8_generic"] == (M + 7) // 8
+
+
+@pytest.mark.parametrize("M", [16, 17, 32, 33, 96])
+def test_default_dispatch_above_16_rows(q, M):
+    """Default routes: NVFP4 on the tcgen05 kernel from 17 rows, FP8 from 33 (one launch,
+    one weight pass); below that one mma.sync pass up to 16 rows, chunks above."""
+    N = 128 * 2 + 45
+    q.route_reset()
+    _nvfp4(q, M, N, 5120, seed=3100 + M)
+    _fp8(q, M, N, 5120, seed=3200 + M)
+    c = {k: v for k, v in q.route_counts().items() if v}
+    want = {}
+    want["nvfp4_tcgen05" if M >= 17 else "nvfp4_mma_m16n8k16"] = 1
+    if M >= 33:
+        want["fp8_tcgen05"] = 1
+    else:
+        want["fp8_mma_m16n8k16"] = (M + 15) // 16
+    assert c == want, c
 
 
 # ------------------------------------------------ largest K and M

@@ -6,9 +6,10 @@ of the device, so no GPU is needed.
 - Choices the design notes measured and kept: three 8-warp CTAs per SM at M = 1
   (the 5120 x 17408 down projection and the lm_head), 16 warps sharing one staged
   copy of the activations at M = 8 with K = 5120, two 8-row activation tiles in one
-  weight pass at M = 9..16, balanced chunks of <= 16 rows above 16 ("v100-skinny
-  README", "Native mixed-precision checkpoint path": the qpn8 / qpn8-mt2 /
-  qpn8-chunked routes), the generic kernel for unaligned data or K off the step.
+  weight pass at M = 9..16, then one pass on the tcgen05 kernel (NVFP4 from 17 rows,
+  FP8 from 33) or balanced chunks of <= 16 rows ("v100-skinny README", "Native
+  mixed-precision checkpoint path": the qpn8 / qpn8-mt2 / qpn8-chunked routes), the
+  generic kernel for unaligned data or K off the step.
 - Invariants over a sweep of shapes, M and register limits: shared memory within the
   device's opt-in limit and the SM, the grid = min(tiles, SMs x CTAs per SM), every
   warp the same number of steps per round, passes dividing the steps, the staged
@@ -21,6 +22,8 @@ import pytest
 from gemm_qmv_quantize_gb300._binding import GB300_DEVICE, QmvError, qmv_debug_plan_wq as plan
 
 MMA = {True: "nvfp4_mma_m16n8k16", False: "fp8_mma_m16n8k16"}
+UMMA = {True: "nvfp4_tcgen05", False: "fp8_tcgen05"}
+UMMA_MIN_M = {True: 17, False: 33}
 GENERIC = {True: "nvfp4_generic", False: "fp8_generic"}
 SHAPES_27B = [(7168, 5120), (5120, 5120), (17408, 5120), (5120, 17408), (151936, 5120)]
 
@@ -50,11 +53,31 @@ def test_m9_to_16_one_weight_pass(M, fp4):
 
 
 @pytest.mark.parametrize("M", [17, 24, 32, 33, 48, 64, 95, 96])
-def test_chunked_band(M):
+def test_chunked_band(M, monkeypatch):
+    """Without the tcgen05 kernel (QMV_WQ_UMMA_MIN_M=0) rows above 16 go in balanced chunks."""
+    monkeypatch.setenv("QMV_WQ_UMMA_MIN_M", "0")
     p = plan(M, 5120, 7168, fp4=False)
     chunks = math.ceil(M / 16)
     assert (p["route"], p["chunks"], p["chunk_rows"]) == (MMA[False], chunks, math.ceil(M / chunks))
     assert p["chunk_rows"] <= 16
+
+
+@pytest.mark.parametrize("fp4", [True, False])
+@pytest.mark.parametrize("M", [16, 17, 24, 32, 33, 48, 64, 80, 96])
+def test_tcgen05_band(fp4, M):
+    """From 17 rows (NVFP4) / 33 (FP8) one pass on the tcgen05 kernel: 128-row tiles, T
+    issuing threads with an accumulator of 16 ceil(M / 16) columns each in 512 columns of
+    tensor memory, at least 3 weight stages, shared memory within the device's limit."""
+    N, K = 17408, 5120
+    p = plan(M, K, N, fp4=fp4)
+    if M < UMMA_MIN_M[fp4]:
+        assert p["route"] == MMA[fp4]
+        return
+    n_pad = 16 * math.ceil(M / 16)
+    assert (p["route"], p["chunks"], p["chunk_rows"]) == (UMMA[fp4], 1, M)
+    assert 1 <= p["warps"] <= min(8, 512 // n_pad) and p["warps"] * n_pad <= 512
+    assert 3 <= p["slots"] <= 8 and p["smem_bytes"] <= GB300_DEVICE["smem_optin"]
+    assert p["grid"] == min(math.ceil(N / 128), GB300_DEVICE["sm_count"])
 
 
 def test_generic_routes():
@@ -81,6 +104,8 @@ def test_rejects_bad_arguments():
     with pytest.raises(QmvError):
         plan(1, 5120 + 16, [7168, 7168])   # a group needs the tensor-core kernel's K step
     with pytest.raises(QmvError):
+        plan(40, 5120 + 16, [7168, 7168])
+    with pytest.raises(QmvError):
         plan(1, 5120, 7168, ctas_by_regs=(0, 1, 1))
 
 
@@ -94,6 +119,9 @@ def test_invariants_over_a_sweep(fp4, regs):
         for M in (1, 2, 3, 5, 8, 9, 12, 16, 17, 40, 96):
             p = plan(M, K, N, fp4=fp4, ctas_by_regs=regs)
             rows = p["chunk_rows"]
+            if M >= UMMA_MIN_M[fp4]:
+                assert p["route"] == UMMA[fp4] and rows == M
+                continue
             assert p["route"] == MMA[fp4]
             assert 1 <= rows <= 16 and p["chunks"] == (math.ceil(M / 16) if M > 16 else 1)
             assert p["warps"] in (8, 16) and 2 <= p["slots"] <= 4
