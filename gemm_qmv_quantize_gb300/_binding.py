@@ -322,7 +322,7 @@ def qmv_debug_plan_q4(M: int, N: int, K: int, q4k: bool = False, n_inputs: int =
 
 
 WQ_PLAN_FIELDS = ("route", "chunks", "chunk_rows", "warps", "slots", "staged", "passes", "tiles_per_round",
-                  "ctas_per_sm", "grid", "smem_bytes")
+                  "ctas_per_sm", "grid", "smem_bytes", "a_bufs", "b_bufs")
 
 
 def qmv_debug_plan_wq(M: int, K: int, N, fp4: bool = True, aligned16: bool = True, ctas_by_regs=None,
@@ -335,7 +335,7 @@ def qmv_debug_plan_wq(M: int, K: int, N, fp4: bool = True, aligned16: bool = Tru
     Ns = [int(N)] if isinstance(N, int) else [int(n) for n in N]
     n_arr = (ctypes.c_int64 * len(Ns))(*Ns)
     regs = None if ctas_by_regs is None else (ctypes.c_int * 3)(*[int(v) for v in ctas_by_regs])
-    out = (ctypes.c_int64 * 11)()
+    out = (ctypes.c_int64 * len(WQ_PLAN_FIELDS))()
     _check("qmv_debug_plan_wq", lib().qmv_debug_plan_wq(int(bool(fp4)), M, K, len(Ns), n_arr, int(bool(aligned16)),
                                                         sm_count, smem_optin, smem_per_sm, regs, out))
     plan = dict(zip(WQ_PLAN_FIELDS, (int(v) for v in out)))

@@ -121,7 +121,7 @@ cudaError_t launch_fp8(Route r, const DeviceInfo &dev, const WqGroup &grp, const
 // row tiles) and 16-warp kernels allow. out: route, chunks, rows of the first chunk,
 // warps, slots, staged, passes, tiles per round, CTAs per SM, grid, shared memory.
 cudaError_t debug_plan_wq(bool fp4, const DeviceInfo &dev, int M, int64_t K, int count, const int64_t *N,
-                          bool aligned16, const int ctas_by_regs[3], int64_t out[11]);
+                          bool aligned16, const int ctas_by_regs[3], int64_t out[13]);
 
 // Device error words of each translation unit (read synchronously; optionally cleared).
 cudaError_t read_error_word_q4_0(uint32_t *out, bool clear);

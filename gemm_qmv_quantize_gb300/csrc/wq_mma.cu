@@ -767,9 +767,9 @@ cudaError_t launch_wq_chunked(Route r, const DeviceInfo &dev, const WqGroup &grp
 int umma_min_m(bool fp4) { return env_int("QMV_WQ_UMMA_MIN_M", fp4 ? 17 : 33); }
 
 cudaError_t debug_plan_wq(bool fp4, const DeviceInfo &dev, int M, int64_t K, int count, const int64_t *N,
-                          bool aligned16, const int ctas_by_regs[3], int64_t out[11])
+                          bool aligned16, const int ctas_by_regs[3], int64_t out[13])
 {
-    for (int i = 0; i < 11; ++i) out[i] = 0;
+    for (int i = 0; i < 13; ++i) out[i] = 0;
     const bool mma = aligned16 && K % (fp4 ? 256 : 128) == 0;
     if (!mma) {   // the generic kernel, 8 activation rows per launch
         if (count != 1) return cudaErrorInvalidValue;
@@ -787,9 +787,9 @@ cudaError_t debug_plan_wq(bool fp4, const DeviceInfo &dev, int M, int64_t K, int
         UmmaPlan pl;
         const cudaError_t e = plan_umma(fp4, dev, std::max<int64_t>(tiles, 1), M, K, &pl);
         if (e != cudaSuccess) return e;
-        const int64_t v[11] = {fp4 ? kRouteNvfp4Umma : kRouteFp8Umma, 1, M, pl.T, pl.S, 1, 1, 1, 1,
-                               tiles ? pl.grid : 0, static_cast<int64_t>(pl.smem)};
-        for (int i = 0; i < 11; ++i) out[i] = v[i];
+        const int64_t v[13] = {fp4 ? kRouteNvfp4Umma : kRouteFp8Umma, 1, M, pl.T, pl.S, 1, 1, 1, 1,
+                               tiles ? pl.grid : 0, static_cast<int64_t>(pl.smem), pl.Q, pl.R};
+        for (int i = 0; i < 13; ++i) out[i] = v[i];
         return cudaSuccess;
     }
     const int nch = M > 16 ? (M + 15) / 16 : 1;

@@ -11,19 +11,23 @@
 //    128 x N) accumulates over all of K in tensor memory. The whole activation
 //    width rides one weight pass: the README's M = 9..16 and 17..96 bands need no
 //    second pass over the weights and no chunking.
+//  * The decoded A operand lives in tensor memory too: a decode thread owns one
+//    weight row, which is one TMEM lane, and writes its fp16 pairs there with
+//    tcgen05.st; the MMA reads A from TMEM and only B from shared memory. Shared
+//    memory then holds the weight stages and activation slices alone, so more weight
+//    bytes are in flight (a weight stage took about 5 us from copy issue to arrival
+//    under full load here: the stream rate of a CTA is its bytes in flight / 5 us).
 //  * Exact decode, as in the mma.sync kernel: an E2M1 code times its E4M3 group
 //    scale is exact in fp16 (at most 6 significant bits, magnitude 2^-10 .. 2688),
 //    so the scale is folded into the fp16 weight; E4M3 to fp16 is exact; the
 //    per-tensor scale (NVFP4) or the row scale (FP8) multiplies the fp32 result.
 //  * Roles (warp specialisation): warp 0 streams, per K step, the codes (a 128-row
-//    box with the 128-byte swizzle), the group scales and the activation slice (a
-//    3-D box that lands in the tensor cores' K-major core-matrix layout, rows past M
-//    zero-filled) with TMA into a ring of stages; warps 2..5 decode one weight row
-//    per thread into fp16 core matrices of a 64-k A buffer (double-buffered); warp 1
-//    allocates tensor memory and one of its threads issues the MMAs (4 per 64 k);
-//    the decode warps read the accumulators back (tcgen05.ld) and store y. The
-//    accumulator is double-buffered across tiles, so a tile's read-back overlaps the
-//    next tile's MMAs.
+//    box with the 128-byte swizzle) and the group scales with TMA into a ring of
+//    stages; warp 2 streams 64-k activation slices (a box with the 128-byte swizzle:
+//    the K-major B operand, rows past M zero-filled); warp 1 allocates tensor memory;
+//    warps 3..10 decode (two threads per weight row, each half of a 64-k A buffer in
+//    TMEM) and at the end of a tile read the accumulators back (tcgen05.ld) and store
+//    y; warps 11.. each have one thread that issues MMAs (4 per 64 k).
 //  * Every mbarrier wait is bounded; a thread whose wait gives up flags the error
 //    word and the CTA's abort word and leaves its loop; all threads meet at the final
 //    barrier, the producer lets its copies land, the MMA thread waits for its
@@ -45,25 +49,29 @@ constexpr int kTileRows = 128;         // MMA M: weight rows per tile = TMEM lan
 constexpr int kQuarterK = 64;          // k per A buffer (8 core matrices of 8 k)
 constexpr int kCodesBox = kTileRows * 128;   // one step's codes: 128 rows x 128 bytes
 constexpr int kScalesBox = kTileRows * 16;   // NVFP4: 128 rows x 16 E4M3 scales
-constexpr int kABytes = kTileRows * kQuarterK * 2;   // 16 KB of fp16 per A buffer
-constexpr int kDecodeWarps = 8;        // two threads per weight row, each half of a 64-k buffer
-constexpr int kFirstDecodeWarp = 3;    // warp 0 weight producer, 1 tensor memory, 2 activation producer, 3..10 decode
+constexpr int kACols = kQuarterK / 2;  // TMEM columns of one 64-k A buffer (fp16 pairs)
+constexpr int kTmemCols = 512;         // the whole of tensor memory: accumulators and A buffers
+constexpr int kWeightProducers = 3;    // warps 0, 1, 2: one thread each streams every third K step
+constexpr int kDecodeWarps = 8;        // two groups of four (one warp per TMEM lane quarter)
+constexpr int kDecodeGroups = 2;       // the groups take alternate 64-k quarters
+constexpr int kFirstDecodeWarp = 3;    // warps 0..2 weight producers (warp 1 also allocates TMEM), 3..10 decode
 constexpr int kMaxIssuers = 8;         // warps 11 .. 11 + T - 1: one MMA-issuing thread each
 constexpr int kFirstIssuerWarp = kFirstDecodeWarp + kDecodeWarps;
 constexpr int kThreadsUmma = 32 * (kFirstIssuerWarp + kMaxIssuers);
-constexpr int kMaxStages = 8;          // weight stages (one K step of codes and scales each)
-constexpr int kMaxABufs = 8;           // 64-k A buffers and 64-k activation slices
+constexpr int kMaxStages = 12;         // weight stages (one K step of codes and scales each), a multiple of 3
+constexpr int kMaxSlicesPerIssuer = 12;
+constexpr int kMaxABufs = 12;          // 64-k A buffers in TMEM
 
 __host__ __device__ constexpr int step_k(bool fp4) { return fp4 ? 256 : 128; }   // 128 code bytes per row
 
 struct UmmaLayout {
-    uint32_t off_codes, off_scales, off_b, off_a, off_bar, off_misc, total;
+    uint32_t off_codes, off_scales, off_b, off_bar, off_misc, total;
     uint32_t b_bytes;   // one 64-k activation slice: 64 x N fp16
 };
 
 // Dynamic shared memory (base aligned to 1024 bytes): S weight stages of codes
-// (1024-aligned for the 128-byte swizzle) and scales, R 64-k activation slices, Q 64-k
-// A buffers, the mbarriers, the tensor-memory address and the abort word.
+// (1024-aligned for the 128-byte swizzle) and scales, R 64-k activation slices, the
+// mbarriers (Q of each A-buffer kind), the tensor-memory address and the abort word.
 __host__ __device__ inline UmmaLayout umma_layout(bool fp4, int S, int R, int Q, int n_pad)
 {
     UmmaLayout L;
@@ -71,12 +79,18 @@ __host__ __device__ inline UmmaLayout umma_layout(bool fp4, int S, int R, int Q,
     L.off_codes = 0;
     L.off_scales = L.off_codes + static_cast<uint32_t>(S * kCodesBox);
     L.off_b = (L.off_scales + (fp4 ? static_cast<uint32_t>(S * kScalesBox) : 0u) + 1023u) & ~1023u;
-    L.off_a = (L.off_b + static_cast<uint32_t>(R) * L.b_bytes + 1023u) & ~1023u;
-    L.off_bar = L.off_a + static_cast<uint32_t>(Q) * kABytes;
+    L.off_bar = L.off_b + static_cast<uint32_t>(R) * L.b_bytes;
     // w_full, w_free: S each; b_full, b_free: R each; a_full, a_free: Q each; acc_full, acc_free, done
     L.off_misc = L.off_bar + static_cast<uint32_t>(2 * S + 2 * R + 2 * Q + 3) * 8u;
     L.total = L.off_misc + 16u;
     return L;
+}
+
+// First TMEM column of the A buffers: after the T accumulators of n_pad columns,
+// 32-aligned. plan_umma keeps a_first_col + 32 Q <= 512.
+__host__ __device__ constexpr uint32_t a_first_col(int T, int n_pad)
+{
+    return (static_cast<uint32_t>(T * n_pad) + 31u) & ~31u;
 }
 
 // Group of matrices with the same K reading the same activations: tensor maps of each
@@ -113,14 +127,15 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n)
     return (1u << 4) | (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate)
+// D (+)= A x B with A in tensor memory (128 lanes = rows, fp16 pairs along columns).
+__device__ __forceinline__ void umma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate)
 {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -134,6 +149,20 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 16 consecutive 32-bit columns of this thread's TMEM lane from v (warp-wide,
+// .sync.aligned); the stores are complete when tcgen05.wait::st returns.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+        "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 16 consecutive fp32 columns of this thread's TMEM lane (warp-wide, .sync.aligned).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
@@ -159,11 +188,12 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
 // the T accumulators in a fixed order, so results do not depend on the interleaving.
 template <bool kFp4>
 __global__ void __launch_bounds__(kThreadsUmma, 1)
-    wq_umma_kernel(const __grid_constant__ UmmaParams p, int M, int64_t K, int n_pad, int S, int R, int Q, int T,
+    wq_umma_kernel(const __grid_constant__ UmmaParams p, int M, int64_t K, int n_pad, int S, int rb, int Q, int T,
                    uint32_t tmem_cols)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    const int R = T * rb;   // activation slices: rb per issuing thread
     const UmmaLayout L = umma_layout(kFp4, S, R, Q, n_pad);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int kStepK = step_k(kFp4);
@@ -183,7 +213,8 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L.off_misc);
     volatile uint32_t *abort_word = reinterpret_cast<volatile uint32_t *>(smem + L.off_misc + 4);
     uint8_t *codes_ring = smem + L.off_codes, *scales_ring = smem + L.off_scales;
-    uint8_t *b_ring = smem + L.off_b, *a_buf = smem + L.off_a;
+    uint8_t *b_ring = smem + L.off_b;
+    const uint32_t a_col0 = a_first_col(T, n_pad);   // TMEM: accumulators, then the A buffers
 
     auto locate = [&](int tile, int &mi, int &row0) {
         mi = 0;
@@ -193,6 +224,11 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
         row0 = (tile - p.tile_start[mi]) * kTileRows;
     };
     auto fail = [&]() { note_wait_timeout(&g_umma_error, abort_word); };
+    // K step g sits in slot (g % 3) + 3 ((g / 3) % (S / 3)): producer g % 3's own slots,
+    // the (g / S)-th use of that slot
+    auto stage_slot = [&](int g) {
+        return g % kWeightProducers + kWeightProducers * ((g / kWeightProducers) % (S / kWeightProducers));
+    };
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -204,7 +240,7 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
             mbar_init(&b_free[j], 1);
         }
         for (int j = 0; j < Q; ++j) {
-            mbar_init(&a_full[j], kDecodeWarps);
+            mbar_init(&a_full[j], kDecodeWarps / kDecodeGroups);
             mbar_init(&a_free[j], 1);
         }
         mbar_init(acc_full, used);
@@ -225,16 +261,17 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
     const uint32_t tmem = *tmem_slot;
     grid_launch_dependents();
 
-    if (warp == 0) {
-        // ------------------------------------------------ weight producer (one thread)
-        // Weights do not depend on the preceding kernel: the ring fills before the
-        // dependency wait (this thread never waits for it: it touches no activation).
+    if (warp < kWeightProducers) {
+        // ------------------------------------------------ weight producers (one thread each)
+        // Producer w loads the K steps g with g % 3 == w into its own slots. Weights do
+        // not depend on the preceding kernel: the ring fills before the dependency wait
+        // (these threads never wait for it: they touch no activation).
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             const uint32_t tx = kCodesBox + (kFp4 ? kScalesBox : 0);
-            int issued = 0;
-            for (int g = 0; g < total_steps && !*abort_word; ++g) {
-                const int s = g % S;
+            int last = -1;
+            for (int g = warp; g < total_steps && !*abort_word; g += kWeightProducers) {
+                const int s = stage_slot(g);
                 if (g >= S && !mbar_wait_bounded(&w_free[s], static_cast<uint32_t>((g / S) - 1) & 1u)) {
                     fail();
                     break;
@@ -245,38 +282,37 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
                 mbar_arrive_expect_tx(&w_full[s], tx);
                 tma_load_2d(codes_ring + s * kCodesBox, &p.codes[mi], st * 128, row0, &w_full[s], pol);
                 if (kFp4) tma_load_2d(scales_ring + s * kScalesBox, &p.scales[mi], st * 16, row0, &w_full[s], pol);
-                issued = g + 1;
+                last = g;
             }
-            for (int g = max(0, issued - S); g < issued; ++g)   // every copy lands before the CTA can exit
-                (void)mbar_wait_bounded(&w_full[g % S], static_cast<uint32_t>(g / S) & 1u);
-        }
-    } else if (warp == 2) {
-        // ------------------------------------------------ activation producer (one thread): 64-k slices
-        if (lane == 0) {
-            grid_dependency_wait();
-            const uint64_t pol_x = policy_evict_last();
-            int issued = 0;
-            for (int h = 0; h < total_quarters && !*abort_word; ++h) {
-                const int j = h % R;
-                if (h >= R && !mbar_wait_bounded(&b_free[j], static_cast<uint32_t>((h / R) - 1) & 1u)) {
-                    fail();
-                    break;
-                }
-                const int kq = h % tile_quarters;   // 64-k slice of K
-                mbar_arrive_expect_tx(&b_full[j], L.b_bytes);
-                tma_load_2d(b_ring + j * L.b_bytes, &p.x, kq * kQuarterK, 0, &b_full[j], pol_x);
-                issued = h + 1;
-            }
-            for (int h = max(0, issued - R); h < issued; ++h)
-                (void)mbar_wait_bounded(&b_full[h % R], static_cast<uint32_t>(h / R) & 1u);
+            // every copy lands before the CTA can exit (the slot of a step within the last S
+            // has not been reused, so its phase is the one that step's copy completes)
+            for (int g = warp; g <= last; g += kWeightProducers)
+                if (g > last - S) (void)mbar_wait_bounded(&w_full[stage_slot(g)], static_cast<uint32_t>(g / S) & 1u);
         }
     } else if (warp >= kFirstIssuerWarp) {
         // ------------------------------------------------ MMA issue: thread t takes quarters t, t + T, ...
+        // of every tile, and streams their activation slices itself through its own rb
+        // slots (slot t + T (i % rb) for its i-th quarter): a single thread sustains only
+        // a few TMA copies per microsecond under load, so the copies are spread over the
+        // T issuing threads.
         const int t = warp - kFirstIssuerWarp;
         if (lane == 0 && t < T) {
             const uint32_t idesc = idesc_f16_f32(kTileRows, n_pad);
             const uint32_t d_tmem = tmem + static_cast<uint32_t>(t * n_pad);
+            const int per_tile = t < tile_quarters ? (tile_quarters - t + T - 1) / T : 0;
+            const int nmine = nt * per_tile;
+            auto bslot = [&](int i) { return t + T * (i % rb); };
+            grid_dependency_wait();   // the activations may be written by the preceding kernel
+            const uint64_t pol_x = policy_evict_last();
+            auto load_b = [&](int i) {
+                const int jb = bslot(i), kq = t + T * (i % per_tile);
+                mbar_arrive_expect_tx(&b_full[jb], L.b_bytes);
+                tma_load_2d(b_ring + jb * L.b_bytes, &p.x, kq * kQuarterK, 0, &b_full[jb], pol_x);
+            };
+            int loaded = 0;
+            for (; loaded < rb && loaded < nmine; ++loaded) load_b(loaded);
             bool ok = true, any = false;
+            int i = 0;   // this thread's quarters so far
             for (int lt = 0; lt < nt && ok; ++lt) {
                 if (lt >= 1 && t < used &&   // the read-back of the previous tile is done
                     !mbar_wait_bounded(acc_free, static_cast<uint32_t>(lt - 1) & 1u)) {
@@ -285,22 +321,32 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
                 }
                 tc_fence_after();
                 bool first = true;
-                for (int kq = t; kq < tile_quarters && ok; kq += T) {
+                for (int kq = t; kq < tile_quarters && ok; kq += T, ++i) {
                     const int h = lt * tile_quarters + kq;
-                    const int ja = h % Q, jb = h % R;
-                    if (*abort_word || !mbar_wait_bounded(&b_full[jb], static_cast<uint32_t>(h / R) & 1u) ||
+                    const int ja = h % Q, jb = bslot(i);
+                    // refill the slot of the previous quarter (loaded == i - 1 + rb) once its
+                    // products are done
+                    if (i >= 1 && loaded < nmine) {
+                        if (*abort_word || !mbar_wait_bounded(&b_free[bslot(i - 1)], static_cast<uint32_t>((i - 1) / rb) & 1u)) {
+                            fail();
+                            ok = false;
+                            break;
+                        }
+                        load_b(loaded++);
+                    }
+                    if (*abort_word || !mbar_wait_bounded(&b_full[jb], static_cast<uint32_t>(i / rb) & 1u) ||
                         !mbar_wait_bounded(&a_full[ja], static_cast<uint32_t>(h / Q) & 1u)) {
                         fail();
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_base = smem_addr(a_buf + ja * kABytes);
+                    const uint32_t a_tmem = tmem + a_col0 + static_cast<uint32_t>(ja * kACols);
                     const uint32_t b_base = smem_addr(b_ring + jb * L.b_bytes);
 #pragma unroll
-                    for (int kk = 0; kk < kQuarterK / 16; ++kk)
-                        umma_f16(d_tmem, smem_desc_sw128(a_base + 32u * kk), smem_desc_sw128(b_base + 32u * kk), idesc,
-                                 (first && kk == 0) ? 0u : 1u);
+                    for (int kk = 0; kk < kQuarterK / 16; ++kk)   // k 16 kk ..: A columns 8 kk .., B bytes 32 kk ..
+                        umma_f16_ta(d_tmem, a_tmem + 8u * kk, smem_desc_sw128(b_base + 32u * kk), idesc,
+                                    (first && kk == 0) ? 0u : 1u);
                     first = false;
                     any = true;
                     umma_commit(&a_free[ja]);   // the A buffer and the activation slice are free once
@@ -308,78 +354,95 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
                 }
                 if (ok && t < used) umma_commit(acc_full);   // this thread's share of the tile is done
             }
-            // every product this thread issued has completed before the tensor memory is released
+            // every product this thread issued has completed before the tensor memory is
+            // released, and every activation copy it started has landed
             if (any) {
                 umma_commit(done);
             } else {
                 mbar_arrive(done);
             }
             (void)mbar_wait_bounded(done, 0u);
+            for (int k = i; k < loaded; ++k) (void)mbar_wait_bounded(&b_full[bslot(k)], static_cast<uint32_t>(k / rb) & 1u);
         }
         __syncwarp();
     } else if (warp >= kFirstDecodeWarp) {
         // ------------------------------------------------ decode, then read back
-        // Two threads per weight row: warps 3..6 take k groups 0..3 of every 64-k
-        // buffer, warps 7..10 groups 4..7; the row is this warp's TMEM lane quarter.
+        // Two groups of four warps take alternate 64-k quarters (group gq the quarters
+        // h with h % 2 == gq; K steps hold an even number of quarters). In a group, warp
+        // w decodes the rows of its TMEM lane quarter 32 (w % 4) .. + 31, one row per
+        // thread, all 64 k of the quarter: 32 TMEM columns of fp16 pairs. Waits are made
+        // warp-uniform, since the tensor-memory accesses that follow them are
+        // .sync.aligned.
         const int r = 32 * (warp & 3) + lane;
-        const int hf = (warp - kFirstDecodeWarp) >> 2;
-        uint8_t *a_row = a_buf + r * 128;   // chunk c (k 8c .. 8c + 7) at 16 (c ^ (r % 8))
-        const int sw = r & 7;
+        const int gq = (warp - kFirstDecodeWarp) >> 2;
+        const uint32_t a_lane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + a_col0;
+        const int sw = r & 7;   // the codes box's 128-byte swizzle: chunk c of row r at c ^ (r % 8)
+        auto wait_all = [&](uint64_t *bar, uint32_t parity) {
+            return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity) ? 1 : 0) != 0;
+        };
         int g = 0, h = 0;
         bool ok = true, waited = false;
         for (int lt = 0; lt < nt && ok; ++lt) {
             int mi, row0;
             locate(static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) * lt, mi, row0);
             for (int st = 0; st < nsteps && ok; ++st, ++g) {
-                const int s = g % S;
-                if (*abort_word || !mbar_wait_bounded(&w_full[s], static_cast<uint32_t>(g / S) & 1u)) {
+                const int s = stage_slot(g);
+                if (*abort_word || !wait_all(&w_full[s], static_cast<uint32_t>(g / S) & 1u)) {
                     fail();
                     ok = false;
                     break;
                 }
                 const uint8_t *crow = codes_ring + s * kCodesBox + r * 128;
-                for (int q = 0; q < kQuarters; ++q, ++h) {
-                    const int j = h % Q;
-                    if (h >= Q && !mbar_wait_bounded(&a_free[j], static_cast<uint32_t>((h / Q) - 1) & 1u)) {
+                for (int q = gq; q < kQuarters; q += kDecodeGroups) {
+                    const int hq = h + q, j = hq % Q;
+                    if (hq >= Q && !wait_all(&a_free[j], static_cast<uint32_t>((hq / Q) - 1) & 1u)) {
                         fail();
                         ok = false;
                         break;
                     }
-                    uint8_t *dst = a_row + j * kABytes;
+                    tc_fence_after();   // the products that read this buffer before are complete
+                    uint32_t av[32];    // k pairs (2i, 2i + 1) of the quarter: TMEM column i
                     if (kFp4) {
-                        // k 64q + 32hf .. + 31: code chunk 2q + hf (swizzled by row), groups 4q + 2hf, + 1
-                        const uint4 c = *reinterpret_cast<const uint4 *>(crow + 16 * ((2 * q + hf) ^ sw));
-                        const uint32_t s2 = *reinterpret_cast<const uint16_t *>(scales_ring + s * kScalesBox + r * 16 +
-                                                                                 4 * q + 2 * hf);
-                        const uint32_t s01 = e4m3x2_to_f16x2(s2);
-                        const uint32_t sc0 = dup_lo16(s01), sc1 = dup_hi16(s01);
-                        const uint32_t cw[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-                        for (int kg = 0; kg < 4; ++kg) {   // 8 k: one word of codes, group kg / 2
-                            uint32_t hv[4];
-                            e2m1x8_to_f16x2(cw[kg], hv);
-                            const uint32_t gsc = kg < 2 ? sc0 : sc1;
-                            *reinterpret_cast<uint4 *>(dst + 16 * ((4 * hf + kg) ^ sw)) =
-                                make_uint4(hmul2_u32(hv[0], gsc), hmul2_u32(hv[1], gsc), hmul2_u32(hv[2], gsc),
-                                           hmul2_u32(hv[3], gsc));
-                        }
-                    } else {
-                        // k 64q + 32hf .. + 31: code chunks 4q + 2hf, + 1, 8 bytes per k8 group
+                        // k 64q .. + 63: code chunks 2q, 2q + 1 (swizzled by row), groups 4q .. 4q + 3
+                        const uint32_t s4 =
+                            *reinterpret_cast<const uint32_t *>(scales_ring + s * kScalesBox + r * 16 + 4 * q);
+                        const uint32_t s01 = e4m3x2_to_f16x2(s4 & 0xffffu), s23 = e4m3x2_to_f16x2(s4 >> 16);
+                        const uint32_t sc[4] = {dup_lo16(s01), dup_hi16(s01), dup_lo16(s23), dup_hi16(s23)};
 #pragma unroll
                         for (int c = 0; c < 2; ++c) {
-                            const uint4 v = *reinterpret_cast<const uint4 *>(crow + 16 * ((4 * q + 2 * hf + c) ^ sw));
-                            *reinterpret_cast<uint4 *>(dst + 16 * ((4 * hf + 2 * c) ^ sw)) =
-                                make_uint4(e4m3x2_to_f16x2(v.x & 0xffffu), e4m3x2_to_f16x2(v.x >> 16),
-                                           e4m3x2_to_f16x2(v.y & 0xffffu), e4m3x2_to_f16x2(v.y >> 16));
-                            *reinterpret_cast<uint4 *>(dst + 16 * ((4 * hf + 2 * c + 1) ^ sw)) =
-                                make_uint4(e4m3x2_to_f16x2(v.z & 0xffffu), e4m3x2_to_f16x2(v.z >> 16),
-                                           e4m3x2_to_f16x2(v.w & 0xffffu), e4m3x2_to_f16x2(v.w >> 16));
+                            const uint4 cv = *reinterpret_cast<const uint4 *>(crow + 16 * ((2 * q + c) ^ sw));
+                            const uint32_t cw[4] = {cv.x, cv.y, cv.z, cv.w};
+#pragma unroll
+                            for (int kg = 0; kg < 4; ++kg) {   // 8 k: one word of codes, group 2c + kg / 2
+                                uint32_t hv[4];
+                                e2m1x8_to_f16x2(cw[kg], hv);
+                                const uint32_t gsc = sc[2 * c + (kg >> 1)];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) av[16 * c + 4 * kg + i] = hmul2_u32(hv[i], gsc);
+                            }
+                        }
+                    } else {
+                        // k 64q .. + 63: code chunks 4q .. 4q + 3 (16 k each)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 v = *reinterpret_cast<const uint4 *>(crow + 16 * ((4 * q + c) ^ sw));
+                            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) {
+                                av[8 * c + 2 * i] = e4m3x2_to_f16x2(wv[i] & 0xffffu);
+                                av[8 * c + 2 * i + 1] = e4m3x2_to_f16x2(wv[i] >> 16);
+                            }
                         }
                     }
-                    fence_proxy_async_shared();   // the generic writes of A before the tensor core reads it
+                    const uint32_t ta = a_lane + static_cast<uint32_t>(j * kACols);
+                    tmem_st16(ta, *reinterpret_cast<const uint32_t(*)[16]>(av));
+                    tmem_st16(ta + 16u, *reinterpret_cast<const uint32_t(*)[16]>(av + 16));
+                    tmem_wait_st();
+                    tc_fence_before();   // the stores before the arrival the MMA thread waits on
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&a_full[j]);
                 }
+                h += kQuarters;
                 if (ok && lane == 0) mbar_arrive(&w_free[s]);   // (the warp's reads fenced above)
             }
             if (!ok) break;
@@ -390,7 +453,7 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
                 grid_dependency_wait();
                 waited = true;
             }
-            if (!mbar_wait_bounded(acc_full, static_cast<uint32_t>(lt) & 1u)) {
+            if (!wait_all(acc_full, static_cast<uint32_t>(lt) & 1u)) {
                 fail();
                 break;
             }
@@ -398,7 +461,7 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
             const int64_t n = row0 + r, Nm = p.N[mi];
             const float scale = kFp4 ? p.g[mi] : (n < Nm ? __ldg(p.row_scale[mi] + n) : 0.0f);
             const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
-            for (int c16 = 16 * hf; c16 < n_pad; c16 += 32) {
+            for (int c16 = 16 * gq; c16 < n_pad; c16 += 32) {
                 float v[16];
                 tmem_ld16(taddr + static_cast<uint32_t>(c16), v);
                 for (int a = 1; a < used; ++a) {
@@ -443,27 +506,43 @@ cudaError_t plan_umma(bool fp4, const DeviceInfo &dev, int64_t tiles, int M, int
 {
     UmmaPlan pl;
     pl.n_pad = 16 * ((M + 15) / 16);
-    // MMA-issuing threads T, each with one accumulator of n_pad columns (512 columns in
-    // all), one 64-k A buffer and one activation slice: thread t takes quarters t, t + T,
-    // ... and always the same buffers, so it waits for every phase of them in order (with
-    // fewer buffers than threads a thread could reach a buffer's next phase while the
-    // previous one is pending and pass its parity test on the phase before). Then as many
-    // weight stages (the bytes in flight from HBM) as shared memory holds, at least 3.
-    int T = std::max(1, std::min({kMaxIssuers, 512 / pl.n_pad, env_int("QMV_UMMA_ISSUERS", kMaxIssuers)}));
-    auto fits = [&](int s_, int t_) {
-        return umma_layout(fp4, s_, std::max(2, t_), std::max(2, t_), pl.n_pad).total + 1024 <=
-               static_cast<uint32_t>(dev.smem_optin);
+    // Tensor memory (512 columns) holds T accumulators of n_pad columns, one per
+    // MMA-issuing thread, and Q 64-k A buffers of 32 columns. T is as large as leaves
+    // room for max(T, 6) A buffers (the decode runs up to Q quarters ahead of the
+    // products). Q is even and >= T: the two decode groups take alternate quarters, so
+    // each A buffer is written by one group only, and thread t (quarters t, t + T, ...)
+    // reaches a buffer's next phase only after the phase it waited for before (with
+    // fewer buffers than threads it could meet a buffer two phases behind and pass its
+    // parity test on the phase before). Each issuing thread streams its activation
+    // slices through rb slots: enough for about 12 quarters of the CTA in flight. Shared
+    // memory then takes as many weight stages as fit, a multiple of the 3 producers,
+    // 3 .. 12. QMV_UMMA_ISSUERS / QMV_UMMA_ABUFS / QMV_UMMA_STAGES cap T, Q and S;
+    // QMV_UMMA_BBUFS sets rb.
+    const int t_cap = std::max(1, std::min(kMaxIssuers, env_int("QMV_UMMA_ISSUERS", kMaxIssuers)));
+    auto q_room = [&](int t_) {
+        return (kTmemCols - static_cast<int>(a_first_col(t_, pl.n_pad))) / kACols;
     };
-    while (T > 1 && !fits(3, T)) --T;
-    int S = std::max(2, std::min(kMaxStages, env_int("QMV_UMMA_STAGES", kMaxStages)));
-    while (S > 2 && !fits(S, T)) --S;
+    auto even_up = [](int v) { return (v + 1) & ~1; };
+    int T = t_cap;
+    while (T > 1 && (q_room(T) & ~1) < std::max(even_up(T), 6)) --T;
+    if ((q_room(T) & ~1) < std::max(even_up(T), 2)) return cudaErrorInvalidValue;
+    const int Q = std::max(std::max(2, even_up(T)),
+                           std::min({kMaxABufs, q_room(T), env_int("QMV_UMMA_ABUFS", kMaxABufs)}) & ~1);
+    int rb = std::max(2, std::min(kMaxSlicesPerIssuer, env_int("QMV_UMMA_BBUFS", (12 + T - 1) / T)));
+    auto fits = [&](int s_, int rb_) {
+        return umma_layout(fp4, s_, T * rb_, Q, pl.n_pad).total + 1024 <= static_cast<uint32_t>(dev.smem_optin);
+    };
+    while (rb > 2 && !fits(kWeightProducers, rb)) --rb;
+    int S = std::max(kWeightProducers, std::min(kMaxStages, env_int("QMV_UMMA_STAGES", kMaxStages))) /
+            kWeightProducers * kWeightProducers;
+    while (S > kWeightProducers && !fits(S, rb)) S -= kWeightProducers;
     pl.T = T;
     pl.S = S;
-    pl.Q = pl.R = std::max(2, T);
+    pl.Q = Q;
+    pl.R = T * rb;
     pl.smem = umma_layout(fp4, pl.S, pl.R, pl.Q, pl.n_pad).total + 1024;
     if (pl.smem > static_cast<uint32_t>(dev.smem_optin) || K % step_k(fp4) != 0) return cudaErrorInvalidValue;
-    pl.tmem_cols = 32;
-    while (pl.tmem_cols < static_cast<uint32_t>(T * pl.n_pad)) pl.tmem_cols <<= 1;
+    pl.tmem_cols = kTmemCols;
     pl.grid = static_cast<int>(std::min<int64_t>(tiles, dev.sm_count));
     *out = pl;
     return cudaSuccess;
@@ -481,7 +560,7 @@ cudaError_t launch_umma(const DeviceInfo &dev, const WqGroup &grp, const uint16_
     UmmaPlan pl;
     cudaError_t pe = plan_umma(kFp4, dev, tiles, M, K, &pl);
     if (pe != cudaSuccess) return pe;
-    const int n_pad = pl.n_pad, S = pl.S, R = pl.R, Q = pl.Q, T = pl.T;
+    const int n_pad = pl.n_pad, S = pl.S, R = pl.R, Q = pl.Q, T = pl.T, rb = R / T;
     const uint32_t smem = pl.smem, cols = pl.tmem_cols;
     UmmaParams p{};
     p.count = grp.count;
@@ -521,7 +600,7 @@ cudaError_t launch_umma(const DeviceInfo &dev, const WqGroup &grp, const uint16_
                      "tmem=%u\n",
                      kFp4 ? "nvfp4" : "fp8", M, n_pad, static_cast<long long>(K), tiles, S, R, Q, T, cfg.gridDim.x,
                      smem, cols);
-    return cudaLaunchKernelEx(&cfg, kern, p, M, K, n_pad, S, R, Q, T, cols);
+    return cudaLaunchKernelEx(&cfg, kern, p, M, K, n_pad, S, rb, Q, T, cols);
 }
 
 }  // namespace

@@ -65,9 +65,12 @@ def test_chunked_band(M, monkeypatch):
 @pytest.mark.parametrize("fp4", [True, False])
 @pytest.mark.parametrize("M", [16, 17, 24, 32, 33, 48, 64, 80, 96])
 def test_tcgen05_band(fp4, M):
-    """From 17 rows (NVFP4) / 33 (FP8) one pass on the tcgen05 kernel: 128-row tiles, T
-    issuing threads with an accumulator of 16 ceil(M / 16) columns each in 512 columns of
-    tensor memory, at least 3 weight stages, shared memory within the device's limit."""
+    """From 17 rows (NVFP4) / 33 (FP8) one pass on the tcgen05 kernel: 128-row tiles; T
+    issuing threads with an accumulator of 16 ceil(M / 16) columns each and Q >= max(T, 2)
+    64-k A buffers of 32 columns (an even count: two decode groups take alternate
+    buffers), all within the 512 columns of tensor memory (the A
+    buffers from the first 32-aligned column after the accumulators); R >= T activation
+    slices; at least 3 weight stages; shared memory within the device's limit."""
     N, K = 17408, 5120
     p = plan(M, K, N, fp4=fp4)
     if M < UMMA_MIN_M[fp4]:
@@ -75,8 +78,11 @@ def test_tcgen05_band(fp4, M):
         return
     n_pad = 16 * math.ceil(M / 16)
     assert (p["route"], p["chunks"], p["chunk_rows"]) == (UMMA[fp4], 1, M)
-    assert 1 <= p["warps"] <= min(8, 512 // n_pad) and p["warps"] * n_pad <= 512
-    assert 3 <= p["slots"] <= 8 and p["smem_bytes"] <= GB300_DEVICE["smem_optin"]
+    T, Q, R = p["warps"], p["a_bufs"], p["b_bufs"]
+    assert 1 <= T <= 8 and Q >= max(T, 2) and Q % 2 == 0 and R >= max(T, 2)
+    assert 32 * math.ceil(T * n_pad / 32) + 32 * Q <= 512
+    assert Q >= min(6, (512 - 32 * math.ceil(T * n_pad / 32)) // 32)   # room for the decode to run ahead
+    assert 3 <= p["slots"] <= 12 and p["smem_bytes"] <= GB300_DEVICE["smem_optin"]
     assert p["grid"] == min(math.ceil(N / 128), GB300_DEVICE["sm_count"])
 
 
