@@ -149,10 +149,11 @@ WORKLOADS["q4_k_12288x4096_m1"] = dict(M=1, mats=lambda: [("q4_k", 12288, 4096)]
                                        desc="Q4_K GEMV M=1, 12288x4096 (Qwen3-8B gate), 16 rotated copies")
 for _m in (32, 96):
     WORKLOADS[f"fp8_7168x5120_m{_m}"] = dict(M=_m, mats=lambda: [("fp8", 7168, 5120)] * 12,
-                                            desc=f"FP8 W8A16 7168x5120, M={_m} (chunks of <= 16 rows), 12 rotated copies")
+                                            desc=f"FP8 W8A16 7168x5120, M={_m} (one tcgen05 pass, K split over 2 CTAs), "
+                                                 "12 rotated copies")
 WORKLOADS["mixed_27b_m32"] = dict(M=32, mats=lambda: dense_27b_stack(True), stages=lambda: dense_27b_stages(True),
                                   desc="27B-class stack, FP8 attention every 4th layer + NVFP4 lm_head, M=32 "
-                                       "(chunks of 16 rows)")
+                                       "(tcgen05, K split on the 5120/7168-row matrices)")
 for _m in (1, 8, 16, 24, 32, 48, 64, 96):
     WORKLOADS[f"nvfp4_17408x5120_m{_m}"] = dict(M=_m, mats=lambda: [("nvfp4", 17408, 5120)] * 8,
                                                desc=f"NVFP4 W4A16 17408x5120, M={_m}, 8 rotated copies")

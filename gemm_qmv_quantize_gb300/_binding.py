@@ -322,7 +322,7 @@ def qmv_debug_plan_q4(M: int, N: int, K: int, q4k: bool = False, n_inputs: int =
 
 
 WQ_PLAN_FIELDS = ("route", "chunks", "chunk_rows", "warps", "slots", "staged", "passes", "tiles_per_round",
-                  "ctas_per_sm", "grid", "smem_bytes", "a_bufs", "b_bufs")
+                  "ctas_per_sm", "grid", "smem_bytes", "a_bufs", "b_bufs", "k_splits")
 
 
 def qmv_debug_plan_wq(M: int, K: int, N, fp4: bool = True, aligned16: bool = True, ctas_by_regs=None,

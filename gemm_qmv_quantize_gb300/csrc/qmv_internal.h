@@ -121,7 +121,7 @@ cudaError_t launch_fp8(Route r, const DeviceInfo &dev, const WqGroup &grp, const
 // row tiles) and 16-warp kernels allow. out: route, chunks, rows of the first chunk,
 // warps, slots, staged, passes, tiles per round, CTAs per SM, grid, shared memory.
 cudaError_t debug_plan_wq(bool fp4, const DeviceInfo &dev, int M, int64_t K, int count, const int64_t *N,
-                          bool aligned16, const int ctas_by_regs[3], int64_t out[13]);
+                          bool aligned16, const int ctas_by_regs[3], int64_t out[14]);
 
 // Device error words of each translation unit (read synchronously; optionally cleared).
 cudaError_t read_error_word_q4_0(uint32_t *out, bool clear);
@@ -143,13 +143,16 @@ cudaError_t encode_map_nd(CUtensorMap *map, CUtensorMapDataType dtype, int rank,
 struct UmmaPlan {
     int n_pad = 0;        // activation rows padded to a multiple of 16 (the MMA's N)
     int T = 0, S = 0, Q = 0, R = 0;   // issuing threads, weight stages, A buffers, activation slices
+    int splits = 1;       // CTAs (a cluster) sharing a tile, each a range of K
     int grid = 0;
     uint32_t smem = 0, tmem_cols = 0;
 };
 // The tcgen05 kernel's plan for `tiles` 128-row tiles (no CUDA call).
 cudaError_t plan_umma(bool fp4, const DeviceInfo &dev, int64_t tiles, int M, int64_t K, UmmaPlan *out);
-// First M the tcgen05 kernel takes by default (QMV_WQ_UMMA_MIN_M overrides; 0 = never).
-int umma_min_m(bool fp4);
+// First M the tcgen05 kernel takes for a launch of `tiles` 128-row tiles: 17, or 9 when
+// the tiles fill at most a third of the SMs (QMV_WQ_UMMA_MIN_M / QMV_WQ_UMMA_FEW_TILES_MIN_M
+// override; QMV_WQ_UMMA_MIN_M = 0: never).
+int umma_min_m(bool fp4, const DeviceInfo &dev, int64_t tiles);
 cudaError_t launch_nvfp4_umma(const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M, int64_t K,
                               cudaStream_t s);
 cudaError_t launch_fp8_umma(const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M, int64_t K,

@@ -726,12 +726,14 @@ namespace {
 // the tensor-core kernel (one or two 8-row tiles per weight pass). Chunk c + 1
 // reads the same weights right after chunk c, from L2 when the group's weights fit
 // there. The generic kernel takes any M in 8-row launches already.
-// The tcgen05 kernel takes a call from umma_min_m(fp4) activation rows on, when its
-// operands suit TMA: K a multiple of the step, codes, scales and x 16-byte aligned (the
-// tensor-core route already requires all but the scales).
-bool umma_applies(bool fp4, const WqGroup &grp, int M)
+// The tcgen05 kernel takes a call from umma_min_m(fp4, tiles) activation rows on, when
+// its operands suit TMA: K a multiple of the step, codes, scales and x 16-byte aligned
+// (the tensor-core route already requires all but the scales).
+bool umma_applies(bool fp4, const DeviceInfo &dev, const WqGroup &grp, int M)
 {
-    const int min_m = umma_min_m(fp4);
+    int64_t tiles = 0;
+    for (int i = 0; i < grp.count; ++i) tiles += (grp.N[i] + 127) / 128;
+    const int min_m = umma_min_m(fp4, dev, tiles);
     if (min_m <= 0 || M < min_m || M > 96) return false;
     for (int i = 0; i < grp.count; ++i)
         if (fp4 && grp.N[i] > 0 && !aligned16(grp.scales[i])) return false;
@@ -742,7 +744,7 @@ template <bool kFp4>
 cudaError_t launch_wq_chunked(Route r, const DeviceInfo &dev, const WqGroup &grp, const uint16_t *x, int M,
                               int64_t K, cudaStream_t s)
 {
-    if ((r == kRouteNvfp4Mma || r == kRouteFp8Mma) && umma_applies(kFp4, grp, M))
+    if ((r == kRouteNvfp4Mma || r == kRouteFp8Mma) && umma_applies(kFp4, dev, grp, M))
         return kFp4 ? launch_nvfp4_umma(dev, grp, x, M, K, s) : launch_fp8_umma(dev, grp, x, M, K, s);
     if (M <= 16 || (r != kRouteNvfp4Mma && r != kRouteFp8Mma)) return launch_wq<kFp4>(r, dev, grp, x, M, K, s);
     const int nch = (M + 15) / 16;
@@ -761,15 +763,29 @@ cudaError_t launch_wq_chunked(Route r, const DeviceInfo &dev, const WqGroup &grp
 }  // namespace
 
 // Where the chunked mma.sync path would take several passes over the weights, the
-// tcgen05 kernel's one pass wins (measured, GB/s, mma.sync / tcgen05: NVFP4 17408 x 5120
-// at M = 16: 1949 / 1364, 24: 1058 / 1373, 48: 695 / 1414, 96: 373 / 1499; FP8 7168 x
-// 5120 at M = 32: 1332 / 1028, 48: 903 / 1018, 96: 477 / 1039).
-int umma_min_m(bool fp4) { return env_int("QMV_WQ_UMMA_MIN_M", fp4 ? 17 : 33); }
+// tcgen05 kernel's one pass wins (measured in chains of calls, GB/s, mma.sync / tcgen05:
+// NVFP4 17408 x 5120 at M = 16: 1945 / 1818, 24: 1058 / 1817, 48: 693 / 1798, 96: 372 /
+// 1633; FP8 7168 x 5120 at M = 16: 2595 / 1805, 24: 1395 / 1688, 32: 1336 / 1631, 96:
+// 479 / 1282). A launch of at most a third of the SMs' worth of tiles splits K over
+// three or more CTAs of a cluster on the tcgen05 kernel, which then wins from 9 rows
+// (27B-class stack at M = 16, its 5120-row matrices split in three: 1295 -> 1747 GB/s;
+// at M = 8 the mma.sync kernel stays ahead, 2645 / 2090; with only two CTAs per tile,
+// FP8 7168 x 5120 at M = 16, it stays ahead too, 2567 / 1804).
+// QMV_WQ_UMMA_MIN_M moves the threshold (0: the tcgen05 kernel is never taken);
+// QMV_WQ_UMMA_FEW_TILES_MIN_M that of launches of few tiles.
+int umma_min_m(bool fp4, const DeviceInfo &dev, int64_t tiles)
+{
+    (void)fp4;
+    const int base = env_int("QMV_WQ_UMMA_MIN_M", 17);
+    if (base <= 0) return 0;
+    if (tiles * 3 <= dev.sm_count) return env_int("QMV_WQ_UMMA_FEW_TILES_MIN_M", std::min(base, 9));
+    return base;
+}
 
 cudaError_t debug_plan_wq(bool fp4, const DeviceInfo &dev, int M, int64_t K, int count, const int64_t *N,
-                          bool aligned16, const int ctas_by_regs[3], int64_t out[13])
+                          bool aligned16, const int ctas_by_regs[3], int64_t out[14])
 {
-    for (int i = 0; i < 13; ++i) out[i] = 0;
+    for (int i = 0; i < 14; ++i) out[i] = 0;
     const bool mma = aligned16 && K % (fp4 ? 256 : 128) == 0;
     if (!mma) {   // the generic kernel, 8 activation rows per launch
         if (count != 1) return cudaErrorInvalidValue;
@@ -780,16 +796,16 @@ cudaError_t debug_plan_wq(bool fp4, const DeviceInfo &dev, int M, int64_t K, int
     }
     int64_t ntiles = 0;
     for (int i = 0; i < count; ++i) ntiles += (N[i] + kRowsPerCta - 1) / kRowsPerCta;
-    const int min_m = umma_min_m(fp4);
+    int64_t tiles = 0;
+    for (int i = 0; i < count; ++i) tiles += (N[i] + 127) / 128;
+    const int min_m = umma_min_m(fp4, dev, tiles);
     if (min_m > 0 && M >= min_m) {   // the tcgen05 kernel: 128-row tiles, one pass for all M rows
-        int64_t tiles = 0;
-        for (int i = 0; i < count; ++i) tiles += (N[i] + 127) / 128;
         UmmaPlan pl;
         const cudaError_t e = plan_umma(fp4, dev, std::max<int64_t>(tiles, 1), M, K, &pl);
         if (e != cudaSuccess) return e;
-        const int64_t v[13] = {fp4 ? kRouteNvfp4Umma : kRouteFp8Umma, 1, M, pl.T, pl.S, 1, 1, 1, 1,
-                               tiles ? pl.grid : 0, static_cast<int64_t>(pl.smem), pl.Q, pl.R};
-        for (int i = 0; i < 13; ++i) out[i] = v[i];
+        const int64_t v[14] = {fp4 ? kRouteNvfp4Umma : kRouteFp8Umma, 1, M, pl.T, pl.S, 1, 1, 1, 1,
+                               tiles ? pl.grid : 0, static_cast<int64_t>(pl.smem), pl.Q, pl.R, pl.splits};
+        for (int i = 0; i < 14; ++i) out[i] = v[i];
         return cudaSuccess;
     }
     const int nch = M > 16 ? (M + 15) / 16 : 1;

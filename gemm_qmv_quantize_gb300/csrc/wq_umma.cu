@@ -164,6 +164,23 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// All threads of every CTA of the cluster (release / acquire: shared-memory writes
+// before it are visible to the cluster's reads after it).
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The float at the same shared-memory offset in the cluster's CTA `rank`.
+__device__ __forceinline__ float ld_peer_f32(const float *local, int rank)
+{
+    uint32_t remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_addr(local)), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
 // 16 consecutive fp32 columns of this thread's TMEM lane (warp-wide, .sync.aligned).
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
 {
@@ -189,7 +206,7 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
 template <bool kFp4>
 __global__ void __launch_bounds__(kThreadsUmma, 1)
     wq_umma_kernel(const __grid_constant__ UmmaParams p, int M, int64_t K, int n_pad, int S, int rb, int Q, int T,
-                   uint32_t tmem_cols)
+                   int splits, uint32_t tmem_cols)
 {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
@@ -198,11 +215,17 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     constexpr int kStepK = step_k(kFp4);
     constexpr int kQuarters = kStepK / kQuarterK;
-    const int nsteps = static_cast<int>(K / kStepK);
+    // Split K (splits > 1): a cluster of `splits` CTAs shares one tile, CTA `rank` taking
+    // the K steps [st0, st0 + nsteps); its partial sums meet in the rank-0 CTA.
+    const int nsteps_all = static_cast<int>(K / kStepK);
+    const int rank = splits > 1 ? static_cast<int>(blockIdx.x) % splits : 0;
+    const int st0 = rank * nsteps_all / splits;
+    const int nsteps = (rank + 1) * nsteps_all / splits - st0;   // K steps of this CTA per tile
     const int tile_quarters = nsteps * kQuarters;
+    const int q0 = st0 * kQuarters;   // first 64-k quarter of K
     const int ntiles = p.tile_start[p.count];
-    const int nt = (ntiles - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) - 1) /
-                   static_cast<int>(gridDim.x);   // tiles of this CTA: blockIdx.x + gridDim.x * lt
+    const int first_tile = static_cast<int>(blockIdx.x) / splits, tile_stride = static_cast<int>(gridDim.x) / splits;
+    const int nt = (ntiles - first_tile + tile_stride - 1) / tile_stride;   // tiles first_tile + tile_stride * lt
     const int total_steps = nt * nsteps, total_quarters = total_steps * kQuarters;
     const int used = min(T, tile_quarters);   // accumulators a tile writes
 
@@ -278,10 +301,10 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
                 }
                 const int lt = g / nsteps, st = g - lt * nsteps;
                 int mi, row0;
-                locate(static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) * lt, mi, row0);
+                locate(first_tile + tile_stride * lt, mi, row0);
                 mbar_arrive_expect_tx(&w_full[s], tx);
-                tma_load_2d(codes_ring + s * kCodesBox, &p.codes[mi], st * 128, row0, &w_full[s], pol);
-                if (kFp4) tma_load_2d(scales_ring + s * kScalesBox, &p.scales[mi], st * 16, row0, &w_full[s], pol);
+                tma_load_2d(codes_ring + s * kCodesBox, &p.codes[mi], (st0 + st) * 128, row0, &w_full[s], pol);
+                if (kFp4) tma_load_2d(scales_ring + s * kScalesBox, &p.scales[mi], (st0 + st) * 16, row0, &w_full[s], pol);
                 last = g;
             }
             // every copy lands before the CTA can exit (the slot of a step within the last S
@@ -307,7 +330,7 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
             auto load_b = [&](int i) {
                 const int jb = bslot(i), kq = t + T * (i % per_tile);
                 mbar_arrive_expect_tx(&b_full[jb], L.b_bytes);
-                tma_load_2d(b_ring + jb * L.b_bytes, &p.x, kq * kQuarterK, 0, &b_full[jb], pol_x);
+                tma_load_2d(b_ring + jb * L.b_bytes, &p.x, (q0 + kq) * kQuarterK, 0, &b_full[jb], pol_x);
             };
             int loaded = 0;
             for (; loaded < rb && loaded < nmine; ++loaded) load_b(loaded);
@@ -384,7 +407,7 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
         bool ok = true, waited = false;
         for (int lt = 0; lt < nt && ok; ++lt) {
             int mi, row0;
-            locate(static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) * lt, mi, row0);
+            locate(first_tile + tile_stride * lt, mi, row0);
             for (int st = 0; st < nsteps && ok; ++st, ++g) {
                 const int s = stage_slot(g);
                 if (*abort_word || !wait_all(&w_full[s], static_cast<uint32_t>(g / S) & 1u)) {
@@ -461,6 +484,9 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
             const int64_t n = row0 + r, Nm = p.N[mi];
             const float scale = kFp4 ? p.g[mi] : (n < Nm ? __ldg(p.row_scale[mi] + n) : 0.0f);
             const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+            // split K: this CTA's partial sums go to its weight ring (idle now: every stage
+            // has been consumed) as [column][128 rows] fp32, for the rank-0 CTA to add up
+            float *part = reinterpret_cast<float *>(codes_ring);
             for (int c16 = 16 * gq; c16 < n_pad; c16 += 32) {
                 float v[16];
                 tmem_ld16(taddr + static_cast<uint32_t>(c16), v);
@@ -470,7 +496,10 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
 #pragma unroll
                     for (int i = 0; i < 16; ++i) v[i] += u[i];
                 }
-                if (n < Nm) {
+                if (splits > 1) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) part[(c16 + i) * kTileRows + r] = v[i];
+                } else if (n < Nm) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
                         if (c16 + i < M) p.y[mi][static_cast<int64_t>(c16 + i) * Nm + n] = v[i] * scale;
@@ -483,6 +512,28 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
     }
     tc_fence_before();
     __syncthreads();
+    if (splits > 1) {
+        // every CTA of the cluster has its partial sums in shared memory; the rank-0 CTA's
+        // decode threads (past the dependency wait, like every writer of y) add them up
+        // in rank order and store y; the second barrier keeps the other CTAs' shared
+        // memory alive until then
+        cluster_sync_all();
+        if (rank == 0 && warp >= kFirstDecodeWarp && warp < kFirstIssuerWarp) {
+            grid_dependency_wait();   // (done already unless this warp gave up early)
+            int mi, row0;
+            locate(first_tile, mi, row0);
+            const int64_t Nm = p.N[mi];
+            const float *part = reinterpret_cast<const float *>(codes_ring);
+            for (int idx = tid - 32 * kFirstDecodeWarp; idx < kTileRows * M; idx += 32 * kDecodeWarps) {
+                const int rr = idx % kTileRows, c = idx / kTileRows;
+                const int64_t n = row0 + rr;
+                float v = part[c * kTileRows + rr];
+                for (int k = 1; k < splits; ++k) v += ld_peer_f32(&part[c * kTileRows + rr], k);
+                if (n < Nm) p.y[mi][static_cast<int64_t>(c) * Nm + n] = v * (kFp4 ? p.g[mi] : __ldg(p.row_scale[mi] + n));
+            }
+        }
+        cluster_sync_all();
+    }
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols) : "memory");
@@ -543,7 +594,15 @@ cudaError_t plan_umma(bool fp4, const DeviceInfo &dev, int64_t tiles, int M, int
     pl.smem = umma_layout(fp4, pl.S, pl.R, pl.Q, pl.n_pad).total + 1024;
     if (pl.smem > static_cast<uint32_t>(dev.smem_optin) || K % step_k(fp4) != 0) return cudaErrorInvalidValue;
     pl.tmem_cols = kTmemCols;
-    pl.grid = static_cast<int>(std::min<int64_t>(tiles, dev.sm_count));
+    // Split K when the tiles leave half the SMs idle: clusters of up to 4 CTAs, each
+    // with a range of K steps (a CTA streams at a fixed rate, so a launch of few tiles
+    // needs more CTAs per tile to fill the device). QMV_UMMA_SPLITS overrides (1: off).
+    const int64_t nsteps = K / step_k(fp4);
+    int splits = env_int("QMV_UMMA_SPLITS", tiles * 2 <= dev.sm_count ? static_cast<int>(dev.sm_count / std::max<int64_t>(tiles, 1)) : 1);
+    splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({splits, 4, nsteps})));
+    while (splits > 1 && tiles * splits > dev.sm_count) --splits;
+    pl.splits = splits;
+    pl.grid = splits > 1 ? static_cast<int>(tiles * splits) : static_cast<int>(std::min<int64_t>(tiles, dev.sm_count));
     *out = pl;
     return cudaSuccess;
 }
@@ -586,7 +645,7 @@ cudaError_t launch_umma(const DeviceInfo &dev, const WqGroup &grp, const uint16_
     if (e != cudaSuccess) return e;
     auto kern = wq_umma_kernel<kFp4>;
     if ((e = ensure_smem_attr(reinterpret_cast<const void *>(kern), static_cast<int>(smem))) != cudaSuccess) return e;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreadsUmma);
     cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
@@ -594,13 +653,20 @@ cudaError_t launch_umma(const DeviceInfo &dev, const WqGroup &grp, const uint16_
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = set_launch_overlap_attr(attr);
+    if (pl.splits > 1) {   // the CTAs of a tile form a cluster
+        attr[cfg.numAttrs].id = cudaLaunchAttributeClusterDimension;
+        attr[cfg.numAttrs].val.clusterDim.x = static_cast<unsigned>(pl.splits);
+        attr[cfg.numAttrs].val.clusterDim.y = 1;
+        attr[cfg.numAttrs].val.clusterDim.z = 1;
+        ++cfg.numAttrs;
+    }
     if (env_int("QMV_PLAN_LOG", 0))
         std::fprintf(stderr,
-                     "umma plan: fmt=%s M=%d n_pad=%d K=%lld tiles=%d S=%d R=%d Q=%d issuers=%d grid=%u smem=%u "
-                     "tmem=%u\n",
-                     kFp4 ? "nvfp4" : "fp8", M, n_pad, static_cast<long long>(K), tiles, S, R, Q, T, cfg.gridDim.x,
-                     smem, cols);
-    return cudaLaunchKernelEx(&cfg, kern, p, M, K, n_pad, S, rb, Q, T, cols);
+                     "umma plan: fmt=%s M=%d n_pad=%d K=%lld tiles=%d S=%d R=%d Q=%d issuers=%d splits=%d grid=%u "
+                     "smem=%u tmem=%u\n",
+                     kFp4 ? "nvfp4" : "fp8", M, n_pad, static_cast<long long>(K), tiles, S, R, Q, T, pl.splits,
+                     cfg.gridDim.x, smem, cols);
+    return cudaLaunchKernelEx(&cfg, kern, p, M, K, n_pad, S, rb, Q, T, pl.splits, cols);
 }
 
 }  // namespace

@@ -296,7 +296,8 @@ QMV_API qmv_status qmv_debug_plan_q4(int q4k, int M, int64_t N, int64_t K, int n
  * fp8_tcgen05: 128-row tiles, all M rows in one pass over the weights; out[3] = its
  * MMA-issuing threads, out[4] = its weight stages, out[9] = grid, out[10] = shared
  * memory, out[11] = its 64-k A buffers in tensor memory, out[12] = its activation
- * slices; QMV_WQ_UMMA_MIN_M moves the threshold). Below it the planner scores
+ * slices, out[13] = the CTAs (a cluster) that share each tile, each a range of K;
+ * QMV_WQ_UMMA_MIN_M moves the threshold). Below it the planner scores
  * candidate plans (warps, ring slots, activations staged in shared memory or not,
  * passes over K) by the whole-tile tail they leave on the device's CTAs; the CTAs
  * per SM of a candidate come from a model here -- the least of ctas_by_regs, the SM's
@@ -312,11 +313,12 @@ QMV_API qmv_status qmv_debug_plan_q4(int q4k, int M, int64_t N, int64_t K, int n
  *                 variants allow -- 8 warps with one 8-row activation tile, 8 warps
  *                 with two, 16 warps. NULL takes the launch bounds' minimum {3, 2, 1}
  *                 (the compiler keeps the registers within them).
- *   out           HOST int64 [13]: route (a qmv_route_name index), chunks, rows of
+ *   out           HOST int64 [14]: route (a qmv_route_name index), chunks, rows of
  *                 the first chunk, warps, ring slots, staged (0/1), passes over K,
  *                 tiles per round, CTAs per SM, grid, dynamic shared memory bytes, A
- *                 buffers and activation slices (tcgen05 route; 0 otherwise). The
- *                 generic route fills only route, chunks (8-row launches) and rows.
+ *                 buffers, activation slices and K splits (tcgen05 route; 0
+ *                 otherwise). The generic route fills only route, chunks (8-row
+ *                 launches) and rows.
  * Returns QMV_ERR_NULL for out or N NULL, QMV_ERR_SHAPE for values out of range or
  * a shape no plan fits.
  */

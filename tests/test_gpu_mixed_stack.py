@@ -12,8 +12,9 @@ programmatic dependent launch on, as the benchmark runs it). Every matrix's samp
 rows (first, last, random) are compared with the oracle within
 |y - y_ref| <= 1e-3 * sum|w x| + 1e-6, and the census must show exactly one launch
 (per chunk of 16 rows) of the FP8 kernel per FP8 region and of the NVFP4 kernel per
-NVFP4 stage, and no generic kernel (from 17 rows the NVFP4 regions take the tcgen05
-kernel, from 33 the FP8 ones: one launch per stage there).
+NVFP4 stage, and no generic kernel: every stage on the kernel the planner chooses
+for it (mma.sync up to 8 rows; from 9 rows the tcgen05 kernel for matrices of few
+128-row tiles, the 5120-row ones here; from 17 rows the tcgen05 kernel everywhere).
 """
 import pytest
 import torch
@@ -45,12 +46,21 @@ def test_mixed_stack_regions_dispatch_and_match_the_oracle(q, M):
     stack.run()
     torch.cuda.synchronize()
     counts = {k: v for k, v in q.route_counts().items() if v}
-    chunks = -(-M // 16) if M > 16 else 1
     fp8_stages = sum(1 for st in stack.stages if stack.mats[st[0]][0] == "fp8")
     nvfp4_stages = len(stack.stages) - fp8_stages
     assert (fp8_stages, nvfp4_stages) == (2, 4 * LAYERS + 1 - 2)
-    want = {"nvfp4_tcgen05": nvfp4_stages} if M >= 17 else {"nvfp4_mma_m16n8k16": nvfp4_stages}
-    want.update({"fp8_tcgen05": fp8_stages} if M >= 33 else {"fp8_mma_m16n8k16": fp8_stages * chunks})
+    # the kernel of every stage as the planner chooses it (its host logic is pinned on the
+    # CPU): launches per stage = its chunks of <= 16 rows on the mma.sync route, 1 otherwise
+    want = {}
+    for st in stack.stages:
+        fmt, _, K = stack.mats[st[0]]
+        plan = q.qmv_debug_plan_wq(M, K, [stack.mats[i][1] for i in st], fp4=fmt == "nvfp4")
+        want[plan["route"]] = want.get(plan["route"], 0) + plan["chunks"]
+    assert sum(want.values()) >= len(stack.stages)
+    if M >= 17:
+        assert set(want) == {"nvfp4_tcgen05", "fp8_tcgen05"}
+    if M <= 8:
+        assert set(want) == {"nvfp4_mma_m16n8k16", "fp8_mma_m16n8k16"}
     assert counts == want, counts
     assert not any(k.endswith("generic") for k in counts)
     par = bench.sampled_parity(stack, rows=8)

@@ -26,6 +26,14 @@ def q():
     return q
 
 
+@pytest.fixture(autouse=True)
+def mma_below_17_rows(monkeypatch):
+    """These tests are about the mma.sync kernel: launches of few tiles keep it up to 16
+    rows (by default they take the tcgen05 kernel from 9 rows; see
+    test_default_dispatch below)."""
+    monkeypatch.setenv("QMV_WQ_UMMA_FEW_TILES_MIN_M", "17")
+
+
 def _synth():
     from gemm_qmv_quantize_gb300 import synth
     return synth
@@ -333,22 +341,26 @@ def test_chunked_group_and_generic(q, M, chunked):
     assert q.route_counts()["nvfp4_generic"] == (M + 7) // 8 and q.route_counts()["fp8_generic"] == (M + 7) // 8
 
 
-@pytest.mark.parametrize("M", [16, 17, 32, 33, 96])
-def test_default_dispatch_above_16_rows(q, M):
-    """Default routes: NVFP4 on the tcgen05 kernel from 17 rows, FP8 from 33 (one launch,
-    one weight pass); below that one mma.sync pass up to 16 rows, chunks above."""
-    N = 128 * 2 + 45
+@pytest.mark.parametrize("M", [8, 9, 16, 17, 32, 96])
+@pytest.mark.parametrize("N", [128 * 2 + 45, 128 * 60 + 7])
+def test_default_dispatch(q, monkeypatch, M, N):
+    """Default routes: one mma.sync pass up to 8 rows; from 9 rows the tcgen05 kernel
+    (one launch, one weight pass, K split over a cluster) when the launch has at most a
+    third of the SMs' worth of 128-row tiles (3 tiles here); otherwise (61 tiles) mma.sync
+    up to 16 rows and the tcgen05 kernel from 17, for NVFP4 and FP8 alike."""
+    monkeypatch.delenv("QMV_WQ_UMMA_FEW_TILES_MIN_M", raising=False)
+    few = (N + 127) // 128 * 3 <= 152
+    umma = M >= 17 or (few and M >= 9)
+    rows = np.arange(N) if N < 1000 else _synth().sample_rows(N, 48, seed=N + M).numpy()
     q.route_reset()
-    _nvfp4(q, M, N, 5120, seed=3100 + M)
-    _fp8(q, M, N, 5120, seed=3200 + M)
+    _nvfp4(q, M, N, 5120, seed=3100 + M, rows=rows)
+    _fp8(q, M, N, 5120, seed=3200 + M, rows=rows)
     c = {k: v for k, v in q.route_counts().items() if v}
-    want = {}
-    want["nvfp4_tcgen05" if M >= 17 else "nvfp4_mma_m16n8k16"] = 1
-    if M >= 33:
-        want["fp8_tcgen05"] = 1
-    else:
-        want["fp8_mma_m16n8k16"] = (M + 15) // 16
+    want = {"nvfp4_tcgen05": 1, "fp8_tcgen05": 1} if umma else {"nvfp4_mma_m16n8k16": 1, "fp8_mma_m16n8k16": 1}
     assert c == want, c
+    for fp4 in (True, False):
+        assert q.qmv_debug_plan_wq(M, 5120, [N], fp4=fp4)["route"] == ("nvfp4" if fp4 else "fp8") + (
+            "_tcgen05" if umma else "_mma_m16n8k16")
 
 
 # ------------------------------------------------ largest K and M

@@ -8,7 +8,9 @@ Every fp32 output within |y - y_ref| <= 1e-3 * sum|w*x| + 1e-6 on: tiles with a
 ragged tail (N not a multiple of 128) at M = 1..96 including every padding boundary,
 K from one step to 17408, fp16 outliers up to 6e4, zero scales, the closed form of
 unit codes, groups with ragged row counts, and sampled rows of the 27B-class shapes
-and the 151936-row lm_head. The route census must show the tcgen05 route only.
+and the 151936-row lm_head; split K (clusters of 2..4 CTAs per tile, partial sums
+added in the rank-0 CTA) forced on and off on the same inputs. The route census must
+show the tcgen05 route only.
 """
 import numpy as np
 import pytest
@@ -183,3 +185,24 @@ def test_chain_with_launch_overlap(q):
             assert_close(f"chain[{i}]", ys[i].cpu().numpy()[:, rows], y_ref, bound)
     finally:
         q.set_launch_overlap(before)
+
+
+@pytest.mark.parametrize("fp4", [True, False])
+@pytest.mark.parametrize("splits", [1, 2, 3, 4])
+def test_split_k_forced(q, monkeypatch, fp4, splits):
+    """The same call with the K range split over 1..4 CTAs of a cluster: every split
+    count within the bound against the oracle, on a ragged tile count and a K whose
+    steps do not divide evenly between the CTAs (K = 5120: 20 NVFP4 / 40 FP8 steps)."""
+    monkeypatch.setenv("QMV_UMMA_SPLITS", str(splits))
+    M, N, K = 33, 1000, 5120
+    assert q.qmv_debug_plan_wq(M, K, [N], fp4=fp4)["k_splits"] == splits
+    (_nvfp4 if fp4 else _fp8)(q, M, N, K, seed=700 + splits + (0 if fp4 else 50))
+
+
+def test_split_k_default_on_few_tiles(q):
+    """With few tiles the default plan splits K (40 tiles of the 5120-row matrices: 3
+    CTAs each) and the result stays within the bound on sampled rows of every tile."""
+    M, N, K = 32, 5120, 17408
+    assert q.qmv_debug_plan_wq(M, K, [N], fp4=True)["k_splits"] == 3
+    rows = np.unique(np.concatenate([np.arange(0, N, 128), np.arange(127, N, 128)]))
+    _nvfp4(q, M, N, K, seed=4242, rows=rows)

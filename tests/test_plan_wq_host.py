@@ -6,8 +6,9 @@ of the device, so no GPU is needed.
 - Choices the design notes measured and kept: three 8-warp CTAs per SM at M = 1
   (the 5120 x 17408 down projection and the lm_head), 16 warps sharing one staged
   copy of the activations at M = 8 with K = 5120, two 8-row activation tiles in one
-  weight pass at M = 9..16, then one pass on the tcgen05 kernel (NVFP4 from 17 rows,
-  FP8 from 33) or balanced chunks of <= 16 rows ("v100-skinny README", "Native
+  weight pass at M = 9..16, then one pass on the tcgen05 kernel (from 17 rows; from 9
+  for launches of at most a third of the SMs' worth of tiles) or balanced chunks of
+  <= 16 rows ("v100-skinny README", "Native
   mixed-precision checkpoint path": the qpn8 / qpn8-mt2 / qpn8-chunked routes), the
   generic kernel for unaligned data or K off the step.
 - Invariants over a sweep of shapes, M and register limits: shared memory within the
@@ -23,7 +24,7 @@ from gemm_qmv_quantize_gb300._binding import GB300_DEVICE, QmvError, qmv_debug_p
 
 MMA = {True: "nvfp4_mma_m16n8k16", False: "fp8_mma_m16n8k16"}
 UMMA = {True: "nvfp4_tcgen05", False: "fp8_tcgen05"}
-UMMA_MIN_M = {True: 17, False: 33}
+UMMA_MIN_M = {True: 17, False: 17}   # launches of many tiles (17408 rows: 136)
 GENERIC = {True: "nvfp4_generic", False: "fp8_generic"}
 SHAPES_27B = [(7168, 5120), (5120, 5120), (17408, 5120), (5120, 17408), (151936, 5120)]
 
@@ -65,7 +66,7 @@ def test_chunked_band(M, monkeypatch):
 @pytest.mark.parametrize("fp4", [True, False])
 @pytest.mark.parametrize("M", [16, 17, 24, 32, 33, 48, 64, 80, 96])
 def test_tcgen05_band(fp4, M):
-    """From 17 rows (NVFP4) / 33 (FP8) one pass on the tcgen05 kernel: 128-row tiles; T
+    """From 17 rows one pass on the tcgen05 kernel: 128-row tiles; T
     issuing threads with an accumulator of 16 ceil(M / 16) columns each and Q >= max(T, 2)
     64-k A buffers of 32 columns (an even count: two decode groups take alternate
     buffers), all within the 512 columns of tensor memory (the A
@@ -125,7 +126,8 @@ def test_invariants_over_a_sweep(fp4, regs):
         for M in (1, 2, 3, 5, 8, 9, 12, 16, 17, 40, 96):
             p = plan(M, K, N, fp4=fp4, ctas_by_regs=regs)
             rows = p["chunk_rows"]
-            if M >= UMMA_MIN_M[fp4]:
+            few = math.ceil(N / 128) * 3 <= dev["sm_count"]
+            if M >= UMMA_MIN_M[fp4] or (few and M >= 9):
                 assert p["route"] == UMMA[fp4] and rows == M
                 continue
             assert p["route"] == MMA[fp4]
@@ -146,3 +148,49 @@ def test_invariants_over_a_sweep(fp4, regs):
                 assert rows * (2 * K // p["passes"] + 16) <= 200 * 1024
             else:
                 assert p["passes"] == 1
+
+
+@pytest.mark.parametrize("fp4,N,K,want", [
+    (True, 17408, 5120, 1), (False, 17408, 5120, 1),   # 136 tiles: no split
+    (True, 7168, 5120, 2), (False, 7168, 5120, 2),     # 56 tiles: 152 // 56
+    (True, 5120, 5120, 3), (False, 5120, 17408, 3),    # 40 tiles: 152 // 40
+    (True, 2048, 4096, 4), (False, 2048, 4096, 4),     # 16 tiles: capped at 4
+    (True, 151936, 5120, 1),                           # lm_head: persistent grid
+    (True, 128, 256, 1), (False, 128, 256, 2),         # one tile: capped by the K steps (1 / 2)
+    (True, 256, 768, 3), (False, 256, 384, 3)])
+def test_tcgen05_split_k(fp4, N, K, want):
+    """Split K when the tiles leave half the SMs idle: floor(152 / tiles) CTAs per tile,
+    at most 4 and at most the K steps (NVFP4 steps of 256 k, FP8 of 128 k); the grid
+    is tiles x splits, never more than the SMs."""
+    tiles = math.ceil(N / 128)
+    p = plan(96, K, N, fp4=fp4)
+    assert p["k_splits"] == want
+    assert p["grid"] == (tiles * want if want > 1 else min(tiles, GB300_DEVICE["sm_count"]))
+    assert p["grid"] <= GB300_DEVICE["sm_count"]
+
+
+@pytest.mark.parametrize("fp4", [True, False])
+@pytest.mark.parametrize("N,few", [(301, True), (5120, True), (128 * 50, True), (128 * 51, False),
+                                   (7168, False), (17408, False)])
+@pytest.mark.parametrize("M", [8, 9, 16, 17])
+def test_tcgen05_few_tiles_band(fp4, N, few, M):
+    """From 9 rows the tcgen05 kernel takes launches of at most a third of the SMs' worth
+    of 128-row tiles (50 of 152: K split over 3+ CTAs of a cluster), from 17 rows every
+    launch; below that the mma.sync kernel in one pass."""
+    p = plan(M, 5120, N, fp4=fp4)
+    umma = M >= 17 or (few and M >= 9)
+    assert p["route"] == (UMMA if umma else MMA)[fp4]
+    if umma and few:
+        assert p["k_splits"] >= 3
+
+
+def test_tcgen05_thresholds_follow_the_environment(monkeypatch):
+    """QMV_WQ_UMMA_MIN_M = 0 keeps the tcgen05 kernel off everywhere; 1 takes it for every
+    M; QMV_WQ_UMMA_FEW_TILES_MIN_M moves the few-tile threshold alone."""
+    monkeypatch.setenv("QMV_WQ_UMMA_MIN_M", "0")
+    assert plan(16, 5120, 5120)["route"] == MMA[True] and plan(96, 5120, 301)["route"] == MMA[True]
+    monkeypatch.setenv("QMV_WQ_UMMA_MIN_M", "1")
+    assert plan(1, 5120, 17408)["route"] == UMMA[True] and plan(1, 5120, 301)["route"] == UMMA[True]
+    monkeypatch.delenv("QMV_WQ_UMMA_MIN_M")
+    monkeypatch.setenv("QMV_WQ_UMMA_FEW_TILES_MIN_M", "17")
+    assert plan(16, 5120, 5120)["route"] == MMA[True] and plan(17, 5120, 5120)["route"] == UMMA[True]
