@@ -184,11 +184,13 @@ QMV_API qmv_status qmv_q4_k_q8_1_fused_group(int count, const void *const *w, co
  *   M = 1..16: rows 9..16 ride the same pass over the weights as rows 1..8 (a
  *   second 8-row activation tile of the tensor-core product), so the weights are
  *   read from memory once for all M rows. M = 17..96 (the chunked band of the
- *   README's "Native mixed-precision checkpoint path" dispatch table): one pass over
- *   the weights on the 5th-generation tensor cores (tcgen05.mma, fp32 accumulators in
- *   tensor memory, M padded to a multiple of 16), x 16-byte aligned and scales_e4m3
- *   16-byte aligned; otherwise balanced chunks of at most 16 rows, one launch and one
- *   weight pass each.
+ *   README's "Native mixed-precision checkpoint path" dispatch table), and M = 9..16
+ *   when N spans at most a third of the SMs' worth of 128-row tiles: one pass over
+ *   the weights on the 5th-generation tensor cores (tcgen05.mma, weights decoded into
+ *   and fp32 accumulators kept in tensor memory, M padded to a multiple of 16, K split
+ *   over a thread-block cluster when the tiles leave half the SMs idle), x 16-byte
+ *   aligned and scales_e4m3 16-byte aligned; otherwise balanced chunks of at most 16
+ *   rows, one launch and one weight pass each.
  */
 QMV_API qmv_status qgemm_nvfp4_w4a16(const uint8_t *codes, const uint8_t *scales_e4m3, float global_scale,
                              const uint16_t *x, float *y, int M, int64_t N, int64_t K,
@@ -203,9 +205,9 @@ QMV_API qmv_status qgemm_nvfp4_w4a16(const uint8_t *codes, const uint8_t *scales
  *   y          fp32 [M][N]: y[m][n] = row_scale[n] * sum_k e4m3(w[n][k]) * x[m][k],
  *              accumulated in fp32.
  *   Any K >= 0. w, x 16-byte aligned and K a multiple of 128 select the
- *   tensor-core streaming kernel. M = 1..16 in one pass over the weights, 17..32 in
- *   chunks of at most 16 rows, 33..96 in one pass on the tcgen05 kernel (as NVFP4
- *   from 17 rows).
+ *   tensor-core streaming kernel. The same bands as qgemm_nvfp4_w4a16: M = 1..16 in
+ *   one pass over the weights, then (from 9 rows for launches of few tiles) one pass
+ *   on the tcgen05 kernel, or chunks of at most 16 rows when it cannot be used.
  */
 QMV_API qmv_status qgemm_fp8_w8a16(const uint8_t *w, const float *row_scale, const uint16_t *x, float *y,
                            int M, int64_t N, int64_t K, qmv_stream_t stream);
@@ -292,12 +294,13 @@ QMV_API qmv_status qmv_debug_plan_q4(int q4k, int M, int64_t N, int64_t K, int n
  * The launch plan the NVFP4 / FP8 heuristic picks for one call (count = 1) or one
  * grouped launch (count 1..8 matrices of N[i] rows, the same M and K) on a device
  * given by its limits, with no CUDA call (usable without a GPU). From 17 activation
- * rows (NVFP4) or 33 (FP8) on, the tcgen05 kernel takes the call (route nvfp4_tcgen05 /
+ * rows on (from 9 when the tiles span at most a third of the SMs), the tcgen05 kernel
+ * takes the call (route nvfp4_tcgen05 /
  * fp8_tcgen05: 128-row tiles, all M rows in one pass over the weights; out[3] = its
  * MMA-issuing threads, out[4] = its weight stages, out[9] = grid, out[10] = shared
  * memory, out[11] = its 64-k A buffers in tensor memory, out[12] = its activation
  * slices, out[13] = the CTAs (a cluster) that share each tile, each a range of K;
- * QMV_WQ_UMMA_MIN_M moves the threshold). Below it the planner scores
+ * QMV_WQ_UMMA_MIN_M / QMV_WQ_UMMA_FEW_TILES_MIN_M move the thresholds). Below it the planner scores
  * candidate plans (warps, ring slots, activations staged in shared memory or not,
  * passes over K) by the whole-tile tail they leave on the device's CTAs; the CTAs
  * per SM of a candidate come from a model here -- the least of ctas_by_regs, the SM's
