@@ -52,10 +52,13 @@ constexpr int kScalesBox = kTileRows * 16;   // NVFP4: 128 rows x 16 E4M3 scales
 constexpr int kACols = kQuarterK / 2;  // TMEM columns of one 64-k A buffer (fp16 pairs)
 constexpr int kTmemCols = 512;         // the whole of tensor memory: accumulators and A buffers
 constexpr int kWeightProducers = 3;    // warps 0, 1, 2: one thread each streams every third K step
-constexpr int kDecodeWarps = 8;        // two groups of four (one warp per TMEM lane quarter)
-constexpr int kDecodeGroups = 2;       // the groups take alternate 64-k quarters
-constexpr int kFirstDecodeWarp = 3;    // warps 0..2 weight producers (warp 1 also allocates TMEM), 3..10 decode
-constexpr int kMaxIssuers = 8;         // warps 11 .. 11 + T - 1: one MMA-issuing thread each
+#ifndef QMV_UMMA_DECODE_GROUPS
+#define QMV_UMMA_DECODE_GROUPS 3
+#endif
+constexpr int kDecodeGroups = QMV_UMMA_DECODE_GROUPS;   // groups of four warps (one per TMEM lane
+constexpr int kDecodeWarps = 4 * kDecodeGroups;         // quarter), quarter h to group h % groups
+constexpr int kFirstDecodeWarp = 3;    // warps 0..2 weight producers (warp 1 also allocates TMEM), then decode
+constexpr int kMaxIssuers = 16 - kDecodeWarps;   // the warps after the decode warps: one MMA-issuing thread each
 constexpr int kFirstIssuerWarp = kFirstDecodeWarp + kDecodeWarps;
 constexpr int kThreadsUmma = 32 * (kFirstIssuerWarp + kMaxIssuers);
 constexpr int kMaxStages = 12;         // weight stages (one K step of codes and scales each), a multiple of 3
@@ -390,12 +393,12 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
         __syncwarp();
     } else if (warp >= kFirstDecodeWarp) {
         // ------------------------------------------------ decode, then read back
-        // Two groups of four warps take alternate 64-k quarters (group gq the quarters
-        // h with h % 2 == gq; K steps hold an even number of quarters). In a group, warp
-        // w decodes the rows of its TMEM lane quarter 32 (w % 4) .. + 31, one row per
-        // thread, all 64 k of the quarter: 32 TMEM columns of fp16 pairs. Waits are made
-        // warp-uniform, since the tensor-memory accesses that follow them are
-        // .sync.aligned.
+        // Groups of four warps take turns on the 64-k quarters (group gq the quarters h
+        // with h % groups == gq; every decode warp takes and releases every K step). In
+        // a group, warp w decodes the rows of its TMEM lane quarter 32 (w % 4) .. + 31,
+        // one row per thread, all 64 k of the quarter: 32 TMEM columns of fp16 pairs.
+        // Waits are made warp-uniform, since the tensor-memory accesses that follow them
+        // are .sync.aligned.
         const int r = 32 * (warp & 3) + lane;
         const int gq = (warp - kFirstDecodeWarp) >> 2;
         const uint32_t a_lane = tmem + (static_cast<uint32_t>(32 * (warp & 3)) << 16) + a_col0;
@@ -416,8 +419,9 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
                     break;
                 }
                 const uint8_t *crow = codes_ring + s * kCodesBox + r * 128;
-                for (int q = gq; q < kQuarters; q += kDecodeGroups) {
+                for (int q = 0; q < kQuarters; ++q) {
                     const int hq = h + q, j = hq % Q;
+                    if (hq % kDecodeGroups != gq) continue;
                     if (hq >= Q && !wait_all(&a_free[j], static_cast<uint32_t>((hq / Q) - 1) & 1u)) {
                         fail();
                         ok = false;
@@ -466,7 +470,13 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
                     if (lane == 0) mbar_arrive(&a_full[j]);
                 }
                 h += kQuarters;
-                if (ok && lane == 0) mbar_arrive(&w_free[s]);   // (the warp's reads fenced above)
+                if (ok) {
+                    // the warp's generic reads of the slot before the next copy's
+                    // async-proxy writes into it
+                    fence_proxy_async_shared();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&w_free[s]);
+                }
             }
             if (!ok) break;
             // read back tile lt: row row0 + r of matrix mi, activation rows in 16-column
@@ -487,7 +497,7 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
             // split K: this CTA's partial sums go to its weight ring (idle now: every stage
             // has been consumed) as [column][128 rows] fp32, for the rank-0 CTA to add up
             float *part = reinterpret_cast<float *>(codes_ring);
-            for (int c16 = 16 * gq; c16 < n_pad; c16 += 32) {
+            for (int c16 = 16 * gq; c16 < n_pad; c16 += 16 * kDecodeGroups) {
                 float v[16];
                 tmem_ld16(taddr + static_cast<uint32_t>(c16), v);
                 for (int a = 1; a < used; ++a) {
@@ -560,8 +570,8 @@ cudaError_t plan_umma(bool fp4, const DeviceInfo &dev, int64_t tiles, int M, int
     // Tensor memory (512 columns) holds T accumulators of n_pad columns, one per
     // MMA-issuing thread, and Q 64-k A buffers of 32 columns. T is as large as leaves
     // room for max(T, 6) A buffers (the decode runs up to Q quarters ahead of the
-    // products). Q is even and >= T: the two decode groups take alternate quarters, so
-    // each A buffer is written by one group only, and thread t (quarters t, t + T, ...)
+    // products). Q is a multiple of the decode groups and >= T: the groups take turns
+    // on the quarters, so each A buffer is written by one group only, and thread t (quarters t, t + T, ...)
     // reaches a buffer's next phase only after the phase it waited for before (with
     // fewer buffers than threads it could meet a buffer two phases behind and pass its
     // parity test on the phase before). Each issuing thread streams its activation
@@ -573,12 +583,13 @@ cudaError_t plan_umma(bool fp4, const DeviceInfo &dev, int64_t tiles, int M, int
     auto q_room = [&](int t_) {
         return (kTmemCols - static_cast<int>(a_first_col(t_, pl.n_pad))) / kACols;
     };
-    auto even_up = [](int v) { return (v + 1) & ~1; };
+    auto g_up = [](int v) { return (v + kDecodeGroups - 1) / kDecodeGroups * kDecodeGroups; };
+    auto g_down = [](int v) { return v / kDecodeGroups * kDecodeGroups; };
     int T = t_cap;
-    while (T > 1 && (q_room(T) & ~1) < std::max(even_up(T), 6)) --T;
-    if ((q_room(T) & ~1) < std::max(even_up(T), 2)) return cudaErrorInvalidValue;
-    const int Q = std::max(std::max(2, even_up(T)),
-                           std::min({kMaxABufs, q_room(T), env_int("QMV_UMMA_ABUFS", kMaxABufs)}) & ~1);
+    while (T > 1 && g_down(q_room(T)) < std::max(g_up(T), 6)) --T;
+    if (g_down(q_room(T)) < std::max(g_up(T), 2)) return cudaErrorInvalidValue;
+    const int Q = std::max(std::max(g_up(2), g_up(T)),
+                           g_down(std::min({kMaxABufs, q_room(T), env_int("QMV_UMMA_ABUFS", kMaxABufs)})));
     int rb = std::max(2, std::min(kMaxSlicesPerIssuer, env_int("QMV_UMMA_BBUFS", (12 + T - 1) / T)));
     auto fits = [&](int s_, int rb_) {
         return umma_layout(fp4, s_, T * rb_, Q, pl.n_pad).total + 1024 <= static_cast<uint32_t>(dev.smem_optin);
