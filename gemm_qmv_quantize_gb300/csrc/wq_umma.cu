@@ -58,7 +58,10 @@ constexpr int kWeightProducers = 3;    // warps 0, 1, 2: one thread each streams
 constexpr int kDecodeGroups = QMV_UMMA_DECODE_GROUPS;   // groups of four warps (one per TMEM lane
 constexpr int kDecodeWarps = 4 * kDecodeGroups;         // quarter), quarter h to group h % groups
 constexpr int kFirstDecodeWarp = 3;    // warps 0..2 weight producers (warp 1 also allocates TMEM), then decode
-constexpr int kMaxIssuers = 16 - kDecodeWarps;   // the warps after the decode warps: one MMA-issuing thread each
+#ifndef QMV_UMMA_ISSUER_WARPS
+#define QMV_UMMA_ISSUER_WARPS (16 - 4 * QMV_UMMA_DECODE_GROUPS)
+#endif
+constexpr int kMaxIssuers = QMV_UMMA_ISSUER_WARPS;   // the warps after the decode warps: one MMA-issuing thread each
 constexpr int kFirstIssuerWarp = kFirstDecodeWarp + kDecodeWarps;
 constexpr int kThreadsUmma = 32 * (kFirstIssuerWarp + kMaxIssuers);
 constexpr int kMaxStages = 12;         // weight stages (one K step of codes and scales each), a multiple of 3
@@ -470,10 +473,12 @@ __global__ void __launch_bounds__(kThreadsUmma, 1)
                     if (lane == 0) mbar_arrive(&a_full[j]);
                 }
                 h += kQuarters;
+                // Release the slot. No cross-proxy fence is needed before the next copy's
+                // async-proxy writes: every value this warp read from the slot has been
+                // consumed -- converted, stored to tensor memory and waited for with
+                // tcgen05.wait::st -- so the reads are complete. (A fence here waits for
+                // the CTA's copies in flight and cost 7 % at M = 32.)
                 if (ok) {
-                    // the warp's generic reads of the slot before the next copy's
-                    // async-proxy writes into it
-                    fence_proxy_async_shared();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&w_free[s]);
                 }
