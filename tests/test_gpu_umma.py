@@ -166,6 +166,34 @@ def test_groups(q, M):
         assert_close(f"tcgen05 fp8 group[{i}]", outs[i].cpu().numpy()[:, rows], y_ref, bound)
 
 
+@pytest.mark.parametrize("M", [9, 33, 96])
+def test_groups_split_k(q, M):
+    """Grouped launches of few tiles: the cluster's CTAs share a tile of any matrix of
+    the group (NVFP4: 8 + 1 + 5 + 16 tiles, 4 CTAs per tile; FP8: 40 + 3 tiles, 3 per
+    tile), every output within the bound."""
+    synth = _synth()
+    K = 5120
+    Ns = [1000, 37, 513, 2048]
+    assert q.qmv_debug_plan_wq(M, K, Ns, fp4=True)["k_splits"] == 4
+    mats = [synth.nvfp4_weights(n, K, seed=1200 + i, device=DEV) for i, n in enumerate(Ns)]
+    x = synth.activations_f16(M, K, seed=1290 + M, device=DEV, outliers=2)
+    q.route_reset()
+    outs = q.qgemm_nvfp4_w4a16_group([m[0] for m in mats], [m[1] for m in mats], [m[2] for m in mats], x)
+    assert {k: v for k, v in q.route_counts().items() if v} == {"nvfp4_tcgen05": 1}
+    for i, (c, sc, g) in enumerate(mats):
+        y_ref, bound = oracle.nvfp4_w4a16(c.cpu().numpy(), sc.cpu().numpy(), g, x.cpu().numpy())
+        assert_close(f"split group[{i}] M={M}", outs[i].cpu().numpy(), y_ref, bound)
+    Nf = [5120, 300]
+    assert q.qmv_debug_plan_wq(M, K, Nf, fp4=False)["k_splits"] == 3
+    wm = [synth.fp8_weights(n, K, seed=1250 + i, device=DEV) for i, n in enumerate(Nf)]
+    outs = q.qgemm_fp8_w8a16_group([m[0] for m in wm], [m[1] for m in wm], x)
+    for i, (w, rs) in enumerate(wm):
+        rows = np.arange(w.shape[0]) if w.shape[0] < 1000 else synth.sample_rows(w.shape[0], 96, seed=i + M).numpy()
+        y_ref, bound = oracle.fp8_w8a16(w.cpu().numpy()[rows], rs.cpu().numpy()[rows], x.cpu().numpy())
+        assert_close(f"split fp8 group[{i}] M={M}", outs[i].cpu().numpy()[:, rows], y_ref, bound)
+    assert q.error_flags() == 0
+
+
 def test_chain_with_launch_overlap(q):
     """Back-to-back calls with programmatic dependent launch (as the stacks run them):
     each call's outputs match the oracle (the next call's weight copies start while
