@@ -33,6 +33,7 @@
 //    barrier, the producer lets its copies land, the MMA thread waits for its
 //    products to complete and the tensor memory is released before the CTA exits.
 #include <algorithm>
+#include <numeric>
 #include <cstdio>
 
 #include <cuda.h>
@@ -573,28 +574,32 @@ cudaError_t plan_umma(bool fp4, const DeviceInfo &dev, int64_t tiles, int M, int
     UmmaPlan pl;
     pl.n_pad = 16 * ((M + 15) / 16);
     // Tensor memory (512 columns) holds T accumulators of n_pad columns, one per
-    // MMA-issuing thread, and Q 64-k A buffers of 32 columns. T is as large as leaves
-    // room for max(T, 6) A buffers (the decode runs up to Q quarters ahead of the
-    // products). Q is a multiple of the decode groups and >= T: the groups take turns
-    // on the quarters, so each A buffer is written by one group only, and thread t (quarters t, t + T, ...)
-    // reaches a buffer's next phase only after the phase it waited for before (with
-    // fewer buffers than threads it could meet a buffer two phases behind and pass its
-    // parity test on the phase before). Each issuing thread streams its activation
-    // slices through rb slots: enough for about 12 quarters of the CTA in flight. Shared
-    // memory then takes as many weight stages as fit, a multiple of the 3 producers,
-    // 3 .. 12. QMV_UMMA_ISSUERS / QMV_UMMA_ABUFS / QMV_UMMA_STAGES cap T, Q and S;
-    // QMV_UMMA_BBUFS sets rb.
+    // MMA-issuing thread, and Q 64-k A buffers of 32 columns. Q is a multiple of the
+    // decode groups (each A buffer is then written by one group only) and of T: thread
+    // t takes quarters t, t + T, ..., so the quarter that last used buffer h % Q,
+    // h - Q, is one of its own earlier quarters, whose phase it has waited for. Any
+    // other Q lets a thread meet a buffer two phases behind -- the decode groups drift
+    // against each other -- and pass its parity test on the phase before (seen as
+    // timeouts with 7 threads and 9 buffers). T is as large as allows such a Q of at
+    // least 6 (the decode runs up to Q quarters ahead of the products). Each issuing
+    // thread streams its activation slices through rb slots: enough for about 12
+    // quarters of the CTA in flight. Shared memory then takes as many weight stages as
+    // fit, a multiple of the 3 producers, 3 .. 12. QMV_UMMA_ISSUERS / QMV_UMMA_ABUFS /
+    // QMV_UMMA_STAGES cap T, Q and S; QMV_UMMA_BBUFS sets rb.
     const int t_cap = std::max(1, std::min(kMaxIssuers, env_int("QMV_UMMA_ISSUERS", kMaxIssuers)));
+    const int q_cap = std::min(kMaxABufs, env_int("QMV_UMMA_ABUFS", kMaxABufs));
     auto q_room = [&](int t_) {
         return (kTmemCols - static_cast<int>(a_first_col(t_, pl.n_pad))) / kACols;
     };
-    auto g_up = [](int v) { return (v + kDecodeGroups - 1) / kDecodeGroups * kDecodeGroups; };
-    auto g_down = [](int v) { return v / kDecodeGroups * kDecodeGroups; };
+    // the largest multiple of lcm(groups, t) that fits, or 0
+    auto q_for = [&](int t_, int cap) {
+        const int l = kDecodeGroups / std::gcd(kDecodeGroups, t_) * t_;
+        return std::min(cap, q_room(t_)) / l * l;
+    };
     int T = t_cap;
-    while (T > 1 && g_down(q_room(T)) < std::max(g_up(T), 6)) --T;
-    if (g_down(q_room(T)) < std::max(g_up(T), 2)) return cudaErrorInvalidValue;
-    const int Q = std::max(std::max(g_up(2), g_up(T)),
-                           g_down(std::min({kMaxABufs, q_room(T), env_int("QMV_UMMA_ABUFS", kMaxABufs)})));
+    while (T > 1 && q_for(T, kMaxABufs) < 6) --T;
+    if (q_for(T, kMaxABufs) == 0) return cudaErrorInvalidValue;
+    const int Q = std::max(q_for(T, q_cap), kDecodeGroups / std::gcd(kDecodeGroups, T) * T);
     int rb = std::max(2, std::min(kMaxSlicesPerIssuer, env_int("QMV_UMMA_BBUFS", (12 + T - 1) / T)));
     auto fits = [&](int s_, int rb_) {
         return umma_layout(fp4, s_, T * rb_, Q, pl.n_pad).total + 1024 <= static_cast<uint32_t>(dev.smem_optin);

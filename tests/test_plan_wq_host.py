@@ -68,8 +68,9 @@ def test_chunked_band(M, monkeypatch):
 def test_tcgen05_band(fp4, M):
     """From 17 rows one pass on the tcgen05 kernel: 128-row tiles; T
     issuing threads with an accumulator of 16 ceil(M / 16) columns each and Q >= max(T, 2)
-    64-k A buffers of 32 columns (a multiple of 3: three decode groups take turns on
-    the buffers), all within the 512 columns of tensor memory (the A
+    64-k A buffers of 32 columns (a multiple of 3 and of T: three decode groups take
+    turns on the buffers, and thread t's buffers were last used by its own quarters),
+    all within the 512 columns of tensor memory (the A
     buffers from the first 32-aligned column after the accumulators); R >= T activation
     slices; at least 3 weight stages; shared memory within the device's limit."""
     N, K = 17408, 5120
@@ -80,7 +81,9 @@ def test_tcgen05_band(fp4, M):
     n_pad = 16 * math.ceil(M / 16)
     assert (p["route"], p["chunks"], p["chunk_rows"]) == (UMMA[fp4], 1, M)
     T, Q, R = p["warps"], p["a_bufs"], p["b_bufs"]
-    assert 1 <= T <= 8 and Q >= max(T, 2) and Q % 3 == 0 and R >= max(T, 2)
+    # Q a multiple of the 3 decode groups and of T: the buffer an issuing thread waits
+    # on was last used by one of its own earlier quarters
+    assert 1 <= T <= 8 and Q >= max(T, 2) and Q % (3 // math.gcd(3, T) * T) == 0 and R >= max(T, 2)
     assert 32 * math.ceil(T * n_pad / 32) + 32 * Q <= 512
     assert Q >= min(6, (512 - 32 * math.ceil(T * n_pad / 32)) // 32)   # room for the decode to run ahead
     assert 3 <= p["slots"] <= 12 and p["smem_bytes"] <= GB300_DEVICE["smem_optin"]
