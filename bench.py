@@ -554,11 +554,12 @@ def run_ours(args, rank, world, local_rank):
 
 
 def secondary_workloads(args):
-    """Workloads timed after the main one in the same run: by default the 27B-class
-    NVFP4 stack at M = 1 beside the default Q4_0 stack (the two M = 1 paths whose
-    HBM fraction is the target), none beside any other workload."""
+    """Workloads timed after the main one in the same run: by default, beside the
+    default Q4_0 stack, the 27B-class NVFP4 stack at M = 1 (the other M = 1 path whose
+    HBM fraction is the target) and the mixed NVFP4/FP8 27B stack at M = 32 (the
+    verification band on the tcgen05 kernel); none beside any other workload."""
     if args.secondary == "auto":
-        return ["nvfp4_27b_m1"] if args.workload == DEFAULT_WORKLOAD else []
+        return ["nvfp4_27b_m1", "mixed_27b_m32"] if args.workload == DEFAULT_WORKLOAD else []
     return [w for w in args.secondary.split(",") if w and w != "none"]
 
 
@@ -967,7 +968,8 @@ def parse_args(argv=None):
                    help="skip the cpu_baseline leg (the oracle's timing and the sampled parity check)")
     p.add_argument("--secondary", default="auto",
                    help="comma-separated workloads timed after the main one in the same run ('none': no "
-                        "secondary record; auto: the NVFP4 27B stack at M = 1 beside the default workload)")
+                        "secondary record; auto: the NVFP4 27B stack at M = 1 and the mixed 27B stack at "
+                        "M = 32 beside the default workload)")
     return p.parse_args(argv)
 
 

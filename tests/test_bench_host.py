@@ -157,3 +157,15 @@ def test_algorithmic_bytes_match_the_closed_forms():
     mats = bench.llama2_7b_stack()
     assert sum(4 * n for _, n, _ in mats) == 5_567_488                         # outputs of one token
     assert sum((k // 32) * 36 for _, _, k in mats) == 1_285_632                # one Q8_1 row per matmul
+
+
+def test_secondary_records_beside_the_default_workload():
+    """The default line also times the 27B NVFP4 stack at M = 1 and the mixed 27B stack
+    at M = 32 (the tcgen05 band); other workloads carry no secondary record unless asked."""
+    import bench
+    args = bench.parse_args([])
+    assert bench.secondary_workloads(args) == ["nvfp4_27b_m1", "mixed_27b_m32"]
+    assert all(w in bench.WORKLOADS for w in bench.secondary_workloads(args))
+    assert bench.secondary_workloads(bench.parse_args(["--workload", "nvfp4_27b_m8"])) == []
+    assert bench.secondary_workloads(bench.parse_args(["--secondary", "none"])) == []
+    assert bench.secondary_workloads(bench.parse_args(["--secondary", "mixed_27b_m16"])) == ["mixed_27b_m16"]
