@@ -4,8 +4,8 @@
 // QPN2 / QPN8 of "v100-skinny README", section "How QPN works": packed weights are
 // streamed once and decoded on chip into the operands of a tensor-core product
 // against fp16 activations, with fp32 accumulation. The page's Volta kernels decode
-// into mma registers lane by lane; here the product is tcgen05.mma issued by one
-// thread per CTA, so the warps only decode:
+// into mma registers lane by lane; here single threads issue tcgen05.mma, so most
+// warps only decode:
 //  * A tile = 128 weight rows x K of one matrix (TMEM lane = weight row); B = the M
 //    activation rows, padded with zero rows to N = 16 ceil(M / 16) <= 96; D (fp32,
 //    128 x N) accumulates over all of K in tensor memory. The whole activation
@@ -13,25 +13,30 @@
 //    second pass over the weights and no chunking.
 //  * The decoded A operand lives in tensor memory too: a decode thread owns one
 //    weight row, which is one TMEM lane, and writes its fp16 pairs there with
-//    tcgen05.st; the MMA reads A from TMEM and only B from shared memory. Shared
-//    memory then holds the weight stages and activation slices alone, so more weight
-//    bytes are in flight (a weight stage took about 5 us from copy issue to arrival
-//    under full load here: the stream rate of a CTA is its bytes in flight / 5 us).
+//    tcgen05.st; the MMA reads A from TMEM and only B from shared memory, which then
+//    holds the weight stages and activation slices alone.
 //  * Exact decode, as in the mma.sync kernel: an E2M1 code times its E4M3 group
 //    scale is exact in fp16 (at most 6 significant bits, magnitude 2^-10 .. 2688),
 //    so the scale is folded into the fp16 weight; E4M3 to fp16 is exact; the
 //    per-tensor scale (NVFP4) or the row scale (FP8) multiplies the fp32 result.
-//  * Roles (warp specialisation): warp 0 streams, per K step, the codes (a 128-row
-//    box with the 128-byte swizzle) and the group scales with TMA into a ring of
-//    stages; warp 2 streams 64-k activation slices (a box with the 128-byte swizzle:
-//    the K-major B operand, rows past M zero-filled); warp 1 allocates tensor memory;
-//    warps 3..10 decode (two threads per weight row, each half of a 64-k A buffer in
-//    TMEM) and at the end of a tile read the accumulators back (tcgen05.ld) and store
-//    y; warps 11.. each have one thread that issues MMAs (4 per 64 k).
+//  * Roles (warp specialisation): warps 0..2 each have one thread that streams every
+//    third K step's codes (a 128-row box with the 128-byte swizzle) and group scales
+//    with TMA into its own slots of the weight ring (warp 1 also allocates tensor
+//    memory); warps 3..14, three groups of four, decode the 64-k quarters in turn (one
+//    weight row per thread, all 64 k of the quarter) and at the end of a tile read the
+//    accumulators back (tcgen05.ld) and store y; warps 15..18 each have one thread
+//    that streams its own 64-k activation slices (the K-major B operand, a box with
+//    the 128-byte swizzle, rows past M zero-filled) and issues four MMAs per quarter
+//    into its own accumulator. A single thread sustains only a few TMA copies per
+//    microsecond under load, hence the copies spread over seven threads.
+//  * Launches of few tiles split K over the CTAs of a cluster: each CTA leaves its
+//    partial sums in shared memory and the rank-0 CTA adds them in rank order through
+//    distributed shared memory.
 //  * Every mbarrier wait is bounded; a thread whose wait gives up flags the error
 //    word and the CTA's abort word and leaves its loop; all threads meet at the final
-//    barrier, the producer lets its copies land, the MMA thread waits for its
-//    products to complete and the tensor memory is released before the CTA exits.
+//    barrier (and both cluster barriers), the producers let their copies land, the
+//    issuing threads wait for their products and copies, and the tensor memory is
+//    released before the CTA exits.
 #include <algorithm>
 #include <numeric>
 #include <cstdio>
