@@ -191,6 +191,11 @@ QMV_API qmv_status qmv_q4_k_q8_1_fused_group(int count, const void *const *w, co
  *   over a thread-block cluster when the tiles leave half the SMs idle), x 16-byte
  *   aligned and scales_e4m3 16-byte aligned; otherwise balanced chunks of at most 16
  *   rows, one launch and one weight pass each.
+ *   Resources of the tcgen05 path: one CTA per SM holding all 512 tensor-memory
+ *   columns (a CTA of another kernel on the same SM that also allocates tensor memory
+ *   waits for it), and, when K is split, a launch of thread-block clusters of 2..4
+ *   CTAs. It allocates no global memory; the partial sums of a split stay in shared
+ *   memory.
  */
 QMV_API qmv_status qgemm_nvfp4_w4a16(const uint8_t *codes, const uint8_t *scales_e4m3, float global_scale,
                              const uint16_t *x, float *y, int M, int64_t N, int64_t K,
