@@ -542,15 +542,27 @@ def run_ours(args, rank, world, local_rank):
         line["secondary"] = []
         for wl in second:
             sargs = argparse.Namespace(**{**vars(args), "workload": wl, "steps": min(args.steps, 300)})
-            st2 = Stack(wl, dev, seed=1234 + rank, fused=q4_fused(sargs), grouped=not args.serial)
-            with torch.cuda.stream(stream):
-                rec = _run_ours_on_stream(sargs, rank, world, local_rank, st2, stream, barrier, max_over_ranks,
-                                          secondary=True)
+            try:
+                st2 = Stack(wl, dev, seed=1234 + rank, fused=q4_fused(sargs), grouped=not args.serial)
+                with torch.cuda.stream(stream):
+                    rec = _run_ours_on_stream(sargs, rank, world, local_rank, st2, stream, barrier,
+                                              max_over_ranks, secondary=True)
+                del st2
+            except Exception as exc:   # the main record stands; this one reports its failure
+                rec = secondary_error(wl, exc)
             line["secondary"].append(rec)
-            del st2
             torch.cuda.empty_cache()
     dist.close()
     return line if rank == 0 else None
+
+
+def secondary_error(workload, exc):
+    """The record of a secondary workload that raised: its name and the error. The main
+    record was measured before it and stands; this record carries no measurement and no
+    parity verdict (a wrong result is still fatal: only a measured violation fails the
+    run)."""
+    return {"config": {"workload": workload}, "error": f"{type(exc).__name__}: {str(exc)[:300]}",
+            "parity": {"ok": None, "error": "not measured"}}
 
 
 def secondary_workloads(args):

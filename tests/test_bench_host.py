@@ -169,3 +169,13 @@ def test_secondary_records_beside_the_default_workload():
     assert bench.secondary_workloads(bench.parse_args(["--workload", "nvfp4_27b_m8"])) == []
     assert bench.secondary_workloads(bench.parse_args(["--secondary", "none"])) == []
     assert bench.secondary_workloads(bench.parse_args(["--secondary", "mixed_27b_m16"])) == ["mixed_27b_m16"]
+
+
+def test_secondary_error_record_keeps_the_line():
+    """A secondary workload that raises leaves an error record beside the main record,
+    with no parity verdict (only a measured violation fails the run)."""
+    import bench
+    rec = bench.secondary_error("mixed_27b_m32", RuntimeError("CUDA error: out of memory"))
+    assert rec["config"]["workload"] == "mixed_27b_m32"
+    assert rec["error"].startswith("RuntimeError: CUDA error")
+    assert rec["parity"]["ok"] is None and "value" not in rec
