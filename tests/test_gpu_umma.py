@@ -146,6 +146,10 @@ def test_zero_scales_and_unit_codes(q):
 
 @pytest.mark.parametrize("M", [1, 9, 40])
 def test_groups(q, M):
+    """A group of 136 + 40 + 1 + 8 = 185 tiles on 152 CTAs: 33 CTAs take a second tile.
+    At M = 40 the plan has T = 3 issuing threads and 80 quarters per tile, not a
+    multiple of 3, so a tile's first A buffers change issuing thread at the boundary
+    (ordered by the wait for the previous tile's read-back)."""
     synth = _synth()
     K = 5120
     Ns = [17408, 5120, 37, 1000]
