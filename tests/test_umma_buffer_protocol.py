@@ -91,7 +91,7 @@ def test_weaker_rules_can_pass_a_stale_phase(T, Q):
     assert any(simulate(3, T, Q, quarters=240, seed=seed) for seed in range(200)), (T, Q)
 
 
-def simulate_kernel(G, T, Q, n_q, nsteps, nt, S, seed, issuer_waits_readback=True):
+def simulate_kernel(G, T, Q, n_q, nsteps, nt, S, seed, issuer_waits_readback=True, readback_lag=1):
     """The same handoff with the rest of the kernel around it: the weight ring (three
     producers, S stages, every decode group taking and releasing every K step), tiles
     of nsteps K steps (tq = nsteps * n_q quarters), the read-back at the end of each
@@ -99,8 +99,9 @@ def simulate_kernel(G, T, Q, n_q, nsteps, nt, S, seed, issuer_waits_readback=Tru
     thread t taking the quarters kq = t, t + T, ... of each tile -- so across a tile
     boundary a buffer can change hands when tq is not a multiple of T. Before its first
     quarter of tile lt >= 1 a thread waits for the read-back of tile lt - 1 (the kernel's
-    acc_free); `issuer_waits_readback=False` drops that wait (a plausible mistake).
-    Returns (stale passes, deadlocked)."""
+    acc_free); `issuer_waits_readback=False` drops that wait and `readback_lag=0` waits
+    for the tile's own read-back instead (plausible mistakes). Returns (stale passes,
+    deadlocked)."""
     rng = random.Random(seed)
     tq = nsteps * n_q
     steps_total = nt * nsteps
@@ -160,7 +161,7 @@ def simulate_kernel(G, T, Q, n_q, nsteps, nt, S, seed, issuer_waits_readback=Tru
         h = iss[t][iss_pos[t]]
         lt = h // tq
         first_of_tile = iss_pos[t] == 0 or iss[t][iss_pos[t] - 1] // tq != lt
-        if issuer_waits_readback and first_of_tile and lt >= 1 and readback[lt - 1] < G:
+        if issuer_waits_readback and first_of_tile and lt >= readback_lag and readback[lt - readback_lag] < G:
             return False
         j, k = h % Q, h // Q
         if (full[j] & 1) == (k & 1):
@@ -218,3 +219,9 @@ def test_readback_wait_keeps_tile_boundaries_safe(n_q, T, Q, nsteps):
     assert (n_q * nsteps) % T and Q == planner_buffers(3, T, Q)
     assert any(simulate_kernel(3, T, Q, n_q, nsteps, nt=3, S=12, seed=seed,
                                issuer_waits_readback=False)[0] for seed in range(300))
+
+
+def test_model_reports_a_deadlock():
+    """The deadlock check is live: a thread that waits for its own tile's read-back
+    (which needs that thread's products) stops the model."""
+    assert simulate_kernel(3, 4, 12, 4, 5, nt=2, S=6, seed=0, readback_lag=0) == (0, True)
